@@ -1,0 +1,160 @@
+/*
+ * moe_gb300.h — C ABI of the GB300 (sm_103a) fused Mixture-of-Experts layer.
+ *
+ * Source of the operation: "Amazon SageMaker AI 上的 Mixture-of-Experts 内核工程
+ * 优化" (English original page).  Its Introduction defines the fused MoE layer
+ * as token routing, data shuffling and the expert network computation merged
+ * into one batched GPU operation; its section "Backend routing for FP8 tensor
+ * quantization" adds FP8 tensor scaling and expert aggregation to the same
+ * single pass; its section "Swap-AB for WGMMA utilization" (with the digest
+ * page's formula B^T[N,K] x A^T[K,M] -> C^T[N,M]) gives the operand swap that
+ * puts the large expert dimension in the MMA's M slot when few tokens reach an
+ * expert.  The pages leave the router, the expert MLP and the scale granularity
+ * open; this library reads them as:
+ *   router   softmax over E fp32 logits, top-k on the raw logits with ties to
+ *            the lower expert index, optional renormalisation of the k weights;
+ *   expert   SwiGLU: w13 rows [0,I) gate, [I,2I) up; h = SiLU(gate) * up;
+ *            y = w2 h; no bias;
+ *   FP8      E4M3 weights with one fp32 scale per expert per tensor; dynamic
+ *            per-tensor E4M3 activations, s = amax / 448 (1 if amax is 0),
+ *            code = E4M3_rne_satfinite(fp32(v) / s);
+ *   combine  out[t] = sum_j w[t,j] * y[t,j], accumulated in fp32, stored bf16.
+ *
+ * Conventions for every entry point:
+ *   - Tensor pointers are DEVICE pointers owned by the caller, contiguous,
+ *     row-major, 16-byte aligned.  The library allocates nothing and keeps no
+ *     state between calls other than lazily cached per-device properties.
+ *   - Work is enqueued asynchronously on `stream` (a cudaStream_t; NULL is the
+ *     legacy default stream).  Nothing synchronises the host.
+ *   - Argument errors are detected on the host before anything is enqueued and
+ *     are returned synchronously with no side effect.  CUDA launch errors
+ *     return MOE_ERR_CUDA.  Device-side faults of the schedule (a bounded wait
+ *     that ran out, an out-of-range expert id) are recorded in the workspace's
+ *     status word; moe_check_status() reads it.
+ *   - All sizes are runtime values: one binary serves every shape (no per-shape
+ *     compilation).
+ */
+#ifndef MOE_GB300_H
+#define MOE_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t. */
+typedef struct CUstream_st* moe_stream_t;
+
+typedef enum {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARG = 1,    /* null pointer, bad size, k > E, misalignment ... */
+  MOE_ERR_UNSUPPORTED = 2,    /* shape outside what the kernels tile (H or I % 128) */
+  MOE_ERR_WORKSPACE = 3,      /* workspace missing or smaller than required */
+  MOE_ERR_CUDA = 4,           /* a CUDA runtime/driver call or launch failed */
+  MOE_ERR_DEVICE_TIMEOUT = 5, /* a bounded device-side wait ran out (status word) */
+  MOE_ERR_DEVICE_RANGE = 6    /* a device kernel met an out-of-range expert id */
+} moe_status_t;
+
+typedef enum { MOE_DT_BF16 = 0, MOE_DT_FP8_E4M3 = 1 } moe_dtype_t;
+
+/*
+ * Router (token routing, page Introduction).
+ *   logits   fp32 [T, E]
+ *   topk_ids int32 [T, top_k]  out: selected experts, slot order = (logit desc, index asc)
+ *   topk_w   fp32 [T, top_k]   out: softmax probability of each selected expert,
+ *                              divided by the sum over the k selected when renormalize != 0
+ * Requires 1 <= top_k <= E <= 1024, T >= 0 (T == 0 enqueues nothing), finite logits.
+ */
+moe_status_t moe_route_topk(const float* logits, int T, int E, int top_k, int renormalize,
+                            int32_t* topk_ids, float* topk_w, moe_stream_t stream);
+
+/*
+ * Alignment by expert (data shuffling, page Introduction; the "fragmented
+ * token arrays" of section "Backend routing for FP8 tensor quantization").
+ * Pair p = t*top_k + j goes to expert topk_ids[p].
+ *   counts      int32 [E]      out: pairs per expert
+ *   offsets     int32 [E+1]    out: exclusive prefix sum of counts rounded up to block_m
+ *   sorted_ids  int32 [T*top_k + E*(block_m-1)]
+ *                              out: per expert segment, its pair ids ascending, then the
+ *                              sentinel T*top_k up to the padded size; entries past
+ *                              offsets[E] are left untouched
+ *   tile_expert int32 [(T*top_k + E*(block_m-1)) / block_m]
+ *                              out: owning expert of each block_m-row block (may be NULL)
+ *   num_padded  int32 [1]      out: offsets[E]
+ * Requires 1 <= E <= 1024, 1 <= block_m <= 256, T*top_k < 2^31 - E*block_m.
+ * Ids outside [0, E) are skipped (not placed, not counted).
+ */
+moe_status_t moe_align_by_expert(const int32_t* topk_ids, int T, int top_k, int E, int block_m,
+                                 int32_t* counts, int32_t* offsets, int32_t* sorted_ids,
+                                 int32_t* tile_expert, int32_t* num_padded, moe_stream_t stream);
+
+/*
+ * Dynamic per-tensor activation quantisation (FP8 tensor scaling, section
+ * "Backend routing for FP8 tensor quantization").
+ *   x      bf16 [T, H]
+ *   x_q    uint8 [T, H]  out: E4M3 codes of fp32(x) / s
+ *   scale  fp32 [1]      out: s = amax|x| / 448 (1 when x is all zero)
+ * Requires H % 16 == 0.  `scratch` is a caller buffer of at least
+ * moe_quantize_scratch_size(T, H) bytes.
+ */
+size_t moe_quantize_scratch_size(int T, int H);
+moe_status_t moe_quantize_e4m3(const void* x, int T, int H, uint8_t* x_q, float* scale,
+                               void* scratch, size_t scratch_bytes, moe_stream_t stream);
+
+/* Arguments of the fused layer forward. */
+typedef struct {
+  const void* x;             /* bf16 [T, H] */
+  const float* router_logits;/* fp32 [T, E] */
+  const void* w13;           /* [E, 2I, H]: gate rows then up rows, H contiguous.
+                                E4M3 codes (FP8) or bf16 */
+  const void* w2;            /* [E, H, I], I contiguous; same element type as w13 */
+  const float* w13_scale;    /* fp32 [E]; required for FP8, must be NULL for BF16 */
+  const float* w2_scale;     /* fp32 [E]; required for FP8, must be NULL for BF16 */
+  moe_dtype_t weight_dtype;
+  int T, H, I, E, top_k, renormalize;
+  void* out;                 /* bf16 [T, H] */
+  int32_t* topk_ids_out;     /* optional int32 [T, top_k] (NULL: not returned) */
+  float* topk_w_out;         /* optional fp32 [T, top_k] */
+  int32_t* counts_out;       /* optional int32 [E]: pairs routed to each expert */
+  int debug_flags;           /* 0 in normal use; see MOE_DEBUG_* */
+} moe_fused_args;
+
+/* Test hook: make the expert-GEMM kernels' MMA warp wait on a barrier that
+ * nothing ever arrives on, so the bounded wait runs out (about
+ * MOE_DEBUG_TIMEOUT_MS) and the call reports MOE_ERR_DEVICE_TIMEOUT through
+ * moe_check_status() while the CUDA context stays usable. */
+#define MOE_DEBUG_FORCE_TIMEOUT 0x1
+#define MOE_DEBUG_TIMEOUT_MS 200
+
+/* Workspace bytes moe_fused_forward needs for these sizes (0 if invalid). */
+size_t moe_fused_workspace_size(int T, int H, int I, int E, int top_k, moe_dtype_t dtype);
+
+/*
+ * Fused MoE layer forward: routing -> alignment by expert -> grouped gate/up
+ * GEMM with the SiLU*up epilogue -> grouped down GEMM with the top-k weighted
+ * combine, FP8-scaled when weight_dtype is MOE_DT_FP8_E4M3 (page Introduction;
+ * sections "Backend routing for FP8 tensor quantization" and "Swap-AB for
+ * WGMMA utilization").
+ * Requires 1 <= top_k <= E <= 1024, H % 128 == 0, I % 128 == 0, T >= 0,
+ * a device of compute capability 10.3, workspace of moe_fused_workspace_size()
+ * bytes (256-byte aligned) that no other in-flight call uses.
+ * T == 0 returns MOE_OK and enqueues nothing.
+ */
+moe_status_t moe_fused_forward(const moe_fused_args* args, void* workspace, size_t workspace_bytes,
+                               moe_stream_t stream);
+
+/* Synchronises `stream`, reads the status word that the last call using
+ * `workspace` left there, and returns MOE_OK, MOE_ERR_DEVICE_TIMEOUT or
+ * MOE_ERR_DEVICE_RANGE (MOE_ERR_CUDA if the synchronisation itself failed). */
+moe_status_t moe_check_status(const void* workspace, moe_stream_t stream);
+
+/* Static description of a status code. */
+const char* moe_status_string(moe_status_t status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_GB300_H */

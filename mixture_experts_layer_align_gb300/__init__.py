@@ -1,0 +1,242 @@
+"""GB300 (sm_103a) fused Mixture-of-Experts layer forward.
+
+Thin Python binding over the C ABI in include/moe_gb300.h
+(libmoe_gb300.so, built in-tree by `build.py`).  Functions keep the C names
+and only marshal arguments: tensors become device pointers, the current torch
+stream becomes the cudaStream_t, outputs and workspaces are allocated with
+torch.  Every step of the layer runs in the library's CUDA kernels; there is
+no fallback path, and a missing library raises immediately.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libmoe_gb300.so")
+
+MOE_OK = 0
+MOE_DT_BF16 = 0
+MOE_DT_FP8_E4M3 = 1
+MOE_DEBUG_FORCE_TIMEOUT = 0x1
+STATUS_NAMES = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED",
+                3: "MOE_ERR_WORKSPACE", 4: "MOE_ERR_CUDA", 5: "MOE_ERR_DEVICE_TIMEOUT",
+                6: "MOE_ERR_DEVICE_RANGE"}
+
+_lock = threading.Lock()
+_lib = None
+
+
+class MoeError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {STATUS_NAMES.get(status, status)} ({status_string(status)})")
+
+
+class MoeFusedArgs(ctypes.Structure):
+    _fields_ = [
+        ("x", ctypes.c_void_p),
+        ("router_logits", ctypes.c_void_p),
+        ("w13", ctypes.c_void_p),
+        ("w2", ctypes.c_void_p),
+        ("w13_scale", ctypes.c_void_p),
+        ("w2_scale", ctypes.c_void_p),
+        ("weight_dtype", ctypes.c_int),
+        ("T", ctypes.c_int),
+        ("H", ctypes.c_int),
+        ("I", ctypes.c_int),
+        ("E", ctypes.c_int),
+        ("top_k", ctypes.c_int),
+        ("renormalize", ctypes.c_int),
+        ("out", ctypes.c_void_p),
+        ("topk_ids_out", ctypes.c_void_p),
+        ("topk_w_out", ctypes.c_void_p),
+        ("counts_out", ctypes.c_void_p),
+        ("debug_flags", ctypes.c_int),
+    ]
+
+
+def load():
+    """Load libmoe_gb300.so (raises if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} is missing: build it with "
+                               "`python -m mixture_experts_layer_align_gb300.build`")
+        L = ctypes.CDLL(LIB_PATH)
+        P, i, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
+        L.moe_route_topk.argtypes = [P, i, i, i, i, P, P, P]
+        L.moe_align_by_expert.argtypes = [P, i, i, i, i, P, P, P, P, P, P]
+        L.moe_quantize_scratch_size.argtypes = [i, i]
+        L.moe_quantize_scratch_size.restype = sz
+        L.moe_quantize_e4m3.argtypes = [P, i, i, P, P, P, sz, P]
+        L.moe_fused_workspace_size.argtypes = [i, i, i, i, i, i]
+        L.moe_fused_workspace_size.restype = sz
+        L.moe_fused_forward.argtypes = [ctypes.POINTER(MoeFusedArgs), P, sz, P]
+        L.moe_check_status.argtypes = [P, P]
+        L.moe_status_string.argtypes = [i]
+        L.moe_status_string.restype = ctypes.c_char_p
+        for name in ("moe_route_topk", "moe_align_by_expert", "moe_quantize_e4m3",
+                     "moe_fused_forward", "moe_check_status"):
+            getattr(L, name).restype = ctypes.c_int
+        _lib = L
+        return _lib
+
+
+def status_string(status: int) -> str:
+    return load().moe_status_string(int(status)).decode()
+
+
+def _check(status: int, where: str):
+    if status != MOE_OK:
+        raise MoeError(status, where)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _require(t, dtype, name, shape=None):
+    import torch
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+
+
+def moe_route_topk(logits, top_k: int, renormalize: bool, topk_ids=None, topk_w=None, stream=None):
+    """Router: softmax + top-k (+ renormalisation).  Returns (ids int32, w fp32), [T, k]."""
+    import torch
+    _require(logits, torch.float32, "logits")
+    T, E = logits.shape
+    if topk_ids is None:
+        topk_ids = torch.empty(T, top_k, dtype=torch.int32, device=logits.device)
+    if topk_w is None:
+        topk_w = torch.empty(T, top_k, dtype=torch.float32, device=logits.device)
+    _require(topk_ids, torch.int32, "topk_ids", (T, top_k))
+    _require(topk_w, torch.float32, "topk_w", (T, top_k))
+    _check(load().moe_route_topk(_ptr(logits), T, E, top_k, int(bool(renormalize)), _ptr(topk_ids),
+                                 _ptr(topk_w), _stream(stream)), "moe_route_topk")
+    return topk_ids, topk_w
+
+
+def moe_align_by_expert(topk_ids, E: int, block_m: int, stream=None):
+    """Alignment by expert.  Returns dict(counts, offsets, sorted_ids, tile_expert,
+    num_padded) as device tensors (sorted_ids / tile_expert at capacity size)."""
+    import torch
+    _require(topk_ids, torch.int32, "topk_ids")
+    T, k = topk_ids.shape
+    P = T * k
+    cap = P + E * (block_m - 1)
+    dev = topk_ids.device
+    counts = torch.empty(E, dtype=torch.int32, device=dev)
+    offsets = torch.empty(E + 1, dtype=torch.int32, device=dev)
+    sorted_ids = torch.full((max(cap, 1),), -1, dtype=torch.int32, device=dev)
+    tile_expert = torch.full((max(cap // block_m, 1),), -1, dtype=torch.int32, device=dev)
+    num_padded = torch.zeros(1, dtype=torch.int32, device=dev)
+    _check(load().moe_align_by_expert(_ptr(topk_ids), T, k, E, block_m, _ptr(counts),
+                                      _ptr(offsets), _ptr(sorted_ids), _ptr(tile_expert),
+                                      _ptr(num_padded), _stream(stream)), "moe_align_by_expert")
+    return dict(counts=counts, offsets=offsets, sorted_ids=sorted_ids, tile_expert=tile_expert,
+                num_padded=num_padded)
+
+
+def moe_quantize_e4m3(x, stream=None):
+    """Dynamic per-tensor E4M3 quantisation of bf16 x.  Returns (codes uint8, scale fp32[1])."""
+    import torch
+    _require(x, torch.bfloat16, "x")
+    T, H = x.shape
+    L = load()
+    xq = torch.empty(T, H, dtype=torch.uint8, device=x.device)
+    scale = torch.empty(1, dtype=torch.float32, device=x.device)
+    nscr = L.moe_quantize_scratch_size(T, H)
+    scratch = torch.empty(max(nscr, 16), dtype=torch.uint8, device=x.device)
+    _check(L.moe_quantize_e4m3(_ptr(x), T, H, _ptr(xq), _ptr(scale), _ptr(scratch), nscr,
+                               _stream(stream)), "moe_quantize_e4m3")
+    return xq, scale
+
+
+def moe_fused_workspace_size(T: int, H: int, I: int, E: int, top_k: int, dtype: int) -> int:
+    return int(load().moe_fused_workspace_size(T, H, I, E, top_k, dtype))
+
+
+def alloc_workspace(T, H, I, E, top_k, dtype, device="cuda"):
+    import torch
+    n = moe_fused_workspace_size(T, H, I, E, top_k, dtype)
+    if n == 0:
+        raise MoeError(1, "moe_fused_workspace_size")
+    return torch.empty(n, dtype=torch.uint8, device=device)
+
+
+def moe_fused_forward(x, router_logits, w13, w2, w13_scale, w2_scale, top_k: int,
+                      renormalize: bool = True, out=None, workspace=None, topk_ids_out=None,
+                      topk_w_out=None, counts_out=None, debug_flags: int = 0, stream=None):
+    """Fused MoE layer forward (see include/moe_gb300.h).
+
+    x bf16 [T,H]; router_logits fp32 [T,E]; w13 [E,2I,H] and w2 [E,H,I] as uint8
+    E4M3 codes (with fp32 [E] scales) or bf16 (scales None).  Returns out bf16 [T,H].
+    """
+    import torch
+    _require(x, torch.bfloat16, "x")
+    _require(router_logits, torch.float32, "router_logits")
+    T, H = x.shape
+    E = router_logits.shape[1]
+    fp8 = w13_scale is not None
+    wdt = torch.uint8 if fp8 else torch.bfloat16
+    _require(w13, wdt, "w13")
+    _require(w2, wdt, "w2")
+    I = w13.shape[1] // 2
+    if tuple(w13.shape) != (E, 2 * I, H) or tuple(w2.shape) != (E, H, I):
+        raise ValueError("w13 must be [E,2I,H] and w2 [E,H,I]")
+    if fp8:
+        _require(w13_scale, torch.float32, "w13_scale", (E,))
+        _require(w2_scale, torch.float32, "w2_scale", (E,))
+    dtype = MOE_DT_FP8_E4M3 if fp8 else MOE_DT_BF16
+    if out is None:
+        out = torch.empty(T, H, dtype=torch.bfloat16, device=x.device)
+    _require(out, torch.bfloat16, "out", (T, H))
+    if workspace is None:
+        workspace = alloc_workspace(T, H, I, E, top_k, dtype, x.device)
+    if topk_ids_out is not None:
+        _require(topk_ids_out, torch.int32, "topk_ids_out", (T, top_k))
+    if topk_w_out is not None:
+        _require(topk_w_out, torch.float32, "topk_w_out", (T, top_k))
+    if counts_out is not None:
+        _require(counts_out, torch.int32, "counts_out", (E,))
+    args = MoeFusedArgs(
+        x=x.data_ptr(), router_logits=router_logits.data_ptr(), w13=w13.data_ptr(),
+        w2=w2.data_ptr(), w13_scale=w13_scale.data_ptr() if fp8 else None,
+        w2_scale=w2_scale.data_ptr() if fp8 else None, weight_dtype=dtype, T=T, H=H, I=I, E=E,
+        top_k=top_k, renormalize=int(bool(renormalize)), out=out.data_ptr(),
+        topk_ids_out=topk_ids_out.data_ptr() if topk_ids_out is not None else None,
+        topk_w_out=topk_w_out.data_ptr() if topk_w_out is not None else None,
+        counts_out=counts_out.data_ptr() if counts_out is not None else None,
+        debug_flags=int(debug_flags))
+    _check(load().moe_fused_forward(ctypes.byref(args), _ptr(workspace), workspace.numel(),
+                                    _stream(stream)), "moe_fused_forward")
+    return out
+
+
+def moe_check_status(workspace, stream=None) -> int:
+    """Synchronise and return the device status word's verdict (0 = MOE_OK)."""
+    return int(load().moe_check_status(_ptr(workspace), _stream(stream)))
+
+
+__all__ = ["load", "moe_route_topk", "moe_align_by_expert", "moe_quantize_e4m3",
+           "moe_fused_workspace_size", "moe_fused_forward", "moe_check_status", "alloc_workspace",
+           "status_string", "MoeError", "MoeFusedArgs", "MOE_DT_BF16", "MOE_DT_FP8_E4M3",
+           "MOE_DEBUG_FORCE_TIMEOUT", "LIB_PATH"]

@@ -1,0 +1,110 @@
+// Internal (non-exported) declarations shared by the library's translation
+// units: the workspace control block, kernel parameter blocks and launchers.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "moe_gb300.h"
+
+namespace moe {
+
+// Status bits of Ctrl::err.
+constexpr int kDevErrTimeout = 1;
+constexpr int kDevErrRange = 2;
+
+// Rows of one alignment block inside the fused path: the tcgen05 MMA with
+// M = 128 takes N in multiples of 16, so each expert's token segment is
+// padded to 16 rows.
+constexpr int kAlignBlock = 16;
+
+// Per-call control words, at the start of the workspace.
+struct Ctrl {
+  int err;          // kDevErr* bits set by device code
+  unsigned amax_h;  // bits of max |h| (non-negative floats order like uints)
+  float s_x;        // activation scale of x
+  float s_h;        // activation scale of h
+  int num_padded;   // rows of the aligned (sorted, padded) pair list
+  int num_mtiles;   // entries of the GEMM row-tile list
+  int pad[10];
+};
+static_assert(sizeof(Ctrl) == 64, "Ctrl layout");
+
+// ------------------------------------------------------------ routing / align
+constexpr int kRouteWarps = 8;  // tokens per router CTA (one warp per token)
+
+cudaError_t launch_route_topk(const float* logits, int T, int E, int k, int renorm, int32_t* ids,
+                              float* wts, const __nv_bfloat16* x, int H, float* amax_partials,
+                              Ctrl* ctrl, cudaStream_t st);
+inline int route_grid(int T) { return (T + kRouteWarps - 1) / kRouteWarps; }
+
+struct AlignParams {
+  const int32_t* ids;
+  int P, E, bm, chunk;
+  int32_t* counts;
+  int32_t* offsets;
+  int32_t* sorted_ids;
+  int32_t* tile_expert;  // may be null
+  int32_t* num_padded;   // may be null
+  // fused-path extras (null when unused)
+  int4* mtiles;          // GEMM row tiles {expert, first row, rows, 0}
+  int bn_max;            // max rows of one row tile
+  Ctrl* ctrl;
+  const float* amax_partials;
+  int n_partials;
+};
+cudaError_t launch_align(const AlignParams& p, cudaStream_t st);
+int align_chunk();
+
+// Gather the routed rows of x into aligned order (E4M3 with s_x, or bf16), zero
+// the fp32 combine buffer.
+cudaError_t launch_gather_x(const __nv_bfloat16* x, int H, const int32_t* sorted_ids,
+                            const Ctrl* ctrl, int P, int k, void* xs, bool fp8, float* acc,
+                            long long acc_elems, int max_rows, int num_sms, cudaStream_t st);
+// h (bf16) -> E4M3 with s_h = amax_h / 448 (stored into ctrl->s_h).
+cudaError_t launch_quant_h(const __nv_bfloat16* h, int I, Ctrl* ctrl, uint8_t* hq, int max_rows,
+                           int num_sms, cudaStream_t st);
+// fp32 combine buffer -> bf16 output.
+cudaError_t launch_finalize(const float* acc, __nv_bfloat16* out, long long n, int num_sms,
+                            cudaStream_t st);
+// Standalone activation quantisation.
+cudaError_t launch_quantize_e4m3(const __nv_bfloat16* x, long long n, uint8_t* xq, float* scale,
+                                 float* partials, int n_partials, cudaStream_t st);
+
+// ------------------------------------------------------------ grouped GEMM
+struct GemmParams {
+  const int4* mtiles;
+  Ctrl* ctrl;
+  int nb_count;         // 128-row weight blocks per expert (I/128 or H/128)
+  int split_k;          // K slices per tile (down projection only)
+  int k_steps;          // K / (128 bytes of K)
+  int k_elems;          // elements of K per step: 128 (E4M3) or 64 (bf16)
+  int bn_max;           // max tokens (MMA N) per row tile
+  int stages;           // shared-memory pipeline depth
+  int acc_stride;       // TMEM columns per accumulator buffer
+  int num_acc;          // accumulator buffers (1 or 2)
+  int tmem_cols;        // allocated TMEM columns (power of two >= 32)
+  int rows_per_expert;  // 2I (gate/up) or H (down)
+  int up_offset;        // I: first up row inside an expert's w13 block
+  const int32_t* sorted_ids;
+  int P, top_k;
+  const float* w_scale;  // [E] per-expert weight scale (FP8) or null
+  int act_scale_sel;     // 1: s_x, 2: s_h (FP8); 0: none
+  const float* topk_w;   // [P]
+  __nv_bfloat16* h_out;  // gate/up: [rows, I] bf16
+  int ldh;
+  float* acc_out;        // down: [T, H] fp32
+  int ldo;
+  unsigned long long timeout_ns;
+  int debug;
+};
+
+constexpr int kGemmThreads = 192;  // warp 0 TMA, warp 1 MMA, warps 2..5 epilogue
+size_t gemm_smem_bytes(bool swiglu, int bn_max, int stages);
+int gemm_max_stages(bool swiglu, int bn_max);
+cudaError_t launch_gemm(bool bf16, bool swiglu, const GemmParams& p, const CUtensorMap& tma,
+                        const CUtensorMap& tmb, int grid, cudaStream_t st);
+
+}  // namespace moe

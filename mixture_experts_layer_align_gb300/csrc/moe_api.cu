@@ -1,0 +1,396 @@
+// C ABI of the fused MoE layer: argument checks, workspace layout, TMA
+// descriptors and the launch sequence.  Every step of the layer runs in this
+// library's kernels; the host only validates and enqueues.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+#include <stdint.h>
+
+#include <algorithm>
+#include <mutex>
+
+#include "internal.h"
+#include "moe_gb300.h"
+
+namespace moe {
+namespace {
+
+constexpr unsigned long long kWaitLimitNs = 5000000000ull;  // 5 s per bounded wait
+constexpr int kMaxExperts = 1024;
+
+size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+struct DeviceInfo {
+  int num_sms = 0;
+  int major = 0, minor = 0;
+};
+
+DeviceInfo device_info(int dev) {
+  static std::mutex mu;
+  static DeviceInfo cache[64];
+  static bool have[64] = {};
+  std::lock_guard<std::mutex> lock(mu);
+  if (dev < 0 || dev >= 64) return DeviceInfo{};
+  if (!have[dev]) {
+    DeviceInfo d;
+    cudaDeviceGetAttribute(&d.num_sms, cudaDevAttrMultiProcessorCount, dev);
+    cudaDeviceGetAttribute(&d.major, cudaDevAttrComputeCapabilityMajor, dev);
+    cudaDeviceGetAttribute(&d.minor, cudaDevAttrComputeCapabilityMinor, dev);
+    cache[dev] = d;
+    have[dev] = true;
+  }
+  return cache[dev];
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// 2-D K-major tile map: rows of `row_bytes`, boxes of (128 bytes of K) x box_rows,
+// written to shared memory with the 128-byte swizzle the UMMA descriptors expect.
+bool make_tmap(CUtensorMap* m, const void* base, bool bf16, uint64_t k_elems, uint64_t rows,
+               uint32_t box_rows) {
+  auto enc = tensor_map_encoder();
+  if (!enc) return false;
+  const uint64_t esize = bf16 ? 2 : 1;
+  cuuint64_t dims[2] = {k_elems, rows};
+  cuuint64_t strides[1] = {k_elems * esize};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(128 / esize), box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = enc(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8, 2,
+                   const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+// Workspace layout of the fused forward (all regions 256-byte aligned).
+struct Layout {
+  long long P = 0;
+  int pad_max = 0;     // upper bound of aligned rows: P + E*(16-1)
+  int max_mtiles = 0;  // upper bound of GEMM row tiles
+  int n_partials = 0;  // router CTAs
+  size_t ctrl = 0, partials = 0, ids = 0, wts = 0, counts = 0, offsets = 0, sorted = 0,
+         mtiles = 0, xs = 0, h = 0, hq = 0, acc = 0, total = 0;
+};
+
+Layout make_layout(int T, int H, int I, int E, int k, bool fp8) {
+  Layout L;
+  L.P = static_cast<long long>(T) * k;
+  L.pad_max = static_cast<int>(L.P + static_cast<long long>(E) * (kAlignBlock - 1));
+  L.max_mtiles = L.pad_max / kAlignBlock + 1;
+  L.n_partials = route_grid(T);
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    const size_t at = off;
+    off = align_up(off + bytes, 256);
+    return at;
+  };
+  L.ctrl = take(sizeof(Ctrl));
+  L.partials = take(sizeof(float) * std::max(L.n_partials, 1));
+  L.ids = take(sizeof(int32_t) * L.P);
+  L.wts = take(sizeof(float) * L.P);
+  L.counts = take(sizeof(int32_t) * E);
+  L.offsets = take(sizeof(int32_t) * (E + 1));
+  L.sorted = take(sizeof(int32_t) * L.pad_max);
+  L.mtiles = take(sizeof(int4) * L.max_mtiles);
+  L.xs = take(static_cast<size_t>(L.pad_max) * H * (fp8 ? 1 : 2));
+  L.h = take(static_cast<size_t>(L.pad_max) * I * 2);
+  L.hq = take(fp8 ? static_cast<size_t>(L.pad_max) * I : 0);
+  L.acc = take(static_cast<size_t>(T) * H * sizeof(float));
+  L.total = off;
+  return L;
+}
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+int next_pow2(int v) {
+  int p = 32;
+  while (p < v) p <<= 1;
+  return p;
+}
+
+int round_up16(long long v) { return static_cast<int>((v + 15) / 16 * 16); }
+
+moe_status_t check_device(DeviceInfo* out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return MOE_ERR_CUDA;
+  DeviceInfo d = device_info(dev);
+  if (d.major != 10 || d.minor != 3) return MOE_ERR_UNSUPPORTED;
+  *out = d;
+  return MOE_OK;
+}
+
+}  // namespace
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" {
+
+const char* moe_status_string(moe_status_t s) {
+  switch (s) {
+    case MOE_OK: return "ok";
+    case MOE_ERR_INVALID_ARG: return "invalid argument";
+    case MOE_ERR_UNSUPPORTED: return "unsupported shape or device";
+    case MOE_ERR_WORKSPACE: return "workspace missing or too small";
+    case MOE_ERR_CUDA: return "CUDA error";
+    case MOE_ERR_DEVICE_TIMEOUT: return "device-side wait timed out";
+    case MOE_ERR_DEVICE_RANGE: return "device kernel met an out-of-range expert id";
+  }
+  return "unknown status";
+}
+
+moe_status_t moe_route_topk(const float* logits, int T, int E, int top_k, int renormalize,
+                            int32_t* topk_ids, float* topk_w, moe_stream_t stream) {
+  if (T < 0 || E < 1 || E > kMaxExperts || top_k < 1 || top_k > E) return MOE_ERR_INVALID_ARG;
+  if (T == 0) return MOE_OK;
+  if (!logits || !topk_ids || !topk_w) return MOE_ERR_INVALID_ARG;
+  if (!aligned(logits, 4) || !aligned(topk_ids, 4) || !aligned(topk_w, 4))
+    return MOE_ERR_INVALID_ARG;
+  DeviceInfo d;
+  moe_status_t s = check_device(&d);
+  if (s != MOE_OK) return s;
+  return launch_route_topk(logits, T, E, top_k, renormalize, topk_ids, topk_w, nullptr, 0,
+                           nullptr, nullptr, stream) == cudaSuccess
+             ? MOE_OK
+             : MOE_ERR_CUDA;
+}
+
+moe_status_t moe_align_by_expert(const int32_t* topk_ids, int T, int top_k, int E, int block_m,
+                                 int32_t* counts, int32_t* offsets, int32_t* sorted_ids,
+                                 int32_t* tile_expert, int32_t* num_padded, moe_stream_t stream) {
+  if (T < 0 || top_k < 1 || E < 1 || E > kMaxExperts || block_m < 1 || block_m > 256)
+    return MOE_ERR_INVALID_ARG;
+  const long long P = static_cast<long long>(T) * top_k;
+  if (P + static_cast<long long>(E) * block_m >= (1ll << 31)) return MOE_ERR_INVALID_ARG;
+  if (!topk_ids && P > 0) return MOE_ERR_INVALID_ARG;
+  if (!counts || !offsets || !sorted_ids) return MOE_ERR_INVALID_ARG;
+  DeviceInfo d;
+  moe_status_t s = check_device(&d);
+  if (s != MOE_OK) return s;
+  AlignParams p{};
+  p.ids = topk_ids;
+  p.P = static_cast<int>(P);
+  p.E = E;
+  p.bm = block_m;
+  p.chunk = align_chunk();
+  p.counts = counts;
+  p.offsets = offsets;
+  p.sorted_ids = sorted_ids;
+  p.tile_expert = tile_expert;
+  p.num_padded = num_padded;
+  return launch_align(p, stream) == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+size_t moe_quantize_scratch_size(int T, int H) {
+  (void)T;
+  (void)H;
+  return 1024 * sizeof(float);
+}
+
+moe_status_t moe_quantize_e4m3(const void* x, int T, int H, uint8_t* x_q, float* scale,
+                               void* scratch, size_t scratch_bytes, moe_stream_t stream) {
+  if (T < 0 || H < 16 || H % 16 != 0) return MOE_ERR_INVALID_ARG;
+  if (T == 0) return MOE_OK;
+  if (!x || !x_q || !scale || !aligned(x, 16) || !aligned(x_q, 16) || !aligned(scale, 4))
+    return MOE_ERR_INVALID_ARG;
+  if (!scratch || !aligned(scratch, 4) || scratch_bytes < moe_quantize_scratch_size(T, H))
+    return MOE_ERR_WORKSPACE;
+  DeviceInfo d;
+  moe_status_t s = check_device(&d);
+  if (s != MOE_OK) return s;
+  const long long n = static_cast<long long>(T) * H;
+  int parts = std::min(1024, std::max(1, d.num_sms * 4));
+  parts = static_cast<int>(std::min<long long>(parts, (n / 8 + 255) / 256));
+  if (parts < 1) parts = 1;
+  return launch_quantize_e4m3(static_cast<const __nv_bfloat16*>(x), n, x_q, scale,
+                              static_cast<float*>(scratch), parts, stream) == cudaSuccess
+             ? MOE_OK
+             : MOE_ERR_CUDA;
+}
+
+size_t moe_fused_workspace_size(int T, int H, int I, int E, int top_k, moe_dtype_t dtype) {
+  if (T < 0 || H <= 0 || I <= 0 || E < 1 || E > kMaxExperts || top_k < 1 || top_k > E) return 0;
+  if (dtype != MOE_DT_BF16 && dtype != MOE_DT_FP8_E4M3) return 0;
+  return make_layout(T, H, I, E, top_k, dtype == MOE_DT_FP8_E4M3).total;
+}
+
+moe_status_t moe_fused_forward(const moe_fused_args* a, void* workspace, size_t workspace_bytes,
+                               moe_stream_t stream) {
+  if (!a) return MOE_ERR_INVALID_ARG;
+  const int T = a->T, H = a->H, I = a->I, E = a->E, k = a->top_k;
+  if (T < 0 || H <= 0 || I <= 0 || E < 1 || E > kMaxExperts || k < 1 || k > E)
+    return MOE_ERR_INVALID_ARG;
+  if (a->weight_dtype != MOE_DT_BF16 && a->weight_dtype != MOE_DT_FP8_E4M3)
+    return MOE_ERR_INVALID_ARG;
+  const bool fp8 = a->weight_dtype == MOE_DT_FP8_E4M3;
+  if (fp8 && (!a->w13_scale || !a->w2_scale)) return MOE_ERR_INVALID_ARG;
+  if (!fp8 && (a->w13_scale || a->w2_scale)) return MOE_ERR_INVALID_ARG;
+  if (H % 128 != 0 || I % 128 != 0) return MOE_ERR_UNSUPPORTED;
+  const long long P = static_cast<long long>(T) * k;
+  if (P + static_cast<long long>(E) * kAlignBlock >= (1ll << 31) / 2) return MOE_ERR_UNSUPPORTED;
+  if (T == 0) return MOE_OK;
+  if (!a->x || !a->router_logits || !a->w13 || !a->w2 || !a->out) return MOE_ERR_INVALID_ARG;
+  if (!aligned(a->x, 16) || !aligned(a->w13, 16) || !aligned(a->w2, 16) || !aligned(a->out, 16) ||
+      !aligned(a->router_logits, 4) || (a->w13_scale && !aligned(a->w13_scale, 4)) ||
+      (a->w2_scale && !aligned(a->w2_scale, 4)) ||
+      (a->topk_ids_out && !aligned(a->topk_ids_out, 4)) ||
+      (a->topk_w_out && !aligned(a->topk_w_out, 4)) ||
+      (a->counts_out && !aligned(a->counts_out, 4)))
+    return MOE_ERR_INVALID_ARG;
+  const Layout L = make_layout(T, H, I, E, k, fp8);
+  if (!workspace || !aligned(workspace, 256) || workspace_bytes < L.total) return MOE_ERR_WORKSPACE;
+  DeviceInfo dev;
+  moe_status_t st = check_device(&dev);
+  if (st != MOE_OK) return st;
+
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  Ctrl* ctrl = reinterpret_cast<Ctrl*>(ws + L.ctrl);
+  float* partials = reinterpret_cast<float*>(ws + L.partials);
+  int32_t* ids = a->topk_ids_out ? a->topk_ids_out : reinterpret_cast<int32_t*>(ws + L.ids);
+  float* wts = a->topk_w_out ? a->topk_w_out : reinterpret_cast<float*>(ws + L.wts);
+  int32_t* counts = a->counts_out ? a->counts_out : reinterpret_cast<int32_t*>(ws + L.counts);
+  int32_t* offsets = reinterpret_cast<int32_t*>(ws + L.offsets);
+  int32_t* sorted = reinterpret_cast<int32_t*>(ws + L.sorted);
+  int4* mtiles = reinterpret_cast<int4*>(ws + L.mtiles);
+  void* xs = ws + L.xs;
+  __nv_bfloat16* h = reinterpret_cast<__nv_bfloat16*>(ws + L.h);
+  uint8_t* hq = ws + L.hq;
+  float* acc = reinterpret_cast<float*>(ws + L.acc);
+
+  // Row-tile width: twice the mean rows per touched expert, 64..256 (any
+  // value is correct; larger tiles re-read each weight block fewer times).
+  const long long touched = std::min<long long>(E, P);
+  const long long mean_rows = (P + touched - 1) / touched;
+  const int bn_max = std::min(256, std::max(64, round_up16(2 * mean_rows)));
+
+  // 1. routing (+ per-CTA amax of x, + reset of the control words)
+  cudaStream_t s = stream;
+  if (launch_route_topk(a->router_logits, T, E, k, a->renormalize, ids, wts,
+                        static_cast<const __nv_bfloat16*>(a->x), H, fp8 ? partials : nullptr, ctrl,
+                        s) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  // 2. alignment by expert, GEMM row tiles, s_x
+  AlignParams ap{};
+  ap.ids = ids;
+  ap.P = static_cast<int>(P);
+  ap.E = E;
+  ap.bm = kAlignBlock;
+  ap.chunk = align_chunk();
+  ap.counts = counts;
+  ap.offsets = offsets;
+  ap.sorted_ids = sorted;
+  ap.tile_expert = nullptr;
+  ap.num_padded = nullptr;
+  ap.mtiles = mtiles;
+  ap.bn_max = bn_max;
+  ap.ctrl = ctrl;
+  ap.amax_partials = fp8 ? partials : nullptr;
+  ap.n_partials = fp8 ? L.n_partials : 0;
+  if (launch_align(ap, s) != cudaSuccess) return MOE_ERR_CUDA;
+  // 3. gather (+ quantise) the routed rows of x; zero the combine buffer
+  if (launch_gather_x(static_cast<const __nv_bfloat16*>(a->x), H, sorted, ctrl, static_cast<int>(P),
+                      k, xs, fp8, acc, static_cast<long long>(T) * H, L.pad_max, dev.num_sms,
+                      s) != cudaSuccess)
+    return MOE_ERR_CUDA;
+
+  // TMA descriptors
+  CUtensorMap tm_w13, tm_xs, tm_w2, tm_h;
+  const bool bf16 = !fp8;
+  if (!make_tmap(&tm_w13, a->w13, bf16, H, static_cast<uint64_t>(E) * 2 * I, 128) ||
+      !make_tmap(&tm_xs, xs, bf16, H, L.pad_max, 16) ||
+      !make_tmap(&tm_w2, a->w2, bf16, I, static_cast<uint64_t>(E) * H, 128) ||
+      !make_tmap(&tm_h, fp8 ? static_cast<const void*>(hq) : static_cast<const void*>(h), bf16, I,
+                 L.pad_max, 16))
+    return MOE_ERR_CUDA;
+
+  const int k_elems = fp8 ? 128 : 64;
+  const long long max_tiles = std::min<long long>(L.max_mtiles, (L.pad_max + bn_max - 1) / bn_max + touched);
+
+  // 4. gate/up GEMM + SiLU*up epilogue
+  GemmParams g1{};
+  g1.mtiles = mtiles;
+  g1.ctrl = ctrl;
+  g1.nb_count = I / 128;
+  g1.split_k = 1;
+  g1.k_steps = H / k_elems;
+  g1.k_elems = k_elems;
+  g1.bn_max = bn_max;
+  g1.stages = gemm_max_stages(true, bn_max);
+  g1.acc_stride = 2 * bn_max;
+  g1.num_acc = (4 * bn_max <= 512) ? 2 : 1;
+  g1.tmem_cols = next_pow2(g1.acc_stride * g1.num_acc);
+  g1.rows_per_expert = 2 * I;
+  g1.up_offset = I;
+  g1.sorted_ids = sorted;
+  g1.P = static_cast<int>(P);
+  g1.top_k = k;
+  g1.w_scale = fp8 ? a->w13_scale : nullptr;
+  g1.act_scale_sel = fp8 ? 1 : 0;
+  g1.topk_w = wts;
+  g1.h_out = h;
+  g1.ldh = I;
+  g1.timeout_ns = (a->debug_flags & MOE_DEBUG_FORCE_TIMEOUT) ? MOE_DEBUG_TIMEOUT_MS * 1000000ull
+                                                             : kWaitLimitNs;
+  g1.debug = a->debug_flags;
+  const long long units1 = max_tiles * g1.nb_count;
+  const int grid1 = static_cast<int>(std::max<long long>(1, std::min<long long>(dev.num_sms, units1)));
+  if (launch_gemm(bf16, true, g1, tm_w13, tm_xs, grid1, s) != cudaSuccess) return MOE_ERR_CUDA;
+
+  // 5. dynamic scale of h and its E4M3 codes
+  if (fp8 && launch_quant_h(h, I, ctrl, hq, L.pad_max, dev.num_sms, s) != cudaSuccess)
+    return MOE_ERR_CUDA;
+
+  // 6. down GEMM + weighted scatter-combine (split over K when few units)
+  GemmParams g2 = g1;
+  g2.nb_count = H / 128;
+  g2.k_steps = I / k_elems;
+  g2.stages = gemm_max_stages(false, bn_max);
+  g2.acc_stride = bn_max;
+  g2.num_acc = 2;
+  g2.tmem_cols = next_pow2(2 * bn_max);
+  g2.rows_per_expert = H;
+  g2.up_offset = 0;
+  g2.w_scale = fp8 ? a->w2_scale : nullptr;
+  g2.act_scale_sel = fp8 ? 2 : 0;
+  g2.h_out = nullptr;
+  g2.acc_out = acc;
+  g2.ldo = H;
+  const long long base_units2 = touched * g2.nb_count;
+  int split = static_cast<int>((2LL * dev.num_sms + base_units2 - 1) / base_units2);
+  split = std::max(1, std::min({split, g2.k_steps, 16}));
+  g2.split_k = split;
+  const long long units2 = max_tiles * g2.nb_count * split;
+  const int grid2 = static_cast<int>(std::max<long long>(1, std::min<long long>(dev.num_sms, units2)));
+  if (launch_gemm(bf16, false, g2, tm_w2, tm_h, grid2, s) != cudaSuccess) return MOE_ERR_CUDA;
+
+  // 7. fp32 combine buffer -> bf16 output
+  if (launch_finalize(acc, static_cast<__nv_bfloat16*>(a->out), static_cast<long long>(T) * H,
+                      dev.num_sms, s) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  return MOE_OK;
+}
+
+moe_status_t moe_check_status(const void* workspace, moe_stream_t stream) {
+  if (!workspace) return MOE_ERR_INVALID_ARG;
+  int err = 0;
+  if (cudaMemcpyAsync(&err, workspace, sizeof(int), cudaMemcpyDeviceToHost, stream) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  if (cudaStreamSynchronize(stream) != cudaSuccess) return MOE_ERR_CUDA;
+  if (err & kDevErrTimeout) return MOE_ERR_DEVICE_TIMEOUT;
+  if (err & kDevErrRange) return MOE_ERR_DEVICE_RANGE;
+  return MOE_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,533 @@
+// Token routing, alignment by expert, activation quantisation/gather and the
+// small elementwise kernels of the fused MoE layer (sm_103a).
+//
+// Routing and "data shuffling" are the first two stages of the fused MoE
+// operation ("Amazon SageMaker AI 上的 Mixture-of-Experts 内核工程优化",
+// Introduction); FP8 tensor scaling is fused with them ("Backend routing for
+// FP8 tensor quantization").  These kernels are HBM/latency bound: all loads
+// are 16-byte vectors where the data allows, and nothing is staged through
+// global memory that a CTA can keep on chip.
+#include <cuda_bf16.h>
+#include <math.h>
+#include <stdint.h>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace moe {
+
+namespace {
+
+constexpr unsigned kFull = 0xffffffffu;
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o; o >>= 1) v = fmaxf(v, __shfl_xor_sync(kFull, v, o));
+  return v;
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(kFull, v, o);
+  return v;
+}
+
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+__device__ __forceinline__ float absmax8(uint4 v, float m) {
+  m = fmaxf(m, fmaxf(fabsf(bf16_lo(v.x)), fabsf(bf16_hi(v.x))));
+  m = fmaxf(m, fmaxf(fabsf(bf16_lo(v.y)), fabsf(bf16_hi(v.y))));
+  m = fmaxf(m, fmaxf(fabsf(bf16_lo(v.z)), fabsf(bf16_hi(v.z))));
+  m = fmaxf(m, fmaxf(fabsf(bf16_lo(v.w)), fabsf(bf16_hi(v.w))));
+  return m;
+}
+
+// amax -> per-tensor scale: amax / 448 (IEEE fp32 division), 1 when amax is 0.
+__device__ __forceinline__ float scale_from_amax(float amax) {
+  return amax > 0.f ? __fdiv_rn(amax, 448.f) : 1.f;
+}
+
+// 8 bf16 (one uint4) / s -> 8 E4M3 codes (two uint32).
+__device__ __forceinline__ uint2 quant8(uint4 v, float s) {
+  uint2 r;
+  r.x = static_cast<uint32_t>(cvt_e4m3x2(__fdiv_rn(bf16_lo(v.x), s), __fdiv_rn(bf16_hi(v.x), s))) |
+        (static_cast<uint32_t>(cvt_e4m3x2(__fdiv_rn(bf16_lo(v.y), s), __fdiv_rn(bf16_hi(v.y), s)))
+         << 16);
+  r.y = static_cast<uint32_t>(cvt_e4m3x2(__fdiv_rn(bf16_lo(v.z), s), __fdiv_rn(bf16_hi(v.z), s))) |
+        (static_cast<uint32_t>(cvt_e4m3x2(__fdiv_rn(bf16_lo(v.w), s), __fdiv_rn(bf16_hi(v.w), s)))
+         << 16);
+  return r;
+}
+
+// Block-wide exclusive scan of one int per thread (blockDim.x == 1024).
+// `tmp` holds 32 ints of shared memory.  Every thread of the block must call it.
+__device__ int block_exclusive_scan_1024(int v, int* tmp, int* total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int incl = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    int n = __shfl_up_sync(kFull, incl, o);
+    if (lane >= o) incl += n;
+  }
+  if (lane == 31) tmp[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    int s = tmp[lane];
+    int si = s;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      int n = __shfl_up_sync(kFull, si, o);
+      if (lane >= o) si += n;
+    }
+    tmp[lane] = si;
+  }
+  __syncthreads();
+  const int excl = incl - v + (warp > 0 ? tmp[warp - 1] : 0);
+  *total = tmp[31];
+  __syncthreads();
+  return excl;
+}
+
+// ------------------------------------------------------------------ router
+// One warp per token.  The row of logits is staged in shared memory; each of
+// the k rounds is a warp arg-max under (logit desc, index asc) over the
+// experts not taken yet (one bit per lane per 32 experts).  The softmax uses
+// expf on max-subtracted logits.  Optionally also the per-CTA amax of x, the
+// first half of the dynamic activation scale.
+__global__ void __launch_bounds__(kRouteWarps * 32)
+    route_topk_kernel(const float* __restrict__ logits, int T, int E, int k, int renorm,
+                      int32_t* __restrict__ ids, float* __restrict__ wts,
+                      const __nv_bfloat16* __restrict__ x, int H, float* __restrict__ amax_partials,
+                      Ctrl* ctrl) {
+  extern __shared__ float s_logits[];
+  __shared__ float s_amax[kRouteWarps];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (ctrl != nullptr && blockIdx.x == 0 && threadIdx.x == 0) {
+    ctrl->err = 0;
+    ctrl->amax_h = 0u;
+  }
+  const int t = blockIdx.x * kRouteWarps + warp;
+  float xmax = 0.f;
+  if (t < T) {
+    float* l = s_logits + static_cast<size_t>(warp) * E;
+    const float* src = logits + static_cast<size_t>(t) * E;
+    float m = -INFINITY;
+    for (int e = lane; e < E; e += 32) {
+      const float v = src[e];
+      l[e] = v;
+      m = fmaxf(m, v);
+    }
+    m = warp_max(m);
+    float z = 0.f;
+    for (int e = lane; e < E; e += 32) z += expf(l[e] - m);
+    z = warp_sum(z);
+    __syncwarp();
+
+    uint32_t taken = 0u;  // bit i <=> expert lane + 32 i already selected
+    float sel = 0.f;
+    int32_t* id_row = ids + static_cast<size_t>(t) * k;
+    float* w_row = wts + static_cast<size_t>(t) * k;
+    for (int j = 0; j < k; ++j) {
+      float bv = -INFINITY;
+      int bi = 0x7fffffff;  // "none"
+      for (int e = lane, i = 0; e < E; e += 32, ++i) {
+        if ((taken >> i) & 1u) continue;
+        const float v = l[e];
+        if (bi == 0x7fffffff || v > bv) {  // ascending scan: equal values keep the lower index
+          bv = v;
+          bi = e;
+        }
+      }
+#pragma unroll
+      for (int o = 16; o; o >>= 1) {
+        const float ov = __shfl_xor_sync(kFull, bv, o);
+        const int oi = __shfl_xor_sync(kFull, bi, o);
+        const bool take =
+            oi != 0x7fffffff && (bi == 0x7fffffff || ov > bv || (ov == bv && oi < bi));
+        if (take) {
+          bv = ov;
+          bi = oi;
+        }
+      }
+      if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
+      const float ex = expf(bv - m);
+      sel += ex;
+      if (lane == 0) {
+        id_row[j] = bi;
+        w_row[j] = ex;
+      }
+    }
+    __syncwarp();
+    const float denom = renorm ? sel : z;
+    for (int j = lane; j < k; j += 32) w_row[j] = __fdiv_rn(w_row[j], denom);
+
+    if (x != nullptr) {
+      const uint4* xr = reinterpret_cast<const uint4*>(x + static_cast<size_t>(t) * H);
+      for (int i = lane; i < H / 8; i += 32) xmax = absmax8(__ldg(xr + i), xmax);
+      xmax = warp_max(xmax);
+    }
+  }
+  if (amax_partials != nullptr) {
+    if (lane == 0) s_amax[warp] = xmax;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      float m = 0.f;
+#pragma unroll
+      for (int w = 0; w < kRouteWarps; ++w) m = fmaxf(m, s_amax[w]);
+      amax_partials[blockIdx.x] = m;
+    }
+  }
+}
+
+// ------------------------------------------------------------------ align
+// Stable counting sort of the T*k (token, slot) pairs by expert, padded per
+// expert to a multiple of bm.  Each CTA owns one chunk of pair ids; it counts
+// all pairs (to get the global offsets) and the pairs before its chunk (to
+// get its own base inside every expert segment), so no CTA waits on another.
+// Inside the chunk each warp owns a contiguous sub-range: per-warp counts are
+// scanned column-wise over the 32 warps, then every warp places its pairs in
+// order with __match_any_sync ranks.  The resulting order is exactly the
+// ascending pair id order within each expert.
+constexpr int kAlignThreads = 1024;
+constexpr int kAlignChunk = 16384;  // pairs per CTA (<= 65535: per-warp counts are uint16)
+
+__global__ void __launch_bounds__(kAlignThreads) align_kernel(AlignParams p) {
+  extern __shared__ int s_align[];
+  __shared__ int s_tmp[32];
+  __shared__ float s_red[32];
+  const int E = p.E;
+  int* hist_all = s_align;
+  int* hist_before = hist_all + E;
+  int* base = hist_before + E;
+  int* seg_off = base + E;
+  uint16_t* seg = reinterpret_cast<uint16_t*>(seg_off + E);  // [32][E]
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int P = p.P;
+  const int cs = blockIdx.x * p.chunk;
+  const int ce = min(cs + p.chunk, P);
+  const int clen = max(ce - cs, 0);
+  const int seglen = (clen + 31) / 32;
+  const int s0 = cs + warp * seglen;
+  const int s1 = min(s0 + seglen, ce);
+
+  for (int e = tid; e < E; e += kAlignThreads) {
+    hist_all[e] = 0;
+    hist_before[e] = 0;
+  }
+  for (int i = tid; i < 32 * E; i += kAlignThreads) seg[i] = 0;
+  __syncthreads();
+
+  // histograms of every pair, and of the pairs before this chunk
+  for (int p0 = 0; p0 < P; p0 += kAlignThreads) {
+    const int q = p0 + tid;
+    const int e = q < P ? p.ids[q] : -1;
+    const bool valid = q < P && static_cast<unsigned>(e) < static_cast<unsigned>(E);
+    const int key = valid ? e : -1;
+    const unsigned mask = __match_any_sync(kFull, key);
+    if (valid && lane == __ffs(mask) - 1) {
+      const int n = __popc(mask);
+      atomicAdd(&hist_all[e], n);
+      if (q < cs) atomicAdd(&hist_before[e], n);
+    }
+  }
+  // per-warp counts of this CTA's chunk
+  for (int q0 = s0; q0 < s1; q0 += 32) {
+    const int q = q0 + lane;
+    const int e = q < s1 ? p.ids[q] : -1;
+    const bool valid = q < s1 && static_cast<unsigned>(e) < static_cast<unsigned>(E);
+    const unsigned mask = __match_any_sync(kFull, valid ? e : -1);
+    if (valid && lane == __ffs(mask) - 1) seg[warp * E + e] += static_cast<uint16_t>(__popc(mask));
+    __syncwarp();
+  }
+  __syncthreads();
+
+  // padded offsets (one expert per thread; E <= 1024)
+  const int c = tid < E ? hist_all[tid] : 0;
+  const int padded = (c + p.bm - 1) / p.bm * p.bm;
+  int total = 0;
+  const int off = block_exclusive_scan_1024(padded, s_tmp, &total);
+  if (tid < E) {
+    base[tid] = off + hist_before[tid];
+    seg_off[tid] = off;
+    uint16_t run = 0;
+    for (int w = 0; w < 32; ++w) {
+      const uint16_t n = seg[w * E + tid];
+      seg[w * E + tid] = run;
+      run = static_cast<uint16_t>(run + n);
+    }
+  }
+  if (blockIdx.x == 0) {
+    if (tid < E) {
+      p.counts[tid] = c;
+      p.offsets[tid] = off;
+    }
+    if (tid == 0) {
+      p.offsets[E] = total;
+      if (p.num_padded) *p.num_padded = total;
+      if (p.ctrl) p.ctrl->num_padded = total;
+    }
+  }
+  __syncthreads();
+
+  // stable scatter of this CTA's chunk
+  for (int q0 = s0; q0 < s1; q0 += 32) {
+    const int q = q0 + lane;
+    const int e = q < s1 ? p.ids[q] : -1;
+    const bool valid = q < s1 && static_cast<unsigned>(e) < static_cast<unsigned>(E);
+    const unsigned mask = __match_any_sync(kFull, valid ? e : -1);
+    const int leader = __ffs(mask) - 1;
+    int slot = 0;
+    if (valid && lane == leader) {
+      slot = base[e] + seg[warp * E + e];
+      seg[warp * E + e] = static_cast<uint16_t>(seg[warp * E + e] + __popc(mask));
+    }
+    slot = __shfl_sync(kFull, slot, leader);
+    if (valid) p.sorted_ids[slot + __popc(mask & ((1u << lane) - 1u))] = q;
+    __syncwarp();
+  }
+
+  if (blockIdx.x != 0) return;  // uniform per block
+
+  // padding sentinels and the per-block expert map
+  if (tid < E) {
+    const int o = seg_off[tid];
+    for (int i = c; i < padded; ++i) p.sorted_ids[o + i] = P;
+    if (p.tile_expert)
+      for (int b = o / p.bm; b < (o + padded) / p.bm; ++b) p.tile_expert[b] = tid;
+  }
+
+  if (p.mtiles != nullptr) {
+    // GEMM row tiles: each expert's padded segment split into
+    // ceil(padded / bn_max) tiles of equal size (multiples of bm)
+    const int nt = padded > 0 ? (padded + p.bn_max - 1) / p.bn_max : 0;
+    int n_tiles = 0;
+    const int first = block_exclusive_scan_1024(nt, s_tmp, &n_tiles);
+    if (nt > 0) {
+      const int per = ((padded + nt - 1) / nt + p.bm - 1) / p.bm * p.bm;
+      const int o = seg_off[tid];
+      for (int j = 0; j < nt; ++j) {
+        const int rows = min(per, padded - j * per);
+        p.mtiles[first + j] = make_int4(tid, o + j * per, rows, 0);
+      }
+    }
+    // activation scale of x from the router's per-CTA amax values
+    float m = 0.f;
+    for (int i = tid; i < p.n_partials; i += kAlignThreads) m = fmaxf(m, p.amax_partials[i]);
+    m = warp_max(m);
+    if (lane == 0) s_red[warp] = m;
+    __syncthreads();
+    if (tid == 0) {
+      float a = 0.f;
+      for (int w = 0; w < 32; ++w) a = fmaxf(a, s_red[w]);
+      p.ctrl->s_x = p.amax_partials ? scale_from_amax(a) : 1.f;
+      p.ctrl->num_mtiles = n_tiles;
+    }
+  }
+}
+
+// ------------------------------------------------------------------ gather
+// One warp per aligned row: the row of x of the pair's token, quantised to
+// E4M3 with s_x (or copied as bf16); padding rows are zero.  The same grid
+// zeroes the fp32 combine buffer.
+__global__ void __launch_bounds__(256)
+    gather_x_kernel(const __nv_bfloat16* __restrict__ x, int H, const int32_t* __restrict__ sorted_ids,
+                    const Ctrl* __restrict__ ctrl, int P, int k, void* __restrict__ xs, int fp8,
+                    float* __restrict__ acc, long long acc_elems) {
+  const int lane = threadIdx.x & 31;
+  const int gw = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int nw = (gridDim.x * blockDim.x) >> 5;
+  const int rows = ctrl->num_padded;
+  if (fp8) {
+    const float s = ctrl->s_x;
+    uint8_t* dst_all = static_cast<uint8_t*>(xs);
+    for (int r = gw; r < rows; r += nw) {
+      const int q = sorted_ids[r];
+      uint4* dst = reinterpret_cast<uint4*>(dst_all + static_cast<size_t>(r) * H);
+      if (q < P) {
+        const uint4* src = reinterpret_cast<const uint4*>(x + static_cast<size_t>(q / k) * H);
+        for (int c = lane; c < H / 16; c += 32) {
+          const uint2 a = quant8(__ldg(src + 2 * c), s);
+          const uint2 b = quant8(__ldg(src + 2 * c + 1), s);
+          dst[c] = make_uint4(a.x, a.y, b.x, b.y);
+        }
+      } else {
+        for (int c = lane; c < H / 16; c += 32) dst[c] = make_uint4(0, 0, 0, 0);
+      }
+    }
+  } else {
+    __nv_bfloat16* dst_all = static_cast<__nv_bfloat16*>(xs);
+    for (int r = gw; r < rows; r += nw) {
+      const int q = sorted_ids[r];
+      uint4* dst = reinterpret_cast<uint4*>(dst_all + static_cast<size_t>(r) * H);
+      if (q < P) {
+        const uint4* src = reinterpret_cast<const uint4*>(x + static_cast<size_t>(q / k) * H);
+        for (int c = lane; c < H / 8; c += 32) dst[c] = __ldg(src + c);
+      } else {
+        for (int c = lane; c < H / 8; c += 32) dst[c] = make_uint4(0, 0, 0, 0);
+      }
+    }
+  }
+  float4* a4 = reinterpret_cast<float4*>(acc);
+  const long long n4 = acc_elems / 4;
+  for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < n4;
+       i += static_cast<long long>(gridDim.x) * blockDim.x)
+    a4[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+}
+
+// ------------------------------------------------------------------ h quant
+__global__ void __launch_bounds__(256)
+    quant_h_kernel(const __nv_bfloat16* __restrict__ h, int I, Ctrl* ctrl, uint8_t* __restrict__ hq) {
+  const float s = scale_from_amax(__uint_as_float(ctrl->amax_h));
+  if (blockIdx.x == 0 && threadIdx.x == 0) ctrl->s_h = s;
+  const long long n16 = static_cast<long long>(ctrl->num_padded) * I / 16;
+  const uint4* src = reinterpret_cast<const uint4*>(h);
+  uint4* dst = reinterpret_cast<uint4*>(hq);
+  for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < n16;
+       i += static_cast<long long>(gridDim.x) * blockDim.x) {
+    const uint2 a = quant8(src[2 * i], s);
+    const uint2 b = quant8(src[2 * i + 1], s);
+    dst[i] = make_uint4(a.x, a.y, b.x, b.y);
+  }
+}
+
+// ------------------------------------------------------------------ finalize
+__global__ void __launch_bounds__(256)
+    finalize_kernel(const float* __restrict__ acc, __nv_bfloat16* __restrict__ out, long long n8) {
+  const float4* a = reinterpret_cast<const float4*>(acc);
+  uint4* o = reinterpret_cast<uint4*>(out);
+  for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < n8;
+       i += static_cast<long long>(gridDim.x) * blockDim.x) {
+    const float4 u = a[2 * i], v = a[2 * i + 1];
+    __nv_bfloat162 b0 = __floats2bfloat162_rn(u.x, u.y);
+    __nv_bfloat162 b1 = __floats2bfloat162_rn(u.z, u.w);
+    __nv_bfloat162 b2 = __floats2bfloat162_rn(v.x, v.y);
+    __nv_bfloat162 b3 = __floats2bfloat162_rn(v.z, v.w);
+    uint4 r;
+    r.x = *reinterpret_cast<uint32_t*>(&b0);
+    r.y = *reinterpret_cast<uint32_t*>(&b1);
+    r.z = *reinterpret_cast<uint32_t*>(&b2);
+    r.w = *reinterpret_cast<uint32_t*>(&b3);
+    o[i] = r;
+  }
+}
+
+// ------------------------------------------------------------------ quantize (standalone)
+__global__ void __launch_bounds__(256)
+    amax_kernel(const __nv_bfloat16* __restrict__ x, long long n8, float* __restrict__ partials) {
+  __shared__ float s_red[8];
+  const uint4* src = reinterpret_cast<const uint4*>(x);
+  float m = 0.f;
+  for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < n8;
+       i += static_cast<long long>(gridDim.x) * blockDim.x)
+    m = absmax8(__ldg(src + i), m);
+  m = warp_max(m);
+  if ((threadIdx.x & 31) == 0) s_red[threadIdx.x >> 5] = m;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float a = 0.f;
+    for (int w = 0; w < 8; ++w) a = fmaxf(a, s_red[w]);
+    partials[blockIdx.x] = a;
+  }
+}
+
+__global__ void __launch_bounds__(256)
+    quant_x_kernel(const __nv_bfloat16* __restrict__ x, long long n16, const float* __restrict__ partials,
+                   int n_partials, uint8_t* __restrict__ xq, float* __restrict__ scale) {
+  __shared__ float s_scale;
+  if (threadIdx.x < 32) {
+    float m = 0.f;
+    for (int i = threadIdx.x; i < n_partials; i += 32) m = fmaxf(m, partials[i]);
+    m = warp_max(m);
+    if (threadIdx.x == 0) s_scale = scale_from_amax(m);
+  }
+  __syncthreads();
+  const float s = s_scale;
+  if (blockIdx.x == 0 && threadIdx.x == 0) *scale = s;
+  const uint4* src = reinterpret_cast<const uint4*>(x);
+  uint4* dst = reinterpret_cast<uint4*>(xq);
+  for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < n16;
+       i += static_cast<long long>(gridDim.x) * blockDim.x) {
+    const uint2 a = quant8(__ldg(src + 2 * i), s);
+    const uint2 b = quant8(__ldg(src + 2 * i + 1), s);
+    dst[i] = make_uint4(a.x, a.y, b.x, b.y);
+  }
+}
+
+}  // namespace
+
+// ------------------------------------------------------------------ launchers
+cudaError_t launch_route_topk(const float* logits, int T, int E, int k, int renorm, int32_t* ids,
+                              float* wts, const __nv_bfloat16* x, int H, float* amax_partials,
+                              Ctrl* ctrl, cudaStream_t st) {
+  const size_t smem = static_cast<size_t>(kRouteWarps) * E * sizeof(float);
+  route_topk_kernel<<<route_grid(T), kRouteWarps * 32, smem, st>>>(logits, T, E, k, renorm, ids,
+                                                                    wts, x, H, amax_partials, ctrl);
+  return cudaGetLastError();
+}
+
+int align_chunk() { return kAlignChunk; }
+
+cudaError_t launch_align(const AlignParams& p, cudaStream_t st) {
+  const size_t smem = static_cast<size_t>(p.E) * 4 * sizeof(int) + 32u * p.E * sizeof(uint16_t);
+  static thread_local int configured_device = -1;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (configured_device != dev) {
+    cudaError_t e = cudaFuncSetAttribute(align_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         4 * 1024 * 4 + 32 * 1024 * 2);
+    if (e != cudaSuccess) return e;
+    configured_device = dev;
+  }
+  const int grid = p.P > 0 ? (p.P + p.chunk - 1) / p.chunk : 1;
+  align_kernel<<<grid, kAlignThreads, smem, st>>>(p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_gather_x(const __nv_bfloat16* x, int H, const int32_t* sorted_ids,
+                            const Ctrl* ctrl, int P, int k, void* xs, bool fp8, float* acc,
+                            long long acc_elems, int max_rows, int num_sms, cudaStream_t st) {
+  int grid = (max_rows + 7) / 8;
+  const int cap = num_sms * 8;
+  if (grid > cap) grid = cap;
+  if (grid < 1) grid = 1;
+  gather_x_kernel<<<grid, 256, 0, st>>>(x, H, sorted_ids, ctrl, P, k, xs, fp8 ? 1 : 0, acc,
+                                        acc_elems);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_quant_h(const __nv_bfloat16* h, int I, Ctrl* ctrl, uint8_t* hq, int max_rows,
+                           int num_sms, cudaStream_t st) {
+  const long long n16 = static_cast<long long>(max_rows) * I / 16;
+  long long grid = (n16 + 255) / 256;
+  const long long cap = static_cast<long long>(num_sms) * 8;
+  if (grid > cap) grid = cap;
+  if (grid < 1) grid = 1;
+  quant_h_kernel<<<static_cast<int>(grid), 256, 0, st>>>(h, I, ctrl, hq);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_finalize(const float* acc, __nv_bfloat16* out, long long n, int num_sms,
+                            cudaStream_t st) {
+  const long long n8 = n / 8;
+  long long grid = (n8 + 255) / 256;
+  const long long cap = static_cast<long long>(num_sms) * 8;
+  if (grid > cap) grid = cap;
+  if (grid < 1) grid = 1;
+  finalize_kernel<<<static_cast<int>(grid), 256, 0, st>>>(acc, out, n8);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_quantize_e4m3(const __nv_bfloat16* x, long long n, uint8_t* xq, float* scale,
+                                 float* partials, int n_partials, cudaStream_t st) {
+  amax_kernel<<<n_partials, 256, 0, st>>>(x, n / 8, partials);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  long long grid = (n / 16 + 255) / 256;
+  if (grid > 4096) grid = 4096;
+  if (grid < 1) grid = 1;
+  quant_x_kernel<<<static_cast<int>(grid), 256, 0, st>>>(x, n / 16, partials, n_partials, xq, scale);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

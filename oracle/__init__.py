@@ -52,6 +52,8 @@ def lib():
             L.oracle_e4m3_encode.restype = ctypes.c_uint8
             L.oracle_e4m3_encode_n.argtypes = [P, ctypes.c_long, P]
             L.oracle_e4m3_encode_n.restype = None
+            L.oracle_quantize_act.argtypes = [P, ctypes.c_long, P, P]
+            L.oracle_quantize_act.restype = None
             L.oracle_quantize.argtypes = [ctypes.c_double, ctypes.c_float]
             L.oracle_quantize.restype = ctypes.c_uint8
             L.oracle_route_topk.argtypes = [P, i, i, i, i, P, P]
@@ -113,6 +115,15 @@ def e4m3_encode_array(v) -> np.ndarray:
 
 def quantize(v: float, s: float) -> int:
     return int(lib().oracle_quantize(float(v), float(s)))
+
+
+def quantize_act(x):
+    """bf16 tensor -> (E4M3 codes uint8 (same shape), s fp32)."""
+    xb = _np(x, np.uint16)
+    codes = np.zeros(xb.shape, np.uint8)
+    s = np.zeros(1, np.float32)
+    lib().oracle_quantize_act(_ptr(xb), xb.size, _ptr(codes), _ptr(s))
+    return codes, float(s[0])
 
 
 def route_topk(logits, top_k: int, renormalize: bool):

@@ -112,6 +112,19 @@ static uint8_t quantize(double v, float s) {
 
 uint8_t oracle_quantize(double v, float s) { return quantize(v, s); }
 
+/* Dynamic per-tensor quantisation of a bf16 tensor: s = amax/448 (1 if the
+ * tensor is zero), codes = E4M3(fp32(x) / s). */
+void oracle_quantize_act(const uint16_t* x, long n, uint8_t* codes, float* s_out) {
+  float amax = 0.0f;
+  for (long i = 0; i < n; ++i) {
+    float a = fabsf((float)bf16_bits_to_double(x[i]));
+    if (a > amax) amax = a;
+  }
+  float s = act_scale_from_amax(amax);
+  for (long i = 0; i < n; ++i) codes[i] = quantize(bf16_bits_to_double(x[i]), s);
+  *s_out = s;
+}
+
 void oracle_e4m3_encode_n(const float* v, long n, uint8_t* out) {
   for (long i = 0; i < n; ++i) out[i] = oracle_e4m3_encode(v[i]);
 }

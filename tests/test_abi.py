@@ -1,0 +1,108 @@
+"""Host-side checks of the C ABI (no GPU needed): the library loads, exports
+every function the header declares, sizes workspaces, and rejects bad
+arguments synchronously before touching the device."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import mixture_experts_layer_align_gb300 as moe
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "moe_gb300.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from mixture_experts_layer_align_gb300 import build
+    build.build()
+    return moe.load()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(moe_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_declares_the_entry_points():
+    names = declared_functions()
+    for n in ("moe_route_topk", "moe_align_by_expert", "moe_fused_forward",
+              "moe_fused_workspace_size", "moe_status_string", "moe_check_status"):
+        assert n in names
+
+
+def test_library_exports_every_declared_function(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+        assert ctypes.cast(getattr(lib, name), ctypes.c_void_p).value
+
+
+def test_status_strings(lib):
+    for code in range(7):
+        assert moe.status_string(code)
+    assert moe.status_string(99) == "unknown status"
+
+
+def test_workspace_size_grows_with_tokens(lib):
+    a = moe.moe_fused_workspace_size(1, 4096, 14336, 8, 2, moe.MOE_DT_FP8_E4M3)
+    b = moe.moe_fused_workspace_size(64, 4096, 14336, 8, 2, moe.MOE_DT_FP8_E4M3)
+    assert 0 < a < b
+    assert b % 256 == 0
+    assert moe.moe_fused_workspace_size(1, 128, 128, 4, 5, moe.MOE_DT_FP8_E4M3) == 0  # k > E
+    assert moe.moe_fused_workspace_size(1, 128, 128, 2000, 2, moe.MOE_DT_FP8_E4M3) == 0
+
+
+def _args(**kw):
+    base = dict(x=16, router_logits=16, w13=16, w2=16, w13_scale=16, w2_scale=16,
+                weight_dtype=1, T=4, H=128, I=256, E=8, top_k=2, renormalize=1, out=16,
+                topk_ids_out=None, topk_w_out=None, counts_out=None, debug_flags=0)
+    base.update(kw)
+    return moe.MoeFusedArgs(**base)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(top_k=9), 1), (dict(top_k=0), 1), (dict(E=0), 1), (dict(E=1025, top_k=2), 1),
+    (dict(T=-1), 1), (dict(H=100), 2), (dict(I=200), 2), (dict(w13_scale=None), 1),
+    (dict(weight_dtype=0), 1), (dict(weight_dtype=7), 1), (dict(x=None), 1),
+    (dict(x=17), 1), (dict(out=24), 1),
+])
+def test_fused_forward_rejects_bad_arguments(lib, kw, code):
+    a = _args(**kw)
+    st = lib.moe_fused_forward(ctypes.byref(a), ctypes.c_void_p(256), 1 << 40, None)
+    assert st == code
+
+
+def test_fused_forward_rejects_small_workspace(lib):
+    a = _args()
+    need = moe.moe_fused_workspace_size(4, 128, 256, 8, 2, moe.MOE_DT_FP8_E4M3)
+    assert lib.moe_fused_forward(ctypes.byref(a), ctypes.c_void_p(256), need - 1, None) == 3
+    assert lib.moe_fused_forward(ctypes.byref(a), None, need, None) == 3
+    assert lib.moe_fused_forward(ctypes.byref(a), ctypes.c_void_p(1024 + 16), need, None) == 3
+
+
+def test_zero_tokens_is_a_no_op(lib):
+    a = _args(T=0)
+    assert lib.moe_fused_forward(ctypes.byref(a), None, 0, None) == 0
+    assert lib.moe_route_topk(None, 0, 8, 2, 1, None, None, None) == 0
+
+
+def test_router_and_align_argument_checks(lib):
+    assert lib.moe_route_topk(None, 4, 8, 9, 1, None, None, None) == 1
+    assert lib.moe_route_topk(None, 4, 8, 2, 1, None, None, None) == 1
+    assert lib.moe_align_by_expert(None, 4, 2, 8, 0, None, None, None, None, None, None) == 1
+    assert lib.moe_align_by_expert(None, 4, 2, 8, 16, None, None, None, None, None, None) == 1
+    assert lib.moe_quantize_e4m3(None, 4, 100, None, None, None, 0, None) == 1
+
+
+def test_no_device_is_reported_not_faked(lib):
+    """Valid arguments on a host without a GPU: the call must fail with a
+    CUDA/unsupported status, never pretend to succeed."""
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("host has a GPU")
+    a = _args(weight_dtype=1)
+    need = moe.moe_fused_workspace_size(4, 128, 256, 8, 2, 1)
+    st = lib.moe_fused_forward(ctypes.byref(a), ctypes.c_void_p(1 << 20), need, None)
+    assert st in (2, 4)

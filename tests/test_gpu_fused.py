@@ -1,0 +1,127 @@
+"""GPU parity of the fused MoE forward against the CPU oracle.
+
+Routing (expert ids, per-expert counts) must match bit-exactly; outputs within
+max|gpu - oracle| <= 2e-2 * max|oracle|.  Small cases are compared on every
+output element; the five measured workloads at full size on sampled rows (the
+oracle still forms h for every routed pair, because the FP8 scale of h spans
+the whole call).
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from helpers import W_ATOL, W_RTOL, assert_out_close, sample_rows
+from mixture_experts_layer_align_gb300 import inputs
+
+pytestmark = pytest.mark.gpu
+
+
+def run_case(moe, w, a, top_k, renorm, rows=None, repeat=1):
+    dev = "cuda"
+    T, E = a.T, w.E
+    x, lg = a.x.to(dev), a.logits.to(dev)
+    w13, w2 = w.w13.to(dev), w.w2.to(dev)
+    s13 = None if w.w13_scale is None else w.w13_scale.to(dev)
+    s2 = None if w.w2_scale is None else w.w2_scale.to(dev)
+    ids = torch.empty(T, top_k, dtype=torch.int32, device=dev)
+    wts = torch.empty(T, top_k, dtype=torch.float32, device=dev)
+    counts = torch.empty(E, dtype=torch.int32, device=dev)
+    ws = moe.alloc_workspace(T, w.H, w.I, E, top_k, 1 if s13 is not None else 0, dev)
+    ws.fill_(0xAB)  # the call must not rely on a zeroed workspace
+    for _ in range(repeat):
+        out = moe.moe_fused_forward(x, lg, w13, w2, s13, s2, top_k, renorm, workspace=ws,
+                                    topk_ids_out=ids, topk_w_out=wts, counts_out=counts)
+    assert moe.moe_check_status(ws) == 0
+    ref = oracle.moe_forward(a.x, a.logits, w.w13.cpu(), w.w2.cpu(),
+                             None if w.w13_scale is None else w.w13_scale.cpu(),
+                             None if w.w2_scale is None else w.w2_scale.cpu(), top_k, renorm,
+                             rows=rows)
+    assert np.array_equal(ids.cpu().numpy(), ref["ids"])
+    assert np.array_equal(counts.cpu().numpy(), ref["counts"])
+    np.testing.assert_allclose(wts.cpu().numpy(), ref["weights"], rtol=W_RTOL, atol=W_ATOL)
+    return assert_out_close(out, ref["out"], rows)
+
+
+@pytest.mark.parametrize("T,H,I,E,k,renorm,dtype", [
+    (4, 128, 256, 8, 2, True, "bf16"),      # tiny bf16 workload
+    (4, 128, 256, 8, 2, True, "fp8"),
+    (37, 256, 384, 8, 2, True, "fp8"),      # ragged token count
+    (200, 512, 256, 16, 4, False, "fp8"),   # several row tiles per expert
+    (1, 256, 128, 4, 1, True, "fp8"),
+    (9, 128, 128, 1, 1, True, "fp8"),       # single expert: plain SwiGLU MLP
+    (9, 128, 128, 1, 1, False, "bf16"),
+    (16, 128, 256, 6, 6, False, "fp8"),     # k = E: dense mixture
+    (33, 384, 256, 12, 3, True, "bf16"),
+    (600, 256, 128, 4, 2, True, "fp8"),     # >256 rows per expert: split tiles
+    (130, 1024, 512, 64, 8, True, "fp8"),
+])
+def test_fused_small(gpu_lib, T, H, I, E, k, renorm, dtype):
+    w = inputs.make_weights(H, I, E, dtype, seed=T)
+    a = inputs.make_activations(T, H, E, "uniform", seed=T)
+    run_case(gpu_lib, w, a, k, renorm, repeat=2)
+
+
+def test_fused_zipf_skew(gpu_lib):
+    T, H, I, E, k = 300, 256, 256, 64, 8
+    w = inputs.make_weights(H, I, E, "fp8", seed=5)
+    a = inputs.make_activations(T, H, E, "zipf", seed=5)
+    run_case(gpu_lib, w, a, k, True)
+
+
+def test_fused_zero_tokens(gpu_lib):
+    w = inputs.make_weights(128, 128, 4, "fp8", seed=1, device="cuda")
+    x = torch.empty(0, 128, dtype=torch.bfloat16, device="cuda")
+    lg = torch.empty(0, 4, device="cuda")
+    out = gpu_lib.moe_fused_forward(x, lg, w.w13, w.w2, w.w13_scale, w.w2_scale, 2, True)
+    assert out.shape == (0, 128)
+
+
+def test_fused_token_permutation(gpu_lib):
+    T, H, I, E, k = 50, 256, 256, 8, 2
+    w = inputs.make_weights(H, I, E, "fp8", seed=2, device="cuda")
+    a = inputs.make_activations(T, H, E, "uniform", seed=2, device="cuda")
+    perm = torch.randperm(T, device="cuda")
+    o1 = gpu_lib.moe_fused_forward(a.x, a.logits, w.w13, w.w2, w.w13_scale, w.w2_scale, k, True)
+    o2 = gpu_lib.moe_fused_forward(a.x[perm].contiguous(), a.logits[perm].contiguous(), w.w13,
+                                   w.w2, w.w13_scale, w.w2_scale, k, True)
+    torch.cuda.synchronize()
+    d = (o2.float() - o1[perm].float()).abs().max().item()
+    assert d <= 2e-2 * o1.float().abs().max().item()
+
+
+# ---------------------------------------------------------------- full sizes
+_WCACHE = {}
+
+
+def _weights(name):
+    if name not in _WCACHE:
+        _WCACHE.clear()
+        c = inputs.workload(name)
+        _WCACHE[name] = inputs.make_weights(c["H"], c["I"], c["E"], c["dtype"], seed=0,
+                                            device="cuda")
+    return _WCACHE[name]
+
+
+FULL = [("decode_e8_top2", 1), ("decode_e8_top2", 8), ("decode_e8_top2", 64),
+        ("finegrained_e128", 1), ("finegrained_e128", 16), ("finegrained_e128", 256),
+        ("skewed_e256", 1), ("skewed_e256", 32), ("skewed_e256", 128),
+        ("prefill_e128_uniform", 2048), ("prefill_e128_zipf", 2048)]
+
+
+@pytest.mark.parametrize("name,T", FULL)
+def test_fused_full_size(gpu_lib, name, T):
+    c = inputs.workload(name)
+    w = _weights(name)
+    a = inputs.make_activations(T, c["H"], c["E"], c["routing"], seed=0, device="cuda")
+    rows = sample_rows(T, 24, seed=T)
+    run_case(gpu_lib, w, a, c["top_k"], True, rows=rows)
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("name", ["prefill_e128_uniform", "prefill_e128_zipf"])
+def test_fused_prefill_8192(gpu_lib, name):
+    c = inputs.workload(name)
+    w = _weights(name)
+    a = inputs.make_activations(8192, c["H"], c["E"], c["routing"], seed=0, device="cuda")
+    run_case(gpu_lib, w, a, c["top_k"], True, rows=sample_rows(8192, 16, seed=1))

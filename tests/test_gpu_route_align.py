@@ -1,0 +1,93 @@
+"""GPU parity: router, alignment by expert and activation quantisation through
+the C ABI, against the CPU oracle (bit-exact on ids, counts, permutation and
+E4M3 codes)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from helpers import W_ATOL, W_RTOL
+from mixture_experts_layer_align_gb300 import inputs
+
+pytestmark = pytest.mark.gpu
+
+
+def _logits(T, E, kind, seed):
+    g = torch.Generator().manual_seed(seed)
+    if kind == "normal":
+        return torch.randn(T, E, generator=g)
+    if kind == "ties":
+        vals = torch.tensor([-1.0, -0.0, 0.0, 0.5, 1.0, 2.0])
+        return vals[torch.randint(0, len(vals), (T, E), generator=g)]
+    if kind == "zipf":
+        return torch.randn(T, E, generator=g) + inputs.zipf_bias(E)
+    if kind == "large":
+        return torch.randn(T, E, generator=g) * 1e4
+    raise ValueError(kind)
+
+
+@pytest.mark.parametrize("T,E,k,kind", [
+    (1, 8, 2, "normal"), (4, 8, 2, "ties"), (37, 128, 8, "normal"), (513, 256, 8, "zipf"),
+    (64, 1, 1, "normal"), (100, 16, 16, "ties"), (300, 1024, 8, "normal"), (200, 64, 40, "large"),
+    (8192, 128, 8, "normal"),
+])
+@pytest.mark.parametrize("renorm", [True, False])
+def test_route_topk_parity(gpu_lib, T, E, k, kind, renorm):
+    lg = _logits(T, E, kind, seed=T * 7 + E).contiguous()
+    ids, w = gpu_lib.moe_route_topk(lg.cuda(), k, renorm)
+    torch.cuda.synchronize()
+    ref_ids, ref_w = oracle.route_topk(lg, k, renorm)
+    assert np.array_equal(ids.cpu().numpy(), ref_ids)
+    np.testing.assert_allclose(w.cpu().numpy(), ref_w, rtol=W_RTOL, atol=W_ATOL)
+
+
+def test_route_zero_tokens(gpu_lib):
+    lg = torch.zeros(0, 8, device="cuda")
+    ids, w = gpu_lib.moe_route_topk(lg, 2, True)
+    assert ids.shape == (0, 2)
+
+
+@pytest.mark.parametrize("T,k,E,bm,kind", [
+    (4, 2, 8, 16, "normal"), (1, 8, 128, 16, "normal"), (256, 8, 128, 16, "normal"),
+    (128, 8, 256, 16, "zipf"), (1000, 3, 5, 1, "normal"), (2048, 8, 128, 64, "zipf"),
+    (8192, 8, 128, 16, "normal"), (8192, 8, 128, 128, "zipf"), (3000, 8, 1024, 7, "normal"),
+    (5, 1, 1, 256, "normal"),
+])
+def test_align_parity(gpu_lib, T, k, E, bm, kind):
+    lg = _logits(T, E, kind, seed=T + k + E)
+    ref_ids, _ = oracle.route_topk(lg, k, True)
+    ids = torch.from_numpy(ref_ids).cuda()
+    res = gpu_lib.moe_align_by_expert(ids, E, bm)
+    torch.cuda.synchronize()
+    ref = oracle.align(ref_ids, E, bm)
+    n = ref["num_padded"]
+    assert int(res["num_padded"].item()) == n
+    assert np.array_equal(res["counts"].cpu().numpy(), ref["counts"])
+    assert np.array_equal(res["offsets"].cpu().numpy(), ref["offsets"])
+    assert np.array_equal(res["sorted_ids"][:n].cpu().numpy(), ref["sorted_ids"])
+    assert np.array_equal(res["tile_expert"][:n // bm].cpu().numpy(), ref["tile_expert"])
+    # entries past the padded end are not written
+    assert torch.all(res["sorted_ids"][n:] == -1)
+
+
+def test_align_out_of_range_ids_are_skipped(gpu_lib):
+    ids = torch.tensor([[0, 5], [9, 1], [-1, 1]], dtype=torch.int32, device="cuda")
+    res = gpu_lib.moe_align_by_expert(ids, 6, 4)
+    torch.cuda.synchronize()
+    assert res["counts"].cpu().tolist() == [1, 2, 0, 0, 0, 1]
+    assert res["sorted_ids"][:12].cpu().tolist() == [0, 6, 6, 6, 3, 5, 6, 6, 1, 6, 6, 6]
+
+
+@pytest.mark.parametrize("T,H,scale", [(1, 4096, 1.0), (64, 4096, 1.0), (8192, 2048, 1.0),
+                                       (7, 7168, 1e-3), (3, 128, 0.0), (5, 256, 300.0)])
+def test_quantize_e4m3_bit_exact(gpu_lib, T, H, scale):
+    g = torch.Generator().manual_seed(T + H)
+    x = (torch.randn(T, H, generator=g) * scale).to(torch.bfloat16)
+    if T > 3:
+        x[0, 0] = 0.0  # exact zero
+        x[1, 1] = -x[1, 1]
+    codes, s = gpu_lib.moe_quantize_e4m3(x.cuda())
+    torch.cuda.synchronize()
+    ref_codes, ref_s = oracle.quantize_act(x)
+    assert float(s.item()) == ref_s
+    assert np.array_equal(codes.cpu().numpy(), ref_codes)
