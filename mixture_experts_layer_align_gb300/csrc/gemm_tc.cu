@@ -17,7 +17,8 @@
 //   warp 1      allocates TMEM and issues tcgen05.mma (one thread), commits
 //               stage release and accumulator-ready barriers;
 //   warps 2..5  epilogue: tcgen05.ld of the accumulator, then either
-//               gate/up:  h = SiLU(g * s) * (u * s) -> bf16, running amax|h|
+//               gate/up:  h = SiLU(g * s) * (u * s) -> fp32 (FP8 path, with a
+//                         running amax|h|) or bf16 (bf16 path)
 //               down:     y * s * topk_weight -> red.add into the fp32 combine
 //                         buffer (expert aggregation fused into the GEMM).
 // The accumulator is double-buffered in TMEM when it fits, so the epilogue of
@@ -232,9 +233,17 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             const float gv = g[j] * sc;
             const float uv = v[j] * sc;
             const float hv = gv / (1.f + __expf(-gv)) * uv;
-            const __nv_bfloat16 hb = __float2bfloat16_rn(hv);
-            p.h_out[static_cast<size_t>(r) * p.ldh + col] = hb;
-            if (p.sorted_ids[r] < p.P) amax = fmaxf(amax, fabsf(__bfloat162float(hb)));
+            const size_t at = static_cast<size_t>(r) * p.ldh + col;
+            if (kBF16) {
+              // bf16 weights: h feeds the bf16 down-projection MMA directly
+              static_cast<__nv_bfloat16*>(p.h_out)[at] = __float2bfloat16_rn(hv);
+            } else {
+              // FP8: h stays fp32 until its per-tensor scale is known; an
+              // intermediate bf16 rounding would move values across E4M3
+              // rounding boundaries and cost percent-level output error
+              static_cast<float*>(p.h_out)[at] = hv;
+              if (p.sorted_ids[r] < p.P) amax = fmaxf(amax, fabsf(hv));
+            }
           }
         } else {
           float y[16];
@@ -256,7 +265,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       if (lane == 0) mbar_arrive(tempty + a);
       ++tt;
     }
-    if (kSwiGLU) {
+    if (kSwiGLU && !kBF16) {
 #pragma unroll
       for (int o = 16; o; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
       if (lane == 0 && amax > 0.f) atomicMax(&p.ctrl->amax_h, __float_as_uint(amax));

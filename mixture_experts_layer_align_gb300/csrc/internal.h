@@ -63,8 +63,8 @@ int align_chunk();
 cudaError_t launch_gather_x(const __nv_bfloat16* x, int H, const int32_t* sorted_ids,
                             const Ctrl* ctrl, int P, int k, void* xs, bool fp8, float* acc,
                             long long acc_elems, int max_rows, int num_sms, cudaStream_t st);
-// h (bf16) -> E4M3 with s_h = amax_h / 448 (stored into ctrl->s_h).
-cudaError_t launch_quant_h(const __nv_bfloat16* h, int I, Ctrl* ctrl, uint8_t* hq, int max_rows,
+// h (fp32) -> E4M3 with s_h = amax_h / 448 (stored into ctrl->s_h).
+cudaError_t launch_quant_h(const float* h, int I, Ctrl* ctrl, uint8_t* hq, int max_rows,
                            int num_sms, cudaStream_t st);
 // fp32 combine buffer -> bf16 output.
 cudaError_t launch_finalize(const float* acc, __nv_bfloat16* out, long long n, int num_sms,
@@ -93,7 +93,7 @@ struct GemmParams {
   const float* w_scale;  // [E] per-expert weight scale (FP8) or null
   int act_scale_sel;     // 1: s_x, 2: s_h (FP8); 0: none
   const float* topk_w;   // [P]
-  __nv_bfloat16* h_out;  // gate/up: [rows, I] bf16
+  void* h_out;           // gate/up: [rows, I], fp32 (FP8 path) or bf16 (bf16 path)
   int ldh;
   float* acc_out;        // down: [T, H] fp32
   int ldo;

@@ -105,7 +105,7 @@ Layout make_layout(int T, int H, int I, int E, int k, bool fp8) {
   L.sorted = take(sizeof(int32_t) * L.pad_max);
   L.mtiles = take(sizeof(int4) * L.max_mtiles);
   L.xs = take(static_cast<size_t>(L.pad_max) * H * (fp8 ? 1 : 2));
-  L.h = take(static_cast<size_t>(L.pad_max) * I * 2);
+  L.h = take(static_cast<size_t>(L.pad_max) * I * (fp8 ? 4 : 2));
   L.hq = take(fp8 ? static_cast<size_t>(L.pad_max) * I : 0);
   L.acc = take(static_cast<size_t>(T) * H * sizeof(float));
   L.total = off;
@@ -265,7 +265,7 @@ moe_status_t moe_fused_forward(const moe_fused_args* a, void* workspace, size_t 
   int32_t* sorted = reinterpret_cast<int32_t*>(ws + L.sorted);
   int4* mtiles = reinterpret_cast<int4*>(ws + L.mtiles);
   void* xs = ws + L.xs;
-  __nv_bfloat16* h = reinterpret_cast<__nv_bfloat16*>(ws + L.h);
+  void* h = ws + L.h;
   uint8_t* hq = ws + L.hq;
   float* acc = reinterpret_cast<float*>(ws + L.acc);
 
@@ -349,7 +349,7 @@ moe_status_t moe_fused_forward(const moe_fused_args* a, void* workspace, size_t 
   if (launch_gemm(bf16, true, g1, tm_w13, tm_xs, grid1, s) != cudaSuccess) return MOE_ERR_CUDA;
 
   // 5. dynamic scale of h and its E4M3 codes
-  if (fp8 && launch_quant_h(h, I, ctrl, hq, L.pad_max, dev.num_sms, s) != cudaSuccess)
+  if (fp8 && launch_quant_h(static_cast<const float*>(h), I, ctrl, hq, L.pad_max, dev.num_sms, s) != cudaSuccess)
     return MOE_ERR_CUDA;
 
   // 6. down GEMM + weighted scatter-combine (split over K when few units)

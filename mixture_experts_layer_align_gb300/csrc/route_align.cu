@@ -376,18 +376,26 @@ __global__ void __launch_bounds__(256)
 }
 
 // ------------------------------------------------------------------ h quant
+__device__ __forceinline__ uint32_t quant4(float4 v, float s) {
+  return static_cast<uint32_t>(cvt_e4m3x2(__fdiv_rn(v.x, s), __fdiv_rn(v.y, s))) |
+         (static_cast<uint32_t>(cvt_e4m3x2(__fdiv_rn(v.z, s), __fdiv_rn(v.w, s))) << 16);
+}
+
 __global__ void __launch_bounds__(256)
-    quant_h_kernel(const __nv_bfloat16* __restrict__ h, int I, Ctrl* ctrl, uint8_t* __restrict__ hq) {
+    quant_h_kernel(const float* __restrict__ h, int I, Ctrl* ctrl, uint8_t* __restrict__ hq) {
   const float s = scale_from_amax(__uint_as_float(ctrl->amax_h));
   if (blockIdx.x == 0 && threadIdx.x == 0) ctrl->s_h = s;
   const long long n16 = static_cast<long long>(ctrl->num_padded) * I / 16;
-  const uint4* src = reinterpret_cast<const uint4*>(h);
+  const float4* src = reinterpret_cast<const float4*>(h);
   uint4* dst = reinterpret_cast<uint4*>(hq);
   for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < n16;
        i += static_cast<long long>(gridDim.x) * blockDim.x) {
-    const uint2 a = quant8(src[2 * i], s);
-    const uint2 b = quant8(src[2 * i + 1], s);
-    dst[i] = make_uint4(a.x, a.y, b.x, b.y);
+    uint4 r;
+    r.x = quant4(src[4 * i + 0], s);
+    r.y = quant4(src[4 * i + 1], s);
+    r.z = quant4(src[4 * i + 2], s);
+    r.w = quant4(src[4 * i + 3], s);
+    dst[i] = r;
   }
 }
 
@@ -496,7 +504,7 @@ cudaError_t launch_gather_x(const __nv_bfloat16* x, int H, const int32_t* sorted
   return cudaGetLastError();
 }
 
-cudaError_t launch_quant_h(const __nv_bfloat16* h, int I, Ctrl* ctrl, uint8_t* hq, int max_rows,
+cudaError_t launch_quant_h(const float* h, int I, Ctrl* ctrl, uint8_t* hq, int max_rows,
                            int num_sms, cudaStream_t st) {
   const long long n16 = static_cast<long long>(max_rows) * I / 16;
   long long grid = (n16 + 255) / 256;
