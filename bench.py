@@ -1,0 +1,471 @@
+#!/usr/bin/env python
+"""Benchmark of the fused MoE layer forward on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+Default workload: the 8-expert top-2 decode sweep (H=4096, I=14336, E=8, k=2,
+FP8 E4M3 weights with per-expert scales, dynamic per-tensor FP8 activations,
+T in {1,2,4,8,16,32,64}).  One step = one moe_fused_forward call per T of the
+sweep (127 tokens).  Inputs are synthetic (seeded); the weights are larger
+than L2 and two copies alternate call to call, so every call streams its
+experts' weights from HBM.
+
+Prints one JSON line: tokens/s over the timed steps (max over ranks), per-T
+microseconds per call, the dominant kernel's roofline (HBM bytes of the
+touched experts' weights per launch / its CUDA-event duration), an end-to-end
+number through the same API with host buffers, SM clocks sampled during the
+timed region, and (rank 0, one GPU) the CPU oracle timed on this host.
+
+--impl reference times the CPU oracle (the plain fp64 implementation the GPU
+path is checked against) on the same workload; under torchrun only rank 0
+runs it.  N > 1 GPUs run independent replicas (the layer needs no exchange).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "fused-MoE layer tokens/s & µs/call; % of HBM BW (decode) or FP8 TC peak"
+STEP_NAMES = ["route", "align", "gather_quant_x", "gemm1_swiglu", "quant_h", "gemm2_combine",
+              "finalize"]
+FALLBACK_HBM_GBS = 6800.0
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=500)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default="decode_e8_top2")
+    ap.add_argument("--tokens", default="", help="comma list overriding the workload's T sweep")
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    return ap.parse_args()
+
+
+def dist_env():
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("LOCAL_RANK", "0")),
+            int(os.environ.get("WORLD_SIZE", "1")))
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d.get("hbm_gbs", FALLBACK_HBM_GBS)), "measured"
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    for f in ("gemm_tc.cu", "ptx.cuh"):
+        with open(os.path.join(ROOT, "mixture_experts_layer_align_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload):
+    """DRAM bytes per launch of the dominant kernel from the committed ncu
+    summary, if it was taken on the current kernel source (else None)."""
+    p = os.path.join(ROOT, "profiles", f"gemm1_swiglu_{workload}_traffic.txt")
+    if not os.path.exists(p):
+        return None
+    kv = {}
+    with open(p) as f:
+        for line in f:
+            if "=" in line and not line.startswith("#"):
+                k, v = line.split("=", 1)
+                kv[k.strip()] = v.strip()
+    if kv.get("kernel_source_hash") != kernel_source_hash():
+        return None
+    try:
+        return float(kv["dram_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle samples while the timed region runs."""
+
+    FIELDS = ("timestamp,uuid,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, uuid):
+        self.uuid = uuid
+        self.proc = None
+        self.tmp = None
+
+    def __enter__(self):
+        try:
+            self.tmp = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "50"], stdout=self.tmp, stderr=subprocess.DEVNULL)
+            time.sleep(0.5)  # let the sampler start before the timed region
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def mark(self, begin: bool):
+        import datetime
+        if begin:
+            self.t0 = datetime.datetime.now()
+        else:
+            self.t1 = datetime.datetime.now()
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        if self.proc is None or self.tmp is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.tmp.flush()
+        with open(self.tmp.name) as f:
+            rows = [r.split(", ") for r in f.read().strip().splitlines() if r.strip()]
+        os.unlink(self.tmp.name)
+        import datetime
+        mine = []
+        uuids = {r[1].strip() for r in rows if len(r) >= 10}
+        use_uuid = self.uuid if self.uuid in uuids else None
+        for r in rows:
+            if len(r) < 10 or (use_uuid and r[1].strip() != use_uuid):
+                continue
+            try:
+                ts = datetime.datetime.strptime(r[0].strip(), "%Y/%m/%d %H:%M:%S.%f")
+            except ValueError:
+                continue
+            if getattr(self, "t0", None) and getattr(self, "t1", None) and not (
+                    self.t0 <= ts <= self.t1):
+                continue
+            mine.append(r[1:])
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in mine:
+            try:
+                sm.append(float(r[1]))
+                smax.append(float(r[2]))
+            except (ValueError, IndexError):
+                continue
+            for n, v in zip(names, r[5:9]):
+                if v.strip().lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def tokens_list(args, cfg):
+    if args.tokens:
+        return [int(t) for t in args.tokens.split(",")]
+    return list(cfg["T"])
+
+
+# --------------------------------------------------------------------------- CPU oracle
+def time_oracle(cfg, Ts, weights_cpu, acts_cpu, min_seconds=10.0, max_passes=3):
+    """Wall time of the CPU oracle over the T sweep; repeats whole passes
+    until `min_seconds` elapsed (at most `max_passes`)."""
+    import oracle
+    w = weights_cpu
+    passes, t0 = 0, time.perf_counter()
+    while True:
+        for T in Ts:
+            a = acts_cpu[T]
+            oracle.moe_forward(a.x, a.logits, w.w13, w.w2, w.w13_scale, w.w2_scale,
+                               cfg["top_k"], True)
+        passes += 1
+        el = time.perf_counter() - t0
+        if el >= min_seconds or passes >= max_passes:
+            return el, passes, oracle.max_threads()
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return
+    import torch
+    from mixture_experts_layer_align_gb300 import inputs
+    cfg = inputs.workload(args.workload)
+    Ts = tokens_list(args, cfg)
+    w = inputs.make_weights(cfg["H"], cfg["I"], cfg["E"], cfg["dtype"], seed=0,
+                            device="cuda" if torch.cuda.is_available() else "cpu")
+    w = inputs.Weights(w.w13.cpu(), w.w2.cpu(), None if w.w13_scale is None else w.w13_scale.cpu(),
+                       None if w.w2_scale is None else w.w2_scale.cpu(), w.dtype, w.H, w.I, w.E)
+    acts = {T: inputs.make_activations(T, cfg["H"], cfg["E"], cfg["routing"], seed=0) for T in Ts}
+    import oracle
+    for _ in range(args.warmup):
+        time_oracle(cfg, Ts, w, acts, min_seconds=0.0, max_passes=1)
+    el = 0.0
+    for _ in range(args.steps):
+        e, _, cores = time_oracle(cfg, Ts, w, acts, min_seconds=0.0, max_passes=1)
+        el += e
+    tokens = sum(Ts) * args.steps
+    value = tokens / el
+    cores = oracle.max_threads()
+    sample = f"{args.workload} T in {Ts}, one oracle call per T per step, fp64, {cores} threads"
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": el / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": args.workload, "tokens": Ts, "H": cfg["H"], "I": cfg["I"],
+                   "E": cfg["E"], "top_k": cfg["top_k"], "routing": cfg["routing"]},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# --------------------------------------------------------------------------- GPU path
+def run_ours(args, rank, local_rank, world):
+    import torch
+    import mixture_experts_layer_align_gb300 as moe
+    from mixture_experts_layer_align_gb300 import inputs
+
+    moe.load()
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+
+    cfg = inputs.workload(args.workload)
+    Ts = tokens_list(args, cfg)
+    H, I, E, k = cfg["H"], cfg["I"], cfg["E"], cfg["top_k"]
+    fp8 = cfg["dtype"] == "fp8"
+    dtype = moe.MOE_DT_FP8_E4M3 if fp8 else moe.MOE_DT_BF16
+    w = inputs.make_weights(H, I, E, cfg["dtype"], seed=0, device=dev)
+    # second copy of the same weights in other buffers: consecutive calls
+    # alternate, so no call finds its weights in L2
+    w_alt = inputs.Weights(w.w13.clone(), w.w2.clone(), w.w13_scale, w.w2_scale, w.dtype, H, I, E)
+    copies = [w, w_alt]
+    acts = {T: inputs.make_activations(T, H, E, cfg["routing"], seed=0, device=dev) for T in Ts}
+    outs = {T: torch.empty(T, H, dtype=torch.bfloat16, device=dev) for T in Ts}
+    wss = {T: moe.alloc_workspace(T, H, I, E, k, dtype, dev) for T in Ts}
+
+    # routing statistics per T (touched experts -> algorithmic bytes)
+    stats = {}
+    esize = 1 if fp8 else 2
+    for T in Ts:
+        counts = torch.empty(E, dtype=torch.int32, device=dev)
+        a = acts[T]
+        moe.moe_fused_forward(a.x, a.logits, w.w13, w.w2, w.w13_scale, w.w2_scale, k, True,
+                              out=outs[T], workspace=wss[T], counts_out=counts)
+        st = moe.moe_check_status(wss[T])
+        if st != 0:
+            raise RuntimeError(f"device status {moe.status_string(st)}")
+        c = counts.cpu()
+        touched = int((c > 0).sum())
+        P = T * k
+        stats[T] = dict(
+            touched=touched, max_rows=int(c.max()),
+            gemm1_bytes=touched * 2 * I * H * esize + P * H * esize + P * I * (4 if fp8 else 2),
+            gemm2_bytes=touched * H * I * esize + P * I * esize + P * H * 4,
+            layer_bytes=touched * 3 * H * I * esize + 8 * E + T * E * 4 + 2 * T * H * 2)
+
+    calls_per_step = len(Ts)
+    launches_per_call = 7 if fp8 else 6
+
+    def one_step(step_idx, events=None):
+        for j, T in enumerate(Ts):
+            ww = copies[(step_idx * calls_per_step + j) % 2]
+            a = acts[T]
+            moe.moe_fused_forward(a.x, a.logits, ww.w13, ww.w2, ww.w13_scale, ww.w2_scale, k,
+                                  True, out=outs[T], workspace=wss[T],
+                                  events=None if events is None else events[j])
+
+    for i in range(max(args.warmup, 3)):
+        one_step(i)
+    torch.cuda.synchronize()
+
+    K = args.steps
+    ev = [[moe.make_step_events(8) for _ in Ts] for _ in range(K)]
+    start = torch.cuda.Event(enable_timing=True)
+    stop = torch.cuda.Event(enable_timing=True)
+    uuid = None
+    try:
+        uuid = str(torch.cuda.get_device_properties(dev).uuid)
+        if not uuid.startswith("GPU-"):
+            uuid = "GPU-" + uuid
+    except Exception:
+        pass
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(uuid) as clk:
+        clk.mark(True)
+        start.record()
+        for s in range(K):
+            one_step(s, ev[s])
+        stop.record()
+        torch.cuda.synchronize()
+        clk.mark(False)
+    if dist is not None:
+        dist.barrier()
+    elapsed_ms = start.elapsed_time(stop)
+    if dist is not None:
+        t = torch.tensor([elapsed_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        elapsed_ms = float(t.item())
+    clocks = clk.summary()
+
+    # per-step (kernel) durations from the events inside the timed region
+    per_T_call_us = {T: [] for T in Ts}
+    step_ms = {n: 0.0 for n in STEP_NAMES}
+    gemm1_ms = {T: [] for T in Ts}
+    gemm2_ms = {T: [] for T in Ts}
+    for s in range(K):
+        for j, T in enumerate(Ts):
+            e = ev[s][j]
+            per_T_call_us[T].append(e[0].elapsed_time(e[7]) * 1e3)
+            for i, n in enumerate(STEP_NAMES):
+                step_ms[n] += e[i].elapsed_time(e[i + 1])
+            gemm1_ms[T].append(e[3].elapsed_time(e[4]))
+            gemm2_ms[T].append(e[5].elapsed_time(e[6]))
+    total_kernel_ms = sum(step_ms.values())
+    hbm_peak, peak_kind = measured_peaks()
+    # roofline of the heavier expert GEMM: algorithmic bytes over its launches
+    if step_ms["gemm2_combine"] > step_ms["gemm1_swiglu"]:
+        dominant = "gemm2_combine"
+        dom_bytes = sum(stats[T]["gemm2_bytes"] for T in Ts) * K
+        dom_ms = sum(sum(gemm2_ms[T]) for T in Ts)
+    else:
+        dominant = "gemm1_swiglu"
+        dom_bytes = sum(stats[T]["gemm1_bytes"] for T in Ts) * K
+        dom_ms = sum(sum(gemm1_ms[T]) for T in Ts)
+    achieved = dom_bytes / (dom_ms * 1e-3) / 1e9
+    traffic = recorded_traffic(args.workload) if dominant == "gemm1_swiglu" else None
+
+    tokens_per_step = sum(Ts)
+    value = world * tokens_per_step * K / (elapsed_ms * 1e-3)
+    sweep = []
+    for T in Ts:
+        us = statistics.median(per_T_call_us[T])
+        sweep.append({
+            "T": T, "us_per_call": round(us, 2), "tokens_per_s": round(T / (us * 1e-6), 1),
+            "touched_experts": stats[T]["touched"], "max_rows_per_expert": stats[T]["max_rows"],
+            "layer_bytes": stats[T]["layer_bytes"],
+            "layer_hbm_frac": round(stats[T]["layer_bytes"] / (us * 1e-6) / 1e9 / hbm_peak, 4),
+            "gemm1_us": round(statistics.median(gemm1_ms[T]) * 1e3, 2),
+            "gemm2_us": round(statistics.median(gemm2_ms[T]) * 1e3, 2)})
+
+    # end to end through the same API: pinned host inputs -> device -> host output
+    e2e = None
+    if not args.no_e2e:
+        host = {T: (acts[T].x.cpu().pin_memory(), acts[T].logits.cpu().pin_memory(),
+                    torch.empty(T, H, dtype=torch.bfloat16).pin_memory()) for T in Ts}
+        dx = {T: torch.empty_like(acts[T].x) for T in Ts}
+        dl = {T: torch.empty_like(acts[T].logits) for T in Ts}
+        h2d = sum(T * H * 2 + T * E * 4 for T in Ts)
+        d2h = sum(T * H * 2 for T in Ts)
+
+        def e2e_step(s):
+            for j, T in enumerate(Ts):
+                ww = copies[(s * calls_per_step + j) % 2]
+                hx, hl, ho = host[T]
+                dx[T].copy_(hx, non_blocking=True)
+                dl[T].copy_(hl, non_blocking=True)
+                moe.moe_fused_forward(dx[T], dl[T], ww.w13, ww.w2, ww.w13_scale, ww.w2_scale, k,
+                                      True, out=outs[T], workspace=wss[T])
+                ho.copy_(outs[T], non_blocking=True)
+
+        for i in range(3):
+            e2e_step(i)
+        torch.cuda.synchronize()
+        if dist is not None:
+            dist.barrier()
+        s0 = torch.cuda.Event(enable_timing=True)
+        s1 = torch.cuda.Event(enable_timing=True)
+        s0.record()
+        for s in range(K):
+            e2e_step(s)
+        s1.record()
+        torch.cuda.synchronize()
+        e_ms = s0.elapsed_time(s1)
+        if dist is not None:
+            t = torch.tensor([e_ms], device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            e_ms = float(t.item())
+        e2e = {"value": world * tokens_per_step * K / (e_ms * 1e-3), "unit": "tokens/s",
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        wc = inputs.Weights(w.w13.cpu(), w.w2.cpu(),
+                            None if w.w13_scale is None else w.w13_scale.cpu(),
+                            None if w.w2_scale is None else w.w2_scale.cpu(), w.dtype, H, I, E)
+        ac = {T: inputs.Activations(acts[T].x.cpu(), acts[T].logits.cpu(), T) for T in Ts}
+        el, passes, cores = time_oracle(cfg, Ts, wc, ac)
+        cpu = {"value": passes * tokens_per_step / el, "unit": "tokens/s", "cores": cores,
+               "kind": "oracle",
+               "sample": f"{passes} pass(es) of the T sweep {Ts} ({passes * tokens_per_step} "
+                         f"tokens), fp64 oracle, {el:.1f} s"}
+
+    if rank != 0:
+        if dist is not None:
+            dist.destroy_process_group()
+        return
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": elapsed_ms / K, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "e4m3" if fp8 else "bf16",
+        "data": "synthetic",
+        "config": {
+            "workload": f"{args.workload}: T in {Ts}, H={H}, I={I}, E={E}, top_k={k}, "
+                        f"renormalised, {cfg['routing']} routing, "
+                        + ("FP8 E4M3 weights (per-expert scale) + dynamic per-tensor FP8 "
+                           "activations" if fp8 else "bf16 weights"),
+            "step": f"one moe_fused_forward per T ({calls_per_step} calls, {tokens_per_step} "
+                    "tokens)",
+            "l2": "inputs larger than L2: two copies of the "
+                  f"{(w.w13.numel() + w.w2.numel()) * esize / 1e9:.2f} GB weights alternate "
+                  "call to call",
+            "parallelism": f"replicas x{world}"},
+        "sweep": sweep,
+        "kernel_share": {n: round(step_ms[n] / total_kernel_ms, 4) for n in STEP_NAMES},
+        "roofline": {"kernel": dominant, "bound": "hbm", "achieved": round(achieved, 1),
+                     "peak": hbm_peak, "peak_kind": f"{peak_kind} hbm_gbs",
+                     "unit": "GB/s", "frac": round(achieved / hbm_peak, 4), "traffic": traffic,
+                     "algorithmic_bytes": "touched experts' weight bytes + routed activation "
+                                          "rows in + h out, per launch"},
+        "clocks": clocks,
+        "gpu_launches": K * calls_per_step * launches_per_call,
+        "e2e": e2e,
+        "cpu_baseline": cpu,
+    }
+    print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+def main():
+    args = parse()
+    rank, local_rank, world = dist_env()
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+    else:
+        run_ours(args, rank, local_rank, world)
+
+
+if __name__ == "__main__":
+    main()

@@ -145,6 +145,20 @@ size_t moe_fused_workspace_size(int T, int H, int I, int E, int top_k, moe_dtype
 moe_status_t moe_fused_forward(const moe_fused_args* args, void* workspace, size_t workspace_bytes,
                                moe_stream_t stream);
 
+/*
+ * Same operation as moe_fused_forward, with the duration of every step made
+ * measurable: events[i] (a cudaEvent_t created by the caller) is recorded on
+ * `stream` before step i and events[7] after the last step.  Steps: 0 routing,
+ * 1 alignment, 2 gather/quantise x, 3 gate/up GEMM + SiLU*up, 4 quantise h
+ * (empty for bf16), 5 down GEMM + combine, 6 bf16 output.  Requires
+ * n_events >= MOE_TIMED_EVENTS and non-null events; otherwise as
+ * moe_fused_forward.
+ */
+#define MOE_TIMED_EVENTS 8
+moe_status_t moe_fused_forward_timed(const moe_fused_args* args, void* workspace,
+                                     size_t workspace_bytes, moe_stream_t stream,
+                                     void* const* events, int n_events);
+
 /* Synchronises `stream`, reads the status word that the last call using
  * `workspace` left there, and returns MOE_OK, MOE_ERR_DEVICE_TIMEOUT or
  * MOE_ERR_DEVICE_RANGE (MOE_ERR_CUDA if the synchronisation itself failed). */

@@ -76,11 +76,13 @@ def load():
         L.moe_fused_workspace_size.argtypes = [i, i, i, i, i, i]
         L.moe_fused_workspace_size.restype = sz
         L.moe_fused_forward.argtypes = [ctypes.POINTER(MoeFusedArgs), P, sz, P]
+        L.moe_fused_forward_timed.argtypes = [ctypes.POINTER(MoeFusedArgs), P, sz, P,
+                                               ctypes.POINTER(ctypes.c_void_p), i]
         L.moe_check_status.argtypes = [P, P]
         L.moe_status_string.argtypes = [i]
         L.moe_status_string.restype = ctypes.c_char_p
         for name in ("moe_route_topk", "moe_align_by_expert", "moe_quantize_e4m3",
-                     "moe_fused_forward", "moe_check_status"):
+                     "moe_fused_forward", "moe_fused_forward_timed", "moe_check_status"):
             getattr(L, name).restype = ctypes.c_int
         _lib = L
         return _lib
@@ -182,14 +184,8 @@ def alloc_workspace(T, H, I, E, top_k, dtype, device="cuda"):
     return torch.empty(n, dtype=torch.uint8, device=device)
 
 
-def moe_fused_forward(x, router_logits, w13, w2, w13_scale, w2_scale, top_k: int,
-                      renormalize: bool = True, out=None, workspace=None, topk_ids_out=None,
-                      topk_w_out=None, counts_out=None, debug_flags: int = 0, stream=None):
-    """Fused MoE layer forward (see include/moe_gb300.h).
-
-    x bf16 [T,H]; router_logits fp32 [T,E]; w13 [E,2I,H] and w2 [E,H,I] as uint8
-    E4M3 codes (with fp32 [E] scales) or bf16 (scales None).  Returns out bf16 [T,H].
-    """
+def _fused_args(x, router_logits, w13, w2, w13_scale, w2_scale, top_k, renormalize, out,
+                topk_ids_out, topk_w_out, counts_out, debug_flags):
     import torch
     _require(x, torch.bfloat16, "x")
     _require(router_logits, torch.float32, "router_logits")
@@ -206,11 +202,7 @@ def moe_fused_forward(x, router_logits, w13, w2, w13_scale, w2_scale, top_k: int
         _require(w13_scale, torch.float32, "w13_scale", (E,))
         _require(w2_scale, torch.float32, "w2_scale", (E,))
     dtype = MOE_DT_FP8_E4M3 if fp8 else MOE_DT_BF16
-    if out is None:
-        out = torch.empty(T, H, dtype=torch.bfloat16, device=x.device)
     _require(out, torch.bfloat16, "out", (T, H))
-    if workspace is None:
-        workspace = alloc_workspace(T, H, I, E, top_k, dtype, x.device)
     if topk_ids_out is not None:
         _require(topk_ids_out, torch.int32, "topk_ids_out", (T, top_k))
     if topk_w_out is not None:
@@ -226,9 +218,48 @@ def moe_fused_forward(x, router_logits, w13, w2, w13_scale, w2_scale, top_k: int
         topk_w_out=topk_w_out.data_ptr() if topk_w_out is not None else None,
         counts_out=counts_out.data_ptr() if counts_out is not None else None,
         debug_flags=int(debug_flags))
-    _check(load().moe_fused_forward(ctypes.byref(args), _ptr(workspace), workspace.numel(),
-                                    _stream(stream)), "moe_fused_forward")
+    return args, (T, H, I, E, dtype)
+
+
+def moe_fused_forward(x, router_logits, w13, w2, w13_scale, w2_scale, top_k: int,
+                      renormalize: bool = True, out=None, workspace=None, topk_ids_out=None,
+                      topk_w_out=None, counts_out=None, debug_flags: int = 0, stream=None,
+                      events=None):
+    """Fused MoE layer forward (see include/moe_gb300.h).
+
+    x bf16 [T,H]; router_logits fp32 [T,E]; w13 [E,2I,H] and w2 [E,H,I] as uint8
+    E4M3 codes (with fp32 [E] scales) or bf16 (scales None).  Returns out bf16 [T,H].
+    `events`: optional list of 8 recorded torch.cuda.Event (enable_timing) that
+    bracket the seven steps (moe_fused_forward_timed).
+    """
+    import torch
+    if out is None:
+        out = torch.empty(x.shape[0], x.shape[1], dtype=torch.bfloat16, device=x.device)
+    args, (T, H, I, E, dtype) = _fused_args(x, router_logits, w13, w2, w13_scale, w2_scale,
+                                            top_k, renormalize, out, topk_ids_out, topk_w_out,
+                                            counts_out, debug_flags)
+    if workspace is None:
+        workspace = alloc_workspace(T, H, I, E, top_k, dtype, x.device)
+    L = load()
+    if events is None:
+        st = L.moe_fused_forward(ctypes.byref(args), _ptr(workspace), workspace.numel(),
+                                 _stream(stream))
+        _check(st, "moe_fused_forward")
+    else:
+        arr = (ctypes.c_void_p * len(events))(*[ctypes.c_void_p(e.cuda_event) for e in events])
+        st = L.moe_fused_forward_timed(ctypes.byref(args), _ptr(workspace), workspace.numel(),
+                                       _stream(stream), arr, len(events))
+        _check(st, "moe_fused_forward_timed")
     return out
+
+
+def make_step_events(n: int = 8):
+    """n timing events, each recorded once so that its CUDA handle exists."""
+    import torch
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
+    for e in evs:
+        e.record()
+    return evs
 
 
 def moe_check_status(workspace, stream=None) -> int:
@@ -238,5 +269,5 @@ def moe_check_status(workspace, stream=None) -> int:
 
 __all__ = ["load", "moe_route_topk", "moe_align_by_expert", "moe_quantize_e4m3",
            "moe_fused_workspace_size", "moe_fused_forward", "moe_check_status", "alloc_workspace",
-           "status_string", "MoeError", "MoeFusedArgs", "MOE_DT_BF16", "MOE_DT_FP8_E4M3",
+           "status_string", "MoeError", "make_step_events", "MoeFusedArgs", "MOE_DT_BF16", "MOE_DT_FP8_E4M3",
            "MOE_DEBUG_FORCE_TIMEOUT", "LIB_PATH"]

@@ -226,8 +226,14 @@ size_t moe_fused_workspace_size(int T, int H, int I, int E, int top_k, moe_dtype
   return make_layout(T, H, I, E, top_k, dtype == MOE_DT_FP8_E4M3).total;
 }
 
-moe_status_t moe_fused_forward(const moe_fused_args* a, void* workspace, size_t workspace_bytes,
-                               moe_stream_t stream) {
+}  // extern "C"
+
+namespace {
+
+// The launch sequence.  When `events` is non-null, events[i] is recorded on
+// the stream before step i (i = 0..6) and events[7] after the last step.
+moe_status_t fused_forward_impl(const moe_fused_args* a, void* workspace, size_t workspace_bytes,
+                                moe_stream_t stream, cudaEvent_t const* events) {
   if (!a) return MOE_ERR_INVALID_ARG;
   const int T = a->T, H = a->H, I = a->I, E = a->E, k = a->top_k;
   if (T < 0 || H <= 0 || I <= 0 || E < 1 || E > kMaxExperts || k < 1 || k > E)
@@ -275,12 +281,14 @@ moe_status_t moe_fused_forward(const moe_fused_args* a, void* workspace, size_t 
   const long long mean_rows = (P + touched - 1) / touched;
   const int bn_max = std::min(256, std::max(64, round_up16(2 * mean_rows)));
 
+  if (events && cudaEventRecord(events[0], stream) != cudaSuccess) return MOE_ERR_CUDA;
   // 1. routing (+ per-CTA amax of x, + reset of the control words)
   cudaStream_t s = stream;
   if (launch_route_topk(a->router_logits, T, E, k, a->renormalize, ids, wts,
                         static_cast<const __nv_bfloat16*>(a->x), H, fp8 ? partials : nullptr, ctrl,
                         s) != cudaSuccess)
     return MOE_ERR_CUDA;
+  if (events && cudaEventRecord(events[1], stream) != cudaSuccess) return MOE_ERR_CUDA;
   // 2. alignment by expert, GEMM row tiles, s_x
   AlignParams ap{};
   ap.ids = ids;
@@ -299,6 +307,7 @@ moe_status_t moe_fused_forward(const moe_fused_args* a, void* workspace, size_t 
   ap.amax_partials = fp8 ? partials : nullptr;
   ap.n_partials = fp8 ? L.n_partials : 0;
   if (launch_align(ap, s) != cudaSuccess) return MOE_ERR_CUDA;
+  if (events && cudaEventRecord(events[2], stream) != cudaSuccess) return MOE_ERR_CUDA;
   // 3. gather (+ quantise) the routed rows of x; zero the combine buffer
   if (launch_gather_x(static_cast<const __nv_bfloat16*>(a->x), H, sorted, ctrl, static_cast<int>(P),
                       k, xs, fp8, acc, static_cast<long long>(T) * H, L.pad_max, dev.num_sms,
@@ -318,6 +327,7 @@ moe_status_t moe_fused_forward(const moe_fused_args* a, void* workspace, size_t 
   const int k_elems = fp8 ? 128 : 64;
   const long long max_tiles = std::min<long long>(L.max_mtiles, (L.pad_max + bn_max - 1) / bn_max + touched);
 
+  if (events && cudaEventRecord(events[3], stream) != cudaSuccess) return MOE_ERR_CUDA;
   // 4. gate/up GEMM + SiLU*up epilogue
   GemmParams g1{};
   g1.mtiles = mtiles;
@@ -348,10 +358,12 @@ moe_status_t moe_fused_forward(const moe_fused_args* a, void* workspace, size_t 
   const int grid1 = static_cast<int>(std::max<long long>(1, std::min<long long>(dev.num_sms, units1)));
   if (launch_gemm(bf16, true, g1, tm_w13, tm_xs, grid1, s) != cudaSuccess) return MOE_ERR_CUDA;
 
+  if (events && cudaEventRecord(events[4], stream) != cudaSuccess) return MOE_ERR_CUDA;
   // 5. dynamic scale of h and its E4M3 codes
   if (fp8 && launch_quant_h(static_cast<const float*>(h), I, ctrl, hq, L.pad_max, dev.num_sms, s) != cudaSuccess)
     return MOE_ERR_CUDA;
 
+  if (events && cudaEventRecord(events[5], stream) != cudaSuccess) return MOE_ERR_CUDA;
   // 6. down GEMM + weighted scatter-combine (split over K when few units)
   GemmParams g2 = g1;
   g2.nb_count = H / 128;
@@ -375,11 +387,32 @@ moe_status_t moe_fused_forward(const moe_fused_args* a, void* workspace, size_t 
   const int grid2 = static_cast<int>(std::max<long long>(1, std::min<long long>(dev.num_sms, units2)));
   if (launch_gemm(bf16, false, g2, tm_w2, tm_h, grid2, s) != cudaSuccess) return MOE_ERR_CUDA;
 
+  if (events && cudaEventRecord(events[6], stream) != cudaSuccess) return MOE_ERR_CUDA;
   // 7. fp32 combine buffer -> bf16 output
   if (launch_finalize(acc, static_cast<__nv_bfloat16*>(a->out), static_cast<long long>(T) * H,
                       dev.num_sms, s) != cudaSuccess)
     return MOE_ERR_CUDA;
+  if (events && cudaEventRecord(events[7], stream) != cudaSuccess) return MOE_ERR_CUDA;
   return MOE_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+moe_status_t moe_fused_forward(const moe_fused_args* a, void* workspace, size_t workspace_bytes,
+                               moe_stream_t stream) {
+  return fused_forward_impl(a, workspace, workspace_bytes, stream, nullptr);
+}
+
+moe_status_t moe_fused_forward_timed(const moe_fused_args* a, void* workspace,
+                                     size_t workspace_bytes, moe_stream_t stream,
+                                     void* const* events, int n_events) {
+  if (!events || n_events < MOE_TIMED_EVENTS) return MOE_ERR_INVALID_ARG;
+  for (int i = 0; i < MOE_TIMED_EVENTS; ++i)
+    if (!events[i]) return MOE_ERR_INVALID_ARG;
+  return fused_forward_impl(a, workspace, workspace_bytes, stream,
+                            reinterpret_cast<cudaEvent_t const*>(events));
 }
 
 moe_status_t moe_check_status(const void* workspace, moe_stream_t stream) {
