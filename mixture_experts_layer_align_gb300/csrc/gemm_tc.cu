@@ -9,9 +9,18 @@
 // useful work on all 128 lanes, and the weight stream is what the kernel
 // waits on.  The same tiling serves prefill, where N grows to 256.
 //
-// One persistent CTA per SM walks a flat list of work units
-// (row tile of an expert's tokens) x (128-row weight block) [x K slice].
-// Warp roles:
+// Work split ("stream-K"): a tile is (row tile of one expert's tokens) x
+// (128-row weight block) with K/128B steps; the flat (tile, K step) space is
+// cut into one contiguous range per CTA, so every SM streams the same number
+// of weight bytes whatever the expert and tile counts.  Tiles of one expert
+// are ordered weight-block-major so a weight block is reused by all of the
+// expert's row tiles back to back (L2 hits in prefill).  A tile cut by a CTA
+// boundary is finished by its last contributor: in the down projection the
+// partial sums simply add into the combine buffer (the combine is linear); in
+// the gate/up projection every contributor stores its partial accumulators and
+// the last to arrive (per-tile counter) adds them and runs SiLU*up.
+//
+// Warp roles (one persistent CTA per SM):
 //   warp 0      TMA producer: weight block(s) + token tile per K step into a
 //               ring of shared-memory stages (128-byte swizzle, K-major);
 //   warp 1      allocates TMEM and issues tcgen05.mma (one thread), commits
@@ -22,8 +31,8 @@
 //               down:     y * s * topk_weight -> red.add into the fp32 combine
 //                         buffer (expert aggregation fused into the GEMM).
 // The accumulator is double-buffered in TMEM when it fits, so the epilogue of
-// one unit overlaps the MMAs of the next.  Every wait is bounded; on timeout
-// the CTA records kDevErrTimeout and leaves.
+// one segment overlaps the MMAs of the next.  Every wait is bounded; on
+// timeout the CTA records kDevErrTimeout and leaves.
 #include <cuda_bf16.h>
 #include <stdint.h>
 
@@ -37,26 +46,62 @@ namespace {
 constexpr int kSmemLimit = 232448;  // 227 KB opt-in per CTA
 constexpr int kSmemSlack = 1024 + 256;
 constexpr int kMaxStages = 8;
+constexpr uint32_t kEpiBarrier = 1;  // named barrier of the 4 epilogue warps
+constexpr uint32_t kEpiThreads = 128;
 
-struct Unit {
-  int e, row0, n, nb, kb, ke;
+struct Tile {
+  int e, row0, n, nb;
 };
 
-__device__ __forceinline__ Unit decode_unit(const GemmParams& p, int u) {
-  const int per_tile = p.nb_count * p.split_k;
-  const int mt = u / per_tile;
-  const int r = u - mt * per_tile;
-  const int nb = r / p.split_k;
-  const int ks = r - nb * p.split_k;
-  const int4 t = p.mtiles[mt];
-  Unit un;
-  un.e = t.x;
-  un.row0 = t.y;
-  un.n = t.z;
-  un.nb = nb;
-  un.kb = ks * p.k_steps / p.split_k;
-  un.ke = (ks + 1) * p.k_steps / p.split_k;
-  return un;
+// Tile u -> (expert, first row, rows, weight block).  Tiles of one expert with
+// m row tiles occupy [first * nb_count, (first + m) * nb_count) and are ordered
+// (weight block, row tile), so u / nb_count always lands on a row tile of the
+// same expert.
+__device__ __forceinline__ Tile decode_tile(const GemmParams& p, int u) {
+  const int4 a = p.mtiles[u / p.nb_count];
+  const int m = a.z >> 12;
+  const int first = a.w;
+  const int local = u - first * p.nb_count;
+  const int nb = local / m;
+  const int j = local - nb * m;
+  const int4 t = p.mtiles[first + j];
+  Tile r;
+  r.e = t.x;
+  r.row0 = t.y;
+  r.n = t.z & 0xfff;
+  r.nb = nb;
+  return r;
+}
+
+// Segments of this CTA: contiguous range [beg, end) of the flat
+// (tile, K step) index space.
+struct Range {
+  long long beg, end, total;
+};
+
+__device__ __forceinline__ Range cta_range(long long total) {
+  Range r;
+  r.total = total;
+  r.beg = total * blockIdx.x / gridDim.x;
+  r.end = total * (blockIdx.x + 1) / gridDim.x;
+  return r;
+}
+
+// CTA whose range holds flat index i.
+__device__ __forceinline__ int owner_of(long long i, long long total) {
+  return static_cast<int>(((i + 1) * gridDim.x - 1) / total);
+}
+
+__device__ __forceinline__ long long range_begin(int c, long long total) {
+  return total * c / gridDim.x;
+}
+
+// Partial slot of CTA c for a tile starting at flat index t0: slot 1 if c's
+// range began before the tile (the tile is c's last segment), else slot 0.
+__device__ __forceinline__ float* part_slot(const GemmParams& p, int c, long long t0,
+                                            long long total) {
+  const int s = range_begin(c, total) < t0 ? 1 : 0;
+  return p.part + (static_cast<size_t>(c) * 2 + s) * gemm_part_slot_floats(p.bn_max);
 }
 
 template <bool kBF16, bool kSwiGLU>
@@ -64,6 +109,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     moe_gemm_kernel(const __grid_constant__ GemmParams p, const __grid_constant__ CUtensorMap tm_a,
                     const __grid_constant__ CUtensorMap tm_b) {
   extern __shared__ uint8_t smem_raw[];
+  __shared__ int s_last;
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
   const int S = p.stages;
@@ -105,7 +151,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   __syncthreads();
   tc_fence_after_sync();
   const uint32_t tmem = *tmem_slot;
-  const int num_units = p.ctrl->num_mtiles * p.nb_count * p.split_k;
+
+  // everything above overlaps the previous kernel; from here on its outputs are read
+  pdl_wait();
+  pdl_trigger();
+
+  const int K = p.k_steps;
+  const Range rg = cta_range(static_cast<long long>(p.ctrl->num_mtiles) * p.nb_count * K);
   const uint64_t limit = p.timeout_ns;
 
   if (warp == 0) {
@@ -114,10 +166,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       const uint64_t pol_w = policy_evict_first();
       uint32_t it = 0;
       bool ok = true;
-      for (int u = blockIdx.x; u < num_units && ok; u += gridDim.x) {
-        const Unit un = decode_unit(p, u);
-        const int wrow = un.e * p.rows_per_expert + un.nb * 128;
-        for (int kk = un.kb; kk < un.ke; ++kk, ++it) {
+      for (long long i = rg.beg; i < rg.end && ok;) {
+        const int u = static_cast<int>(i / K);
+        const int k0 = static_cast<int>(i - static_cast<long long>(u) * K);
+        const int k1 = static_cast<int>((K < k0 + (rg.end - i) ? static_cast<long long>(K) : k0 + (rg.end - i)));
+        const Tile t = decode_tile(p, u);
+        const int wrow = t.e * p.rows_per_expert + t.nb * 128;
+        for (int kk = k0; kk < k1; ++kk, ++it) {
           const uint32_t s = it % S;
           const uint32_t ph = (it / S) & 1u;
           if (!mbar_wait(empty + s, ph ^ 1u, abort_flag, limit)) {
@@ -126,12 +181,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           }
           uint8_t* sa = smem + static_cast<size_t>(s) * stage_bytes;
           uint8_t* sb = sa + kABytes;
-          mbar_arrive_expect_tx(full + s, kABytes + static_cast<uint32_t>(un.n) * 128u);
+          mbar_arrive_expect_tx(full + s, kABytes + static_cast<uint32_t>(t.n) * 128u);
           const int kc = kk * p.k_elems;
           tma_load_2d_hint(sa, &tm_a, full + s, kc, wrow, pol_w);
           if (kSwiGLU) tma_load_2d_hint(sa + 16384, &tm_a, full + s, kc, wrow + p.up_offset, pol_w);
-          for (int j = 0; j < un.n; j += 16) tma_load_2d(sb + j * 128, &tm_b, full + s, kc, un.row0 + j);
+          for (int j = 0; j < t.n; j += 16) tma_load_2d(sb + j * 128, &tm_b, full + s, kc, t.row0 + j);
         }
+        i += k1 - k0;
       }
       if (!ok) {
         *abort_flag = 1;
@@ -151,8 +207,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       uint32_t it = 0, tt = 0;
       bool ok = true;
       if (p.debug & MOE_DEBUG_FORCE_TIMEOUT) ok = mbar_wait(never, 0, abort_flag, limit);
-      for (int u = blockIdx.x; u < num_units && ok; u += gridDim.x) {
-        const Unit un = decode_unit(p, u);
+      for (long long i = rg.beg; i < rg.end && ok;) {
+        const int u = static_cast<int>(i / K);
+        const int k0 = static_cast<int>(i - static_cast<long long>(u) * K);
+        const int k1 = static_cast<int>((K < k0 + (rg.end - i) ? static_cast<long long>(K) : k0 + (rg.end - i)));
+        const Tile t = decode_tile(p, u);
         const uint32_t a = tt % static_cast<uint32_t>(p.num_acc);
         const uint32_t aph = (tt / static_cast<uint32_t>(p.num_acc)) & 1u;
         if (!mbar_wait(tempty + a, aph ^ 1u, abort_flag, limit)) {
@@ -160,10 +219,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           break;
         }
         tc_fence_after_sync();
-        const uint32_t idesc = umma_idesc(kBF16, 128, un.n);
+        const uint32_t idesc = umma_idesc(kBF16, 128, t.n);
         const uint32_t d0 = tmem + a * static_cast<uint32_t>(p.acc_stride);
         const uint32_t d1 = d0 + static_cast<uint32_t>(p.bn_max);
-        for (int kk = un.kb; kk < un.ke; ++kk, ++it) {
+        for (int kk = k0; kk < k1; ++kk, ++it) {
           const uint32_t s = it % S;
           const uint32_t ph = (it / S) & 1u;
           if (!mbar_wait(full + s, ph, abort_flag, limit)) {
@@ -177,7 +236,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           const uint64_t db = sdesc_kmajor_sw128(sa + kABytes);
 #pragma unroll
           for (int k4 = 0; k4 < 4; ++k4) {
-            const uint32_t acc = (kk > un.kb || k4 > 0) ? 1u : 0u;
+            const uint32_t acc = (kk > k0 || k4 > 0) ? 1u : 0u;
             // +2 in the start-address field = +32 bytes of K inside the swizzle atom
             if (kBF16) {
               umma_bf16(d0, da0 + 2 * k4, db + 2 * k4, idesc, acc);
@@ -192,6 +251,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         if (!ok) break;
         umma_commit(tfull + a);
         ++tt;
+        i += k1 - k0;
       }
       if (!ok) {
         *abort_flag = 1;
@@ -207,54 +267,106 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     float amax = 0.f;
     uint32_t tt = 0;
     bool ok = true;
-    for (int u = blockIdx.x; u < num_units; u += gridDim.x) {
-      const Unit un = decode_unit(p, u);
+    for (long long i = rg.beg; i < rg.end;) {
+      const int u = static_cast<int>(i / K);
+      const int k0 = static_cast<int>(i - static_cast<long long>(u) * K);
+      const int k1 = static_cast<int>((K < k0 + (rg.end - i) ? static_cast<long long>(K) : k0 + (rg.end - i)));
+      const Tile t = decode_tile(p, u);
       const uint32_t a = tt % static_cast<uint32_t>(p.num_acc);
       const uint32_t aph = (tt / static_cast<uint32_t>(p.num_acc)) & 1u;
       int got = 0;
       if (lane == 0) got = mbar_wait(tfull + a, aph, abort_flag, limit) ? 1 : 0;
       got = __shfl_sync(0xffffffffu, got, 0);
-      if (!got) {
+      // all four epilogue warps take the same branch (they share named barriers below)
+      if (!named_barrier_and(kEpiBarrier, kEpiThreads, got != 0)) {
         ok = false;
         break;
       }
       tc_fence_after_sync();
-      const float sc = kBF16 ? 1.f : act_s * p.w_scale[un.e];
+      const float sc = kBF16 ? 1.f : act_s * p.w_scale[t.e];
       const uint32_t tbase = tmem + (static_cast<uint32_t>(q * 32) << 16) +
                              a * static_cast<uint32_t>(p.acc_stride);
-      const int col = un.nb * 128 + row_l;
-      for (int c0 = 0; c0 < un.n; c0 += 16) {
-        if (kSwiGLU) {
-          float g[16], v[16];
-          tmem_ld16x2(tbase + c0, tbase + p.bn_max + c0, g, v);
+      const int col = t.nb * 128 + row_l;
+      if (kSwiGLU) {
+        const bool whole = (k0 == 0 && k1 == K);
+        bool finish = whole;
+        long long t0 = static_cast<long long>(u) * K;
+        int c_first = 0, c_last = 0;
+        if (!whole) {
+          // store this contributor's partial, then count arrivals on the tile
+          c_first = owner_of(t0, rg.total);
+          c_last = owner_of(t0 + K - 1, rg.total);
+          float* mine = part_slot(p, blockIdx.x, t0, rg.total);
+          for (int c0 = 0; c0 < t.n; c0 += 16) {
+            float g[16], v[16];
+            tmem_ld16x2(tbase + c0, tbase + p.bn_max + c0, g, v);
 #pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            const int r = un.row0 + c0 + j;
-            const float gv = g[j] * sc;
-            const float uv = v[j] * sc;
-            const float hv = gv / (1.f + __expf(-gv)) * uv;
-            const size_t at = static_cast<size_t>(r) * p.ldh + col;
-            if (kBF16) {
-              // bf16 weights: h feeds the bf16 down-projection MMA directly
-              static_cast<__nv_bfloat16*>(p.h_out)[at] = __float2bfloat16_rn(hv);
-            } else {
-              // FP8: h stays fp32 until its per-tensor scale is known; an
-              // intermediate bf16 rounding would move values across E4M3
-              // rounding boundaries and cost percent-level output error
-              static_cast<float*>(p.h_out)[at] = hv;
-              if (p.sorted_ids[r] < p.P) amax = fmaxf(amax, fabsf(hv));
+            for (int j = 0; j < 16; ++j) {
+              mine[static_cast<size_t>(c0 + j) * 128 + row_l] = g[j];
+              mine[static_cast<size_t>(p.bn_max + c0 + j) * 128 + row_l] = v[j];
             }
           }
-        } else {
+          __threadfence();
+          named_barrier(kEpiBarrier, kEpiThreads);
+          if (threadIdx.x == 64) {
+            // contributors: CTAs in [c_first, c_last] whose range is not empty
+            int n_seg = 0;
+            for (int c = c_first; c <= c_last; ++c)
+              n_seg += range_begin(c, rg.total) < range_begin(c + 1, rg.total) ? 1 : 0;
+            s_last = (atomicAdd(p.tile_cnt + u, 1) == n_seg - 1) ? 1 : 0;
+          }
+          named_barrier(kEpiBarrier, kEpiThreads);
+          finish = s_last != 0;
+          if (finish) __threadfence();
+        }
+        if (finish) {
+          for (int c0 = 0; c0 < t.n; c0 += 16) {
+            float g[16], v[16];
+            tmem_ld16x2(tbase + c0, tbase + p.bn_max + c0, g, v);
+            if (!whole) {
+              for (int c = c_first; c <= c_last; ++c) {
+                if (c == static_cast<int>(blockIdx.x) ||
+                    range_begin(c, rg.total) == range_begin(c + 1, rg.total))
+                  continue;
+                const float* other = part_slot(p, c, t0, rg.total);
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                  g[j] += __ldcg(other + static_cast<size_t>(c0 + j) * 128 + row_l);
+                  v[j] += __ldcg(other + static_cast<size_t>(p.bn_max + c0 + j) * 128 + row_l);
+                }
+              }
+            }
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+              const int r = t.row0 + c0 + j;
+              const float gv = g[j] * sc;
+              const float uv = v[j] * sc;
+              const float hv = gv / (1.f + __expf(-gv)) * uv;
+              const size_t at = static_cast<size_t>(r) * p.ldh + col;
+              if (kBF16) {
+                // bf16 weights: h feeds the bf16 down-projection MMA directly
+                static_cast<__nv_bfloat16*>(p.h_out)[at] = __float2bfloat16_rn(hv);
+              } else {
+                // FP8: h stays fp32 until its per-tensor scale is known; an
+                // intermediate bf16 rounding would move values across E4M3
+                // rounding boundaries and cost percent-level output error
+                static_cast<float*>(p.h_out)[at] = hv;
+                if (p.sorted_ids[r] < p.P) amax = fmaxf(amax, fabsf(hv));
+              }
+            }
+          }
+        }
+      } else {
+        for (int c0 = 0; c0 < t.n; c0 += 16) {
           float y[16];
           tmem_ld16(tbase + c0, y);
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
-            const int r = un.row0 + c0 + j;
+            const int r = t.row0 + c0 + j;
             const int pid = p.sorted_ids[r];
             if (pid < p.P) {
-              const int t = pid / p.top_k;
-              red_add_f32(p.acc_out + static_cast<size_t>(t) * p.ldo + col,
+              const int tok = pid / p.top_k;
+              red_add_f32(p.acc_out + static_cast<size_t>(tok) * p.ldo + col,
                           y[j] * sc * p.topk_w[pid]);
             }
           }
@@ -264,6 +376,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(tempty + a);
       ++tt;
+      i += k1 - k0;
     }
     if (kSwiGLU && !kBF16) {
 #pragma unroll
@@ -297,8 +410,8 @@ cudaError_t launch_one(const GemmParams& p, const CUtensorMap& ta, const CUtenso
     configured_device = dev;
   }
   const size_t smem = gemm_smem_bytes(kSwiGLU, p.bn_max, p.stages);
-  moe_gemm_kernel<kBF16, kSwiGLU><<<grid, kGemmThreads, smem, st>>>(p, ta, tb);
-  return cudaGetLastError();
+  return launch_pdl(moe_gemm_kernel<kBF16, kSwiGLU>, dim3(grid), dim3(kGemmThreads), smem, st, p,
+                    ta, tb);
 }
 
 }  // namespace

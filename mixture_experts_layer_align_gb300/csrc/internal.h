@@ -7,6 +7,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <utility>
+
 #include "moe_gb300.h"
 
 namespace moe {
@@ -19,6 +21,25 @@ constexpr int kDevErrRange = 2;
 // M = 128 takes N in multiples of 16, so each expert's token segment is
 // padded to 16 rows.
 constexpr int kAlignBlock = 16;
+
+// Launch with programmatic stream serialisation: the kernel may start while
+// its predecessor drains; every kernel of this library calls pdl_wait()
+// before touching global memory, so stream order is kept for the data.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t st, Args&&... args) {
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 // Per-call control words, at the start of the workspace.
 struct Ctrl {
@@ -37,7 +58,7 @@ constexpr int kRouteWarps = 8;  // tokens per router CTA (one warp per token)
 
 cudaError_t launch_route_topk(const float* logits, int T, int E, int k, int renorm, int32_t* ids,
                               float* wts, const __nv_bfloat16* x, int H, float* amax_partials,
-                              Ctrl* ctrl, cudaStream_t st);
+                              Ctrl* ctrl, int* zero_ints, int n_zero, cudaStream_t st);
 inline int route_grid(int T) { return (T + kRouteWarps - 1) / kRouteWarps; }
 
 struct AlignParams {
@@ -75,10 +96,11 @@ cudaError_t launch_quantize_e4m3(const __nv_bfloat16* x, long long n, uint8_t* x
 
 // ------------------------------------------------------------ grouped GEMM
 struct GemmParams {
+  // Row tiles {expert, first row, rows | (tiles of this expert << 12), index of
+  // the expert's first tile}, written by the alignment kernel.
   const int4* mtiles;
   Ctrl* ctrl;
   int nb_count;         // 128-row weight blocks per expert (I/128 or H/128)
-  int split_k;          // K slices per tile (down projection only)
   int k_steps;          // K / (128 bytes of K)
   int k_elems;          // elements of K per step: 128 (E4M3) or 64 (bf16)
   int bn_max;           // max tokens (MMA N) per row tile
@@ -97,9 +119,16 @@ struct GemmParams {
   int ldh;
   float* acc_out;        // down: [T, H] fp32
   int ldo;
+  // gate/up tiles split across CTAs: per-tile arrival counters (zeroed by the
+  // router kernel) and two partial-accumulator slots per CTA
+  int* tile_cnt;
+  float* part;
   unsigned long long timeout_ns;
   int debug;
 };
+
+// Partial-accumulator slot (gate and up, bn_max columns x 128 rows, fp32).
+__host__ __device__ inline size_t gemm_part_slot_floats(int bn_max) { return static_cast<size_t>(2) * bn_max * 128; }
 
 constexpr int kGemmThreads = 192;  // warp 0 TMA, warp 1 MMA, warps 2..5 epilogue
 size_t gemm_smem_bytes(bool swiglu, int bn_max, int stages);

@@ -74,14 +74,37 @@ bool make_tmap(CUtensorMap* m, const void* base, bool bf16, uint64_t k_elems, ui
   return r == CUDA_SUCCESS;
 }
 
+int round_up16(long long v) { return static_cast<int>((v + 15) / 16 * 16); }
+
+// Row-tile width (MMA N) of the expert GEMMs: twice the mean rows per touched
+// expert, 64..256.  Any value is correct; wider tiles re-read each weight
+// block fewer times, narrower ones leave more stages of weights in flight.
+int choose_bn_max(long long P, int E) {
+  const long long touched = std::min<long long>(E, P);
+  const long long mean_rows = touched > 0 ? (P + touched - 1) / touched : 1;
+  return std::min(256, std::max(64, round_up16(2 * mean_rows)));
+}
+
+// CTAs the persistent GEMMs may use on the current device (also sizes the
+// split-tile partial slots); 256 when no device can be queried.
+int gemm_ctas() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 256;
+  const DeviceInfo d = device_info(dev);
+  return d.num_sms > 0 ? std::min(d.num_sms, 256) : 256;
+}
+
 // Workspace layout of the fused forward (all regions 256-byte aligned).
 struct Layout {
   long long P = 0;
   int pad_max = 0;     // upper bound of aligned rows: P + E*(16-1)
   int max_mtiles = 0;  // upper bound of GEMM row tiles
   int n_partials = 0;  // router CTAs
+  int bn_max = 0;
+  int ctas = 0;
+  int n_tile_cnt = 0;
   size_t ctrl = 0, partials = 0, ids = 0, wts = 0, counts = 0, offsets = 0, sorted = 0,
-         mtiles = 0, xs = 0, h = 0, hq = 0, acc = 0, total = 0;
+         mtiles = 0, tile_cnt = 0, part = 0, xs = 0, h = 0, hq = 0, acc = 0, total = 0;
 };
 
 Layout make_layout(int T, int H, int I, int E, int k, bool fp8) {
@@ -90,6 +113,9 @@ Layout make_layout(int T, int H, int I, int E, int k, bool fp8) {
   L.pad_max = static_cast<int>(L.P + static_cast<long long>(E) * (kAlignBlock - 1));
   L.max_mtiles = L.pad_max / kAlignBlock + 1;
   L.n_partials = route_grid(T);
+  L.bn_max = choose_bn_max(L.P, E);
+  L.ctas = gemm_ctas();
+  L.n_tile_cnt = L.max_mtiles * (I / 128);
   size_t off = 0;
   auto take = [&](size_t bytes) {
     const size_t at = off;
@@ -104,6 +130,8 @@ Layout make_layout(int T, int H, int I, int E, int k, bool fp8) {
   L.offsets = take(sizeof(int32_t) * (E + 1));
   L.sorted = take(sizeof(int32_t) * L.pad_max);
   L.mtiles = take(sizeof(int4) * L.max_mtiles);
+  L.tile_cnt = take(sizeof(int) * static_cast<size_t>(L.n_tile_cnt));
+  L.part = take(sizeof(float) * 2 * static_cast<size_t>(L.ctas) * gemm_part_slot_floats(L.bn_max));
   L.xs = take(static_cast<size_t>(L.pad_max) * H * (fp8 ? 1 : 2));
   L.h = take(static_cast<size_t>(L.pad_max) * I * (fp8 ? 4 : 2));
   L.hq = take(fp8 ? static_cast<size_t>(L.pad_max) * I : 0);
@@ -119,8 +147,6 @@ int next_pow2(int v) {
   while (p < v) p <<= 1;
   return p;
 }
-
-int round_up16(long long v) { return static_cast<int>((v + 15) / 16 * 16); }
 
 moe_status_t check_device(DeviceInfo* out) {
   int dev = 0;
@@ -162,7 +188,7 @@ moe_status_t moe_route_topk(const float* logits, int T, int E, int top_k, int re
   moe_status_t s = check_device(&d);
   if (s != MOE_OK) return s;
   return launch_route_topk(logits, T, E, top_k, renormalize, topk_ids, topk_w, nullptr, 0,
-                           nullptr, nullptr, stream) == cudaSuccess
+                           nullptr, nullptr, nullptr, 0, stream) == cudaSuccess
              ? MOE_OK
              : MOE_ERR_CUDA;
 }
@@ -275,18 +301,17 @@ moe_status_t fused_forward_impl(const moe_fused_args* a, void* workspace, size_t
   uint8_t* hq = ws + L.hq;
   float* acc = reinterpret_cast<float*>(ws + L.acc);
 
-  // Row-tile width: twice the mean rows per touched expert, 64..256 (any
-  // value is correct; larger tiles re-read each weight block fewer times).
   const long long touched = std::min<long long>(E, P);
-  const long long mean_rows = (P + touched - 1) / touched;
-  const int bn_max = std::min(256, std::max(64, round_up16(2 * mean_rows)));
+  const int bn_max = L.bn_max;
+  int* tile_cnt = reinterpret_cast<int*>(ws + L.tile_cnt);
+  float* part = reinterpret_cast<float*>(ws + L.part);
 
-  if (events && cudaEventRecord(events[0], stream) != cudaSuccess) return MOE_ERR_CUDA;
   // 1. routing (+ per-CTA amax of x, + reset of the control words)
   cudaStream_t s = stream;
+  if (events && cudaEventRecord(events[0], stream) != cudaSuccess) return MOE_ERR_CUDA;
   if (launch_route_topk(a->router_logits, T, E, k, a->renormalize, ids, wts,
                         static_cast<const __nv_bfloat16*>(a->x), H, fp8 ? partials : nullptr, ctrl,
-                        s) != cudaSuccess)
+                        tile_cnt, L.n_tile_cnt, s) != cudaSuccess)
     return MOE_ERR_CUDA;
   if (events && cudaEventRecord(events[1], stream) != cudaSuccess) return MOE_ERR_CUDA;
   // 2. alignment by expert, GEMM row tiles, s_x
@@ -326,14 +351,13 @@ moe_status_t fused_forward_impl(const moe_fused_args* a, void* workspace, size_t
 
   const int k_elems = fp8 ? 128 : 64;
   const long long max_tiles = std::min<long long>(L.max_mtiles, (L.pad_max + bn_max - 1) / bn_max + touched);
+  const int ctas = std::min(L.ctas, dev.num_sms);
 
-  if (events && cudaEventRecord(events[3], stream) != cudaSuccess) return MOE_ERR_CUDA;
   // 4. gate/up GEMM + SiLU*up epilogue
   GemmParams g1{};
   g1.mtiles = mtiles;
   g1.ctrl = ctrl;
   g1.nb_count = I / 128;
-  g1.split_k = 1;
   g1.k_steps = H / k_elems;
   g1.k_elems = k_elems;
   g1.bn_max = bn_max;
@@ -351,20 +375,25 @@ moe_status_t fused_forward_impl(const moe_fused_args* a, void* workspace, size_t
   g1.topk_w = wts;
   g1.h_out = h;
   g1.ldh = I;
+  g1.tile_cnt = tile_cnt;
+  g1.part = part;
   g1.timeout_ns = (a->debug_flags & MOE_DEBUG_FORCE_TIMEOUT) ? MOE_DEBUG_TIMEOUT_MS * 1000000ull
                                                              : kWaitLimitNs;
   g1.debug = a->debug_flags;
-  const long long units1 = max_tiles * g1.nb_count;
-  const int grid1 = static_cast<int>(std::max<long long>(1, std::min<long long>(dev.num_sms, units1)));
+  const long long work1 = max_tiles * g1.nb_count * g1.k_steps;
+  const int grid1 = static_cast<int>(std::max<long long>(1, std::min<long long>(ctas, work1)));
+  if (events && cudaEventRecord(events[3], stream) != cudaSuccess) return MOE_ERR_CUDA;
   if (launch_gemm(bf16, true, g1, tm_w13, tm_xs, grid1, s) != cudaSuccess) return MOE_ERR_CUDA;
 
-  if (events && cudaEventRecord(events[4], stream) != cudaSuccess) return MOE_ERR_CUDA;
   // 5. dynamic scale of h and its E4M3 codes
-  if (fp8 && launch_quant_h(static_cast<const float*>(h), I, ctrl, hq, L.pad_max, dev.num_sms, s) != cudaSuccess)
+  if (events && cudaEventRecord(events[4], stream) != cudaSuccess) return MOE_ERR_CUDA;
+  if (fp8 && launch_quant_h(static_cast<const float*>(h), I, ctrl, hq, L.pad_max, dev.num_sms,
+                            s) != cudaSuccess)
     return MOE_ERR_CUDA;
 
+  // 6. down GEMM + weighted scatter-combine (tiles cut across CTAs add into
+  //    the combine buffer like any other partial sum)
   if (events && cudaEventRecord(events[5], stream) != cudaSuccess) return MOE_ERR_CUDA;
-  // 6. down GEMM + weighted scatter-combine (split over K when few units)
   GemmParams g2 = g1;
   g2.nb_count = H / 128;
   g2.k_steps = I / k_elems;
@@ -379,16 +408,14 @@ moe_status_t fused_forward_impl(const moe_fused_args* a, void* workspace, size_t
   g2.h_out = nullptr;
   g2.acc_out = acc;
   g2.ldo = H;
-  const long long base_units2 = touched * g2.nb_count;
-  int split = static_cast<int>((2LL * dev.num_sms + base_units2 - 1) / base_units2);
-  split = std::max(1, std::min({split, g2.k_steps, 16}));
-  g2.split_k = split;
-  const long long units2 = max_tiles * g2.nb_count * split;
-  const int grid2 = static_cast<int>(std::max<long long>(1, std::min<long long>(dev.num_sms, units2)));
+  g2.tile_cnt = nullptr;
+  g2.part = nullptr;
+  const long long work2 = max_tiles * g2.nb_count * g2.k_steps;
+  const int grid2 = static_cast<int>(std::max<long long>(1, std::min<long long>(ctas, work2)));
   if (launch_gemm(bf16, false, g2, tm_w2, tm_h, grid2, s) != cudaSuccess) return MOE_ERR_CUDA;
 
-  if (events && cudaEventRecord(events[6], stream) != cudaSuccess) return MOE_ERR_CUDA;
   // 7. fp32 combine buffer -> bf16 output
+  if (events && cudaEventRecord(events[6], stream) != cudaSuccess) return MOE_ERR_CUDA;
   if (launch_finalize(acc, static_cast<__nv_bfloat16*>(a->out), static_cast<long long>(T) * H,
                       dev.num_sms, s) != cudaSuccess)
     return MOE_ERR_CUDA;

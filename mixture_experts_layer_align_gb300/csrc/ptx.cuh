@@ -25,6 +25,35 @@ __device__ __forceinline__ uint32_t lane_id() {
   return l;
 }
 
+// ---------------------------------------------------------------- launch order
+// Programmatic dependent launch: wait until the preceding grid in the stream
+// has completed and its memory is visible (a no-op without the launch
+// attribute), and allow the next grid to begin its prologue.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+__device__ __forceinline__ void pdl_trigger() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// Barrier over `count` threads (a multiple of 32) on hardware barrier `id`.
+__device__ __forceinline__ void named_barrier(uint32_t id, uint32_t count) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
+// Same, returning the AND of `v` over the participating threads.
+__device__ __forceinline__ bool named_barrier_and(uint32_t id, uint32_t count, bool v) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred pi, po;\n\t"
+      "setp.ne.u32 pi, %3, 0;\n\t"
+      "bar.red.and.pred po, %1, %2, pi;\n\t"
+      "selp.u32 %0, 1, 0, po;\n\t}"
+      : "=r"(r)
+      : "r"(id), "r"(count), "r"(static_cast<uint32_t>(v))
+      : "memory");
+  return r != 0;
+}
+
 // ---------------------------------------------------------------- mbarrier
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count)

@@ -11,6 +11,8 @@
 #include <math.h>
 #include <stdint.h>
 
+#include <algorithm>
+
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -99,14 +101,18 @@ __global__ void __launch_bounds__(kRouteWarps * 32)
     route_topk_kernel(const float* __restrict__ logits, int T, int E, int k, int renorm,
                       int32_t* __restrict__ ids, float* __restrict__ wts,
                       const __nv_bfloat16* __restrict__ x, int H, float* __restrict__ amax_partials,
-                      Ctrl* ctrl) {
+                      Ctrl* ctrl, int* __restrict__ zero_ints, int n_zero) {
   extern __shared__ float s_logits[];
   __shared__ float s_amax[kRouteWarps];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  pdl_wait();
+  pdl_trigger();
   if (ctrl != nullptr && blockIdx.x == 0 && threadIdx.x == 0) {
     ctrl->err = 0;
     ctrl->amax_h = 0u;
   }
+  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n_zero; i += gridDim.x * blockDim.x)
+    zero_ints[i] = 0;
   const int t = blockIdx.x * kRouteWarps + warp;
   float xmax = 0.f;
   if (t < T) {
@@ -210,6 +216,8 @@ __global__ void __launch_bounds__(kAlignThreads) align_kernel(AlignParams p) {
   const int seglen = (clen + 31) / 32;
   const int s0 = cs + warp * seglen;
   const int s1 = min(s0 + seglen, ce);
+  pdl_wait();
+  pdl_trigger();
 
   for (int e = tid; e < E; e += kAlignThreads) {
     hist_all[e] = 0;
@@ -299,7 +307,8 @@ __global__ void __launch_bounds__(kAlignThreads) align_kernel(AlignParams p) {
 
   if (p.mtiles != nullptr) {
     // GEMM row tiles: each expert's padded segment split into
-    // ceil(padded / bn_max) tiles of equal size (multiples of bm)
+    // ceil(padded / bn_max) tiles of equal size (multiples of bm); each entry
+    // also carries the expert's tile count and first tile index
     const int nt = padded > 0 ? (padded + p.bn_max - 1) / p.bn_max : 0;
     int n_tiles = 0;
     const int first = block_exclusive_scan_1024(nt, s_tmp, &n_tiles);
@@ -308,7 +317,7 @@ __global__ void __launch_bounds__(kAlignThreads) align_kernel(AlignParams p) {
       const int o = seg_off[tid];
       for (int j = 0; j < nt; ++j) {
         const int rows = min(per, padded - j * per);
-        p.mtiles[first + j] = make_int4(tid, o + j * per, rows, 0);
+        p.mtiles[first + j] = make_int4(tid, o + j * per, rows | (nt << 12), first);
       }
     }
     // activation scale of x from the router's per-CTA amax values
@@ -327,52 +336,55 @@ __global__ void __launch_bounds__(kAlignThreads) align_kernel(AlignParams p) {
 }
 
 // ------------------------------------------------------------------ gather
-// One warp per aligned row: the row of x of the pair's token, quantised to
-// E4M3 with s_x (or copied as bf16); padding rows are zero.  The same grid
-// zeroes the fp32 combine buffer.
+// One thread per 16 elements of an aligned row: the pair's token row of x,
+// quantised to E4M3 with s_x (or copied as bf16); padding rows are zero.  The
+// same grid zeroes the fp32 combine buffer.
 __global__ void __launch_bounds__(256)
     gather_x_kernel(const __nv_bfloat16* __restrict__ x, int H, const int32_t* __restrict__ sorted_ids,
                     const Ctrl* __restrict__ ctrl, int P, int k, void* __restrict__ xs, int fp8,
                     float* __restrict__ acc, long long acc_elems) {
-  const int lane = threadIdx.x & 31;
-  const int gw = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-  const int nw = (gridDim.x * blockDim.x) >> 5;
-  const int rows = ctrl->num_padded;
+  pdl_wait();
+  pdl_trigger();
+  const long long rows = ctrl->num_padded;
+  const int per_row = H / 16;
+  const long long n = rows * per_row;
+  const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
+  const long long tid = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (fp8) {
     const float s = ctrl->s_x;
-    uint8_t* dst_all = static_cast<uint8_t*>(xs);
-    for (int r = gw; r < rows; r += nw) {
+    uint4* dst = static_cast<uint4*>(xs);
+    for (long long i = tid; i < n; i += stride) {
+      const long long r = i / per_row;
+      const int c = static_cast<int>(i - r * per_row);
       const int q = sorted_ids[r];
-      uint4* dst = reinterpret_cast<uint4*>(dst_all + static_cast<size_t>(r) * H);
+      uint4 v = make_uint4(0, 0, 0, 0);
       if (q < P) {
         const uint4* src = reinterpret_cast<const uint4*>(x + static_cast<size_t>(q / k) * H);
-        for (int c = lane; c < H / 16; c += 32) {
-          const uint2 a = quant8(__ldg(src + 2 * c), s);
-          const uint2 b = quant8(__ldg(src + 2 * c + 1), s);
-          dst[c] = make_uint4(a.x, a.y, b.x, b.y);
-        }
-      } else {
-        for (int c = lane; c < H / 16; c += 32) dst[c] = make_uint4(0, 0, 0, 0);
+        const uint2 a = quant8(__ldg(src + 2 * c), s);
+        const uint2 b = quant8(__ldg(src + 2 * c + 1), s);
+        v = make_uint4(a.x, a.y, b.x, b.y);
       }
+      dst[i] = v;
     }
   } else {
-    __nv_bfloat16* dst_all = static_cast<__nv_bfloat16*>(xs);
-    for (int r = gw; r < rows; r += nw) {
+    uint4* dst = static_cast<uint4*>(xs);
+    for (long long i = tid; i < n; i += stride) {
+      const long long r = i / per_row;
+      const int c = static_cast<int>(i - r * per_row);
       const int q = sorted_ids[r];
-      uint4* dst = reinterpret_cast<uint4*>(dst_all + static_cast<size_t>(r) * H);
+      uint4 v0 = make_uint4(0, 0, 0, 0), v1 = v0;
       if (q < P) {
         const uint4* src = reinterpret_cast<const uint4*>(x + static_cast<size_t>(q / k) * H);
-        for (int c = lane; c < H / 8; c += 32) dst[c] = __ldg(src + c);
-      } else {
-        for (int c = lane; c < H / 8; c += 32) dst[c] = make_uint4(0, 0, 0, 0);
+        v0 = __ldg(src + 2 * c);
+        v1 = __ldg(src + 2 * c + 1);
       }
+      dst[2 * i] = v0;
+      dst[2 * i + 1] = v1;
     }
   }
   float4* a4 = reinterpret_cast<float4*>(acc);
   const long long n4 = acc_elems / 4;
-  for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < n4;
-       i += static_cast<long long>(gridDim.x) * blockDim.x)
-    a4[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (long long i = tid; i < n4; i += stride) a4[i] = make_float4(0.f, 0.f, 0.f, 0.f);
 }
 
 // ------------------------------------------------------------------ h quant
@@ -383,6 +395,8 @@ __device__ __forceinline__ uint32_t quant4(float4 v, float s) {
 
 __global__ void __launch_bounds__(256)
     quant_h_kernel(const float* __restrict__ h, int I, Ctrl* ctrl, uint8_t* __restrict__ hq) {
+  pdl_wait();
+  pdl_trigger();
   const float s = scale_from_amax(__uint_as_float(ctrl->amax_h));
   if (blockIdx.x == 0 && threadIdx.x == 0) ctrl->s_h = s;
   const long long n16 = static_cast<long long>(ctrl->num_padded) * I / 16;
@@ -402,6 +416,8 @@ __global__ void __launch_bounds__(256)
 // ------------------------------------------------------------------ finalize
 __global__ void __launch_bounds__(256)
     finalize_kernel(const float* __restrict__ acc, __nv_bfloat16* __restrict__ out, long long n8) {
+  pdl_wait();
+  pdl_trigger();
   const float4* a = reinterpret_cast<const float4*>(acc);
   uint4* o = reinterpret_cast<uint4*>(out);
   for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < n8;
@@ -424,6 +440,8 @@ __global__ void __launch_bounds__(256)
 __global__ void __launch_bounds__(256)
     amax_kernel(const __nv_bfloat16* __restrict__ x, long long n8, float* __restrict__ partials) {
   __shared__ float s_red[8];
+  pdl_wait();
+  pdl_trigger();
   const uint4* src = reinterpret_cast<const uint4*>(x);
   float m = 0.f;
   for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < n8;
@@ -443,6 +461,8 @@ __global__ void __launch_bounds__(256)
     quant_x_kernel(const __nv_bfloat16* __restrict__ x, long long n16, const float* __restrict__ partials,
                    int n_partials, uint8_t* __restrict__ xq, float* __restrict__ scale) {
   __shared__ float s_scale;
+  pdl_wait();
+  pdl_trigger();
   if (threadIdx.x < 32) {
     float m = 0.f;
     for (int i = threadIdx.x; i < n_partials; i += 32) m = fmaxf(m, partials[i]);
@@ -465,13 +485,23 @@ __global__ void __launch_bounds__(256)
 }  // namespace
 
 // ------------------------------------------------------------------ launchers
+namespace {
+int capped_grid(long long work, long long per_block, int num_sms, int per_sm) {
+  long long g = (work + per_block - 1) / per_block;
+  const long long cap = static_cast<long long>(num_sms) * per_sm;
+  if (g > cap) g = cap;
+  if (g < 1) g = 1;
+  return static_cast<int>(g);
+}
+}  // namespace
+
 cudaError_t launch_route_topk(const float* logits, int T, int E, int k, int renorm, int32_t* ids,
                               float* wts, const __nv_bfloat16* x, int H, float* amax_partials,
-                              Ctrl* ctrl, cudaStream_t st) {
+                              Ctrl* ctrl, int* zero_ints, int n_zero, cudaStream_t st) {
   const size_t smem = static_cast<size_t>(kRouteWarps) * E * sizeof(float);
-  route_topk_kernel<<<route_grid(T), kRouteWarps * 32, smem, st>>>(logits, T, E, k, renorm, ids,
-                                                                    wts, x, H, amax_partials, ctrl);
-  return cudaGetLastError();
+  return launch_pdl(route_topk_kernel, dim3(route_grid(T)), dim3(kRouteWarps * 32), smem, st,
+                    logits, T, E, k, renorm, ids, wts, x, H, amax_partials, ctrl, zero_ints,
+                    n_zero);
 }
 
 int align_chunk() { return kAlignChunk; }
@@ -488,54 +518,39 @@ cudaError_t launch_align(const AlignParams& p, cudaStream_t st) {
     configured_device = dev;
   }
   const int grid = p.P > 0 ? (p.P + p.chunk - 1) / p.chunk : 1;
-  align_kernel<<<grid, kAlignThreads, smem, st>>>(p);
-  return cudaGetLastError();
+  return launch_pdl(align_kernel, dim3(grid), dim3(kAlignThreads), smem, st, p);
 }
 
 cudaError_t launch_gather_x(const __nv_bfloat16* x, int H, const int32_t* sorted_ids,
                             const Ctrl* ctrl, int P, int k, void* xs, bool fp8, float* acc,
                             long long acc_elems, int max_rows, int num_sms, cudaStream_t st) {
-  int grid = (max_rows + 7) / 8;
-  const int cap = num_sms * 8;
-  if (grid > cap) grid = cap;
-  if (grid < 1) grid = 1;
-  gather_x_kernel<<<grid, 256, 0, st>>>(x, H, sorted_ids, ctrl, P, k, xs, fp8 ? 1 : 0, acc,
-                                        acc_elems);
-  return cudaGetLastError();
+  const long long work = std::max(static_cast<long long>(max_rows) * (H / 16), acc_elems / 4);
+  const int grid = capped_grid(work, 256, num_sms, 8);
+  return launch_pdl(gather_x_kernel, dim3(grid), dim3(256), 0, st, x, H, sorted_ids, ctrl, P, k,
+                    xs, fp8 ? 1 : 0, acc, acc_elems);
 }
 
 cudaError_t launch_quant_h(const float* h, int I, Ctrl* ctrl, uint8_t* hq, int max_rows,
                            int num_sms, cudaStream_t st) {
-  const long long n16 = static_cast<long long>(max_rows) * I / 16;
-  long long grid = (n16 + 255) / 256;
-  const long long cap = static_cast<long long>(num_sms) * 8;
-  if (grid > cap) grid = cap;
-  if (grid < 1) grid = 1;
-  quant_h_kernel<<<static_cast<int>(grid), 256, 0, st>>>(h, I, ctrl, hq);
-  return cudaGetLastError();
+  const int grid = capped_grid(static_cast<long long>(max_rows) * I / 16, 256, num_sms, 8);
+  return launch_pdl(quant_h_kernel, dim3(grid), dim3(256), 0, st, h, I, ctrl, hq);
 }
 
 cudaError_t launch_finalize(const float* acc, __nv_bfloat16* out, long long n, int num_sms,
                             cudaStream_t st) {
-  const long long n8 = n / 8;
-  long long grid = (n8 + 255) / 256;
-  const long long cap = static_cast<long long>(num_sms) * 8;
-  if (grid > cap) grid = cap;
-  if (grid < 1) grid = 1;
-  finalize_kernel<<<static_cast<int>(grid), 256, 0, st>>>(acc, out, n8);
-  return cudaGetLastError();
+  const int grid = capped_grid(n / 8, 256, num_sms, 8);
+  return launch_pdl(finalize_kernel, dim3(grid), dim3(256), 0, st, acc, out, n / 8);
 }
 
 cudaError_t launch_quantize_e4m3(const __nv_bfloat16* x, long long n, uint8_t* xq, float* scale,
                                  float* partials, int n_partials, cudaStream_t st) {
-  amax_kernel<<<n_partials, 256, 0, st>>>(x, n / 8, partials);
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e = launch_pdl(amax_kernel, dim3(n_partials), dim3(256), 0, st, x, n / 8, partials);
   if (e != cudaSuccess) return e;
   long long grid = (n / 16 + 255) / 256;
   if (grid > 4096) grid = 4096;
   if (grid < 1) grid = 1;
-  quant_x_kernel<<<static_cast<int>(grid), 256, 0, st>>>(x, n / 16, partials, n_partials, xq, scale);
-  return cudaGetLastError();
+  return launch_pdl(quant_x_kernel, dim3(static_cast<int>(grid)), dim3(256), 0, st, x, n / 16,
+                    static_cast<const float*>(partials), n_partials, xq, scale);
 }
 
 }  // namespace moe
