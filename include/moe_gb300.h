@@ -167,6 +167,12 @@ moe_status_t moe_check_status(const void* workspace, moe_stream_t stream);
 /* Static description of a status code. */
 const char* moe_status_string(moe_status_t status);
 
+/* Text naming the last failing CUDA runtime/driver call made by this library on
+ * the calling host thread and its error code (after a MOE_ERR_CUDA status).
+ * Thread-local storage owned by the library, valid until that thread's next
+ * failing call. */
+const char* moe_last_error_detail(void);
+
 #ifdef __cplusplus
 }
 #endif

@@ -31,7 +31,10 @@ _lib = None
 class MoeError(RuntimeError):
     def __init__(self, status: int, where: str):
         self.status = status
-        super().__init__(f"{where}: {STATUS_NAMES.get(status, status)} ({status_string(status)})")
+        msg = f"{where}: {STATUS_NAMES.get(status, status)} ({status_string(status)})"
+        if status == 4:
+            msg += f" [{load().moe_last_error_detail().decode()}]"
+        super().__init__(msg)
 
 
 class MoeFusedArgs(ctypes.Structure):
@@ -81,6 +84,8 @@ def load():
         L.moe_check_status.argtypes = [P, P]
         L.moe_status_string.argtypes = [i]
         L.moe_status_string.restype = ctypes.c_char_p
+        L.moe_last_error_detail.argtypes = []
+        L.moe_last_error_detail.restype = ctypes.c_char_p
         for name in ("moe_route_topk", "moe_align_by_expert", "moe_quantize_e4m3",
                      "moe_fused_forward", "moe_fused_forward_timed", "moe_check_status"):
             getattr(L, name).restype = ctypes.c_int

@@ -109,7 +109,6 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     moe_gemm_kernel(const __grid_constant__ GemmParams p, const __grid_constant__ CUtensorMap tm_a,
                     const __grid_constant__ CUtensorMap tm_b) {
   extern __shared__ uint8_t smem_raw[];
-  __shared__ int s_last;
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
   const int S = p.stages;
@@ -122,6 +121,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   uint64_t* never = tempty + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(never + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  volatile int* s_last = abort_flag + 1;  // "this CTA finishes the split tile" flag
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -313,10 +313,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             int n_seg = 0;
             for (int c = c_first; c <= c_last; ++c)
               n_seg += range_begin(c, rg.total) < range_begin(c + 1, rg.total) ? 1 : 0;
-            s_last = (atomicAdd(p.tile_cnt + u, 1) == n_seg - 1) ? 1 : 0;
+            *s_last = (atomicAdd(p.tile_cnt + u, 1) == n_seg - 1) ? 1 : 0;
           }
           named_barrier(kEpiBarrier, kEpiThreads);
-          finish = s_last != 0;
+          finish = *s_last != 0;
           if (finish) __threadfence();
         }
         if (finish) {
@@ -404,8 +404,8 @@ cudaError_t launch_one(const GemmParams& p, const CUtensorMap& ta, const CUtenso
   int dev = 0;
   cudaGetDevice(&dev);
   if (configured_device != dev) {
-    cudaError_t e = cudaFuncSetAttribute(moe_gemm_kernel<kBF16, kSwiGLU>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit);
+    cudaError_t e = checked(cudaFuncSetAttribute(moe_gemm_kernel<kBF16, kSwiGLU>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit), "smem attribute");
     if (e != cudaSuccess) return e;
     configured_device = dev;
   }

@@ -22,6 +22,14 @@ constexpr int kDevErrRange = 2;
 // padded to 16 rows.
 constexpr int kAlignBlock = 16;
 
+// Remembers (per host thread) the last failing CUDA call for
+// moe_last_error_detail(); returns `e` unchanged.
+void note_cuda_error(int code, const char* what, const char* where);
+inline cudaError_t checked(cudaError_t e, const char* where) {
+  if (e != cudaSuccess) note_cuda_error(static_cast<int>(e), cudaGetErrorName(e), where);
+  return e;
+}
+
 // Launch with programmatic stream serialisation: the kernel may start while
 // its predecessor drains; every kernel of this library calls pdl_wait()
 // before touching global memory, so stream order is kept for the data.
@@ -38,7 +46,7 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+  return checked(cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...), "kernel launch");
 }
 
 // Per-call control words, at the start of the workspace.

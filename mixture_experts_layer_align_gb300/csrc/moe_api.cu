@@ -5,6 +5,7 @@
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
 #include <stdint.h>
+#include <stdio.h>
 
 #include <algorithm>
 #include <mutex>
@@ -61,7 +62,10 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 bool make_tmap(CUtensorMap* m, const void* base, bool bf16, uint64_t k_elems, uint64_t rows,
                uint32_t box_rows) {
   auto enc = tensor_map_encoder();
-  if (!enc) return false;
+  if (!enc) {
+    note_cuda_error(0, "entry point not found", "cuTensorMapEncodeTiled");
+    return false;
+  }
   const uint64_t esize = bf16 ? 2 : 1;
   cuuint64_t dims[2] = {k_elems, rows};
   cuuint64_t strides[1] = {k_elems * esize};
@@ -71,6 +75,7 @@ bool make_tmap(CUtensorMap* m, const void* base, bool bf16, uint64_t k_elems, ui
                    const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                    CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) note_cuda_error(static_cast<int>(r), "CUresult", "cuTensorMapEncodeTiled");
   return r == CUDA_SUCCESS;
 }
 
@@ -158,11 +163,23 @@ moe_status_t check_device(DeviceInfo* out) {
 }
 
 }  // namespace
+
+namespace {
+thread_local char g_last_error[256] = "no error";
+}
+
+void note_cuda_error(int code, const char* what, const char* where) {
+  snprintf(g_last_error, sizeof g_last_error, "%s: %s (%d)", where ? where : "?",
+           what ? what : "?", code);
+}
+
 }  // namespace moe
 
 using namespace moe;
 
 extern "C" {
+
+const char* moe_last_error_detail(void) { return g_last_error; }
 
 const char* moe_status_string(moe_status_t s) {
   switch (s) {

@@ -512,8 +512,8 @@ cudaError_t launch_align(const AlignParams& p, cudaStream_t st) {
   int dev = 0;
   cudaGetDevice(&dev);
   if (configured_device != dev) {
-    cudaError_t e = cudaFuncSetAttribute(align_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         4 * 1024 * 4 + 32 * 1024 * 2);
+    cudaError_t e = checked(cudaFuncSetAttribute(align_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         4 * 1024 * 4 + 32 * 1024 * 2), "smem attribute");
     if (e != cudaSuccess) return e;
     configured_device = dev;
   }
