@@ -128,6 +128,14 @@ typedef struct {
 #define MOE_DEBUG_FORCE_TIMEOUT 0x1
 #define MOE_DEBUG_TIMEOUT_MS 200
 
+/* Diagnostic: the two expert-GEMM kernels record, per CTA, four %globaltimer
+ * stamps (ns): kernel entry, inputs ready, first weight tile landed, exit.
+ * They go to uint64 [2][MOE_TRACE_MAX_CTAS][4] at byte offset
+ * moe_fused_trace_offset() of the workspace (gate/up kernel first). */
+#define MOE_DEBUG_TRACE 0x2
+#define MOE_TRACE_MAX_CTAS 256
+size_t moe_fused_trace_offset(int T, int H, int I, int E, int top_k, moe_dtype_t dtype);
+
 /* Workspace bytes moe_fused_forward needs for these sizes (0 if invalid). */
 size_t moe_fused_workspace_size(int T, int H, int I, int E, int top_k, moe_dtype_t dtype);
 

@@ -20,6 +20,8 @@ MOE_OK = 0
 MOE_DT_BF16 = 0
 MOE_DT_FP8_E4M3 = 1
 MOE_DEBUG_FORCE_TIMEOUT = 0x1
+MOE_DEBUG_TRACE = 0x2
+TRACE_MAX_CTAS = 256
 STATUS_NAMES = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED",
                 3: "MOE_ERR_WORKSPACE", 4: "MOE_ERR_CUDA", 5: "MOE_ERR_DEVICE_TIMEOUT",
                 6: "MOE_ERR_DEVICE_RANGE"}
@@ -76,6 +78,8 @@ def load():
         L.moe_quantize_scratch_size.argtypes = [i, i]
         L.moe_quantize_scratch_size.restype = sz
         L.moe_quantize_e4m3.argtypes = [P, i, i, P, P, P, sz, P]
+        L.moe_fused_trace_offset.argtypes = [i, i, i, i, i, i]
+        L.moe_fused_trace_offset.restype = sz
         L.moe_fused_workspace_size.argtypes = [i, i, i, i, i, i]
         L.moe_fused_workspace_size.restype = sz
         L.moe_fused_forward.argtypes = [ctypes.POINTER(MoeFusedArgs), P, sz, P]
@@ -265,6 +269,16 @@ def make_step_events(n: int = 8):
     for e in evs:
         e.record()
     return evs
+
+
+def read_trace(workspace, T, H, I, E, top_k, dtype):
+    """Per-CTA %globaltimer stamps left by a MOE_DEBUG_TRACE call: uint64
+    [2 kernels][TRACE_MAX_CTAS][entry, inputs ready, first weights, exit]."""
+    import torch
+    off = int(load().moe_fused_trace_offset(T, H, I, E, top_k, dtype))
+    n = 2 * TRACE_MAX_CTAS * 4 * 8
+    raw = workspace[off:off + n].cpu()
+    return raw.view(torch.int64).reshape(2, TRACE_MAX_CTAS, 4)
 
 
 def moe_check_status(workspace, stream=None) -> int:

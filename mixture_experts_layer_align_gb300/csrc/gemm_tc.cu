@@ -125,6 +125,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  unsigned long long* trace =
+      (p.trace != nullptr && blockIdx.x < MOE_TRACE_MAX_CTAS) ? p.trace + blockIdx.x * 4 : nullptr;
+  if (trace && threadIdx.x == 0) trace[0] = global_timer_ns();
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
@@ -155,6 +158,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   // everything above overlaps the previous kernel; from here on its outputs are read
   pdl_wait();
   pdl_trigger();
+  if (trace && threadIdx.x == 0) trace[1] = global_timer_ns();
 
   const int K = p.k_steps;
   const Range rg = cta_range(static_cast<long long>(p.ctrl->num_mtiles) * p.nb_count * K);
@@ -229,6 +233,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             ok = false;
             break;
           }
+          if (trace && it == 0) trace[2] = global_timer_ns();
           tc_fence_after_sync();
           const uint32_t sa = smem_addr(smem + static_cast<size_t>(s) * stage_bytes);
           const uint64_t da0 = sdesc_kmajor_sw128(sa);
@@ -394,6 +399,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   if (warp == 1) {
     tc_fence_after_sync();
     tmem_dealloc(tmem, static_cast<uint32_t>(p.tmem_cols));
+  }
+  if (trace && threadIdx.x == 0) {
+    __threadfence();
+    trace[3] = global_timer_ns();
   }
 }
 

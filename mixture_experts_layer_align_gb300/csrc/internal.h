@@ -133,6 +133,7 @@ struct GemmParams {
   float* part;
   unsigned long long timeout_ns;
   int debug;
+  unsigned long long* trace;  // [MOE_TRACE_MAX_CTAS][4] stamps or null
 };
 
 // Partial-accumulator slot (gate and up, bn_max columns x 128 rows, fp32).

@@ -108,8 +108,9 @@ struct Layout {
   int bn_max = 0;
   int ctas = 0;
   int n_tile_cnt = 0;
-  size_t ctrl = 0, partials = 0, ids = 0, wts = 0, counts = 0, offsets = 0, sorted = 0,
-         mtiles = 0, tile_cnt = 0, part = 0, xs = 0, h = 0, hq = 0, acc = 0, total = 0;
+  size_t ctrl = 0, trace = 0, partials = 0, ids = 0, wts = 0, counts = 0, offsets = 0,
+         sorted = 0, mtiles = 0, tile_cnt = 0, part = 0, xs = 0, h = 0, hq = 0, acc = 0,
+         total = 0;
 };
 
 Layout make_layout(int T, int H, int I, int E, int k, bool fp8) {
@@ -128,6 +129,7 @@ Layout make_layout(int T, int H, int I, int E, int k, bool fp8) {
     return at;
   };
   L.ctrl = take(sizeof(Ctrl));
+  L.trace = take(sizeof(unsigned long long) * 2 * MOE_TRACE_MAX_CTAS * 4);
   L.partials = take(sizeof(float) * std::max(L.n_partials, 1));
   L.ids = take(sizeof(int32_t) * L.P);
   L.wts = take(sizeof(float) * L.P);
@@ -397,6 +399,8 @@ moe_status_t fused_forward_impl(const moe_fused_args* a, void* workspace, size_t
   g1.timeout_ns = (a->debug_flags & MOE_DEBUG_FORCE_TIMEOUT) ? MOE_DEBUG_TIMEOUT_MS * 1000000ull
                                                              : kWaitLimitNs;
   g1.debug = a->debug_flags;
+  unsigned long long* trace = reinterpret_cast<unsigned long long*>(ws + L.trace);
+  g1.trace = (a->debug_flags & MOE_DEBUG_TRACE) ? trace : nullptr;
   const long long work1 = max_tiles * g1.nb_count * g1.k_steps;
   const int grid1 = static_cast<int>(std::max<long long>(1, std::min<long long>(ctas, work1)));
   if (events && cudaEventRecord(events[3], stream) != cudaSuccess) return MOE_ERR_CUDA;
@@ -427,6 +431,7 @@ moe_status_t fused_forward_impl(const moe_fused_args* a, void* workspace, size_t
   g2.ldo = H;
   g2.tile_cnt = nullptr;
   g2.part = nullptr;
+  g2.trace = (a->debug_flags & MOE_DEBUG_TRACE) ? trace + MOE_TRACE_MAX_CTAS * 4 : nullptr;
   const long long work2 = max_tiles * g2.nb_count * g2.k_steps;
   const int grid2 = static_cast<int>(std::max<long long>(1, std::min<long long>(ctas, work2)));
   if (launch_gemm(bf16, false, g2, tm_w2, tm_h, grid2, s) != cudaSuccess) return MOE_ERR_CUDA;
@@ -447,6 +452,11 @@ extern "C" {
 moe_status_t moe_fused_forward(const moe_fused_args* a, void* workspace, size_t workspace_bytes,
                                moe_stream_t stream) {
   return fused_forward_impl(a, workspace, workspace_bytes, stream, nullptr);
+}
+
+size_t moe_fused_trace_offset(int T, int H, int I, int E, int top_k, moe_dtype_t dtype) {
+  if (moe_fused_workspace_size(T, H, I, E, top_k, dtype) == 0) return 0;
+  return make_layout(T, H, I, E, top_k, dtype == MOE_DT_FP8_E4M3).trace;
 }
 
 moe_status_t moe_fused_forward_timed(const moe_fused_args* a, void* workspace,
