@@ -73,8 +73,29 @@ __device__ __forceinline__ Tile decode_tile(const GemmParams& p, int u) {
   return r;
 }
 
+// Order in which the flat index space visits tiles: the tiles are laid out
+// row-major on a grid G wide (G = CTAs) and visited column by column, so the
+// contiguous range of one CTA covers tiles c, c+G, c+2G, ... spread over the
+// whole weight tensor (every CTA sees the same mix of memory), while a tile
+// cut at a range boundary is still shared by neighbouring CTAs only.
+__device__ __forceinline__ int tile_of_seq(int s, int tiles) {
+  const int G = static_cast<int>(gridDim.x);
+  const int W = (tiles + G - 1) / G;         // rows
+  const int r = tiles - (W - 1) * G;         // columns that have W rows
+  int row, col;
+  if (s < r * W) {
+    col = s / W;
+    row = s - col * W;
+  } else {
+    const int s2 = s - r * W;
+    col = r + s2 / (W - 1);
+    row = s2 - (col - r) * (W - 1);
+  }
+  return row * G + col;
+}
+
 // Segments of this CTA: contiguous range [beg, end) of the flat
-// (tile, K step) index space.
+// (tile sequence, K step) index space.
 struct Range {
   long long beg, end, total;
 };
@@ -161,7 +182,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   if (trace && threadIdx.x == 0) trace[1] = global_timer_ns();
 
   const int K = p.k_steps;
-  const Range rg = cta_range(static_cast<long long>(p.ctrl->num_mtiles) * p.nb_count * K);
+  const int tiles = p.ctrl->num_mtiles * p.nb_count;
+  const Range rg = cta_range(static_cast<long long>(tiles) * K);
   const uint64_t limit = p.timeout_ns;
 
   if (warp == 0) {
@@ -174,7 +196,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         const int u = static_cast<int>(i / K);
         const int k0 = static_cast<int>(i - static_cast<long long>(u) * K);
         const int k1 = static_cast<int>((K < k0 + (rg.end - i) ? static_cast<long long>(K) : k0 + (rg.end - i)));
-        const Tile t = decode_tile(p, u);
+        const Tile t = decode_tile(p, tile_of_seq(u, tiles));
         const int wrow = t.e * p.rows_per_expert + t.nb * 128;
         for (int kk = k0; kk < k1; ++kk, ++it) {
           const uint32_t s = it % S;
@@ -215,7 +237,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         const int u = static_cast<int>(i / K);
         const int k0 = static_cast<int>(i - static_cast<long long>(u) * K);
         const int k1 = static_cast<int>((K < k0 + (rg.end - i) ? static_cast<long long>(K) : k0 + (rg.end - i)));
-        const Tile t = decode_tile(p, u);
+        const Tile t = decode_tile(p, tile_of_seq(u, tiles));
         const uint32_t a = tt % static_cast<uint32_t>(p.num_acc);
         const uint32_t aph = (tt / static_cast<uint32_t>(p.num_acc)) & 1u;
         if (!mbar_wait(tempty + a, aph ^ 1u, abort_flag, limit)) {
@@ -276,7 +298,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       const int u = static_cast<int>(i / K);
       const int k0 = static_cast<int>(i - static_cast<long long>(u) * K);
       const int k1 = static_cast<int>((K < k0 + (rg.end - i) ? static_cast<long long>(K) : k0 + (rg.end - i)));
-      const Tile t = decode_tile(p, u);
+      const Tile t = decode_tile(p, tile_of_seq(u, tiles));
       const uint32_t a = tt % static_cast<uint32_t>(p.num_acc);
       const uint32_t aph = (tt / static_cast<uint32_t>(p.num_acc)) & 1u;
       int got = 0;
