@@ -28,8 +28,10 @@
 //   warps 2..5  epilogue: tcgen05.ld of the accumulator, then either
 //               gate/up:  h = SiLU(g * s) * (u * s) -> fp32 (FP8 path, with a
 //                         running amax|h|) or bf16 (bf16 path)
-//               down:     y * s * topk_weight -> red.add into the fp32 combine
-//                         buffer (expert aggregation fused into the GEMM).
+//               down:     y * s * topk_weight staged in shared memory and
+//                         added into the fp32 combine buffer with bulk
+//                         asynchronous reductions (expert aggregation fused
+//                         into the GEMM).
 // The accumulator is double-buffered in TMEM when it fits, so the epilogue of
 // one segment overlaps the MMAs of the next.  Every wait is bounded; on
 // timeout the CTA records kDevErrTimeout and leaves.
@@ -143,6 +145,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(never + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   volatile int* s_last = abort_flag + 1;  // "this CTA finishes the split tile" flag
+  // down projection: per epilogue warp, two 16-column x 32-row fp32 staging
+  // buffers for the bulk reductions into the combine buffer
+  float* stage_out = reinterpret_cast<float*>(smem + static_cast<size_t>(S) * stage_bytes + 256);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -292,6 +297,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     float act_s = 1.f;
     if (!kBF16) act_s = p.act_scale_sel == 1 ? p.ctrl->s_x : p.ctrl->s_h;
     float amax = 0.f;
+    uint32_t n_chunks = 0;  // combine staging chunks issued by this warp
     uint32_t tt = 0;
     bool ok = true;
     for (long long i = rg.beg; i < rg.end;) {
@@ -384,19 +390,34 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           }
         }
       } else {
+        // combine: y * s * topk_weight for 16 token columns at a time, staged
+        // in shared memory and added into the token rows of the fp32 combine
+        // buffer with one bulk asynchronous reduction (128 B) per column
+        float* wstage = stage_out + static_cast<size_t>(q) * 2 * 16 * 32;
         for (int c0 = 0; c0 < t.n; c0 += 16) {
           float y[16];
           tmem_ld16(tbase + c0, y);
-#pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            const int r = t.row0 + c0 + j;
-            const int pid = p.sorted_ids[r];
-            if (pid < p.P) {
-              const int tok = pid / p.top_k;
-              red_add_f32(p.acc_out + static_cast<size_t>(tok) * p.ldo + col,
-                          y[j] * sc * p.topk_w[pid]);
-            }
+          float* buf = wstage + (n_chunks & 1u) * 16 * 32;
+          int pid = p.P;
+          float wscale = 0.f;
+          if (lane < 16) {
+            pid = p.sorted_ids[t.row0 + c0 + lane];
+            if (pid < p.P) wscale = sc * p.topk_w[pid];
+            bulk_wait_read<1>();  // this buffer's reductions from two chunks ago have read it
           }
+          __syncwarp();
+#pragma unroll
+          for (int j = 0; j < 16; ++j) buf[j * 32 + lane] = y[j] * __shfl_sync(0xffffffffu, wscale, j);
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane < 16) {
+            if (pid < p.P)
+              bulk_reduce_add_f32(p.acc_out + static_cast<size_t>(pid / p.top_k) * p.ldo +
+                                      t.nb * 128 + q * 32,
+                                  buf + lane * 32, 128);
+            bulk_commit();
+          }
+          ++n_chunks;
         }
       }
       tc_fence_before_sync();
@@ -410,6 +431,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       for (int o = 16; o; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
       if (lane == 0 && amax > 0.f) atomicMax(&p.ctrl->amax_h, __float_as_uint(amax));
     }
+    if (!kSwiGLU && lane < 16) bulk_wait_all();  // reductions done before the CTA leaves
     if (!ok && lane == 0) {
       *abort_flag = 1;
       atomicOr(&p.ctrl->err, kDevErrTimeout);
@@ -447,14 +469,18 @@ cudaError_t launch_one(const GemmParams& p, const CUtensorMap& ta, const CUtenso
 
 }  // namespace
 
+// Combine staging of the down projection: 4 warps x 2 buffers x 16 x 32 fp32.
+constexpr size_t kCombineStaging = 4 * 2 * 16 * 32 * sizeof(float);
+
 size_t gemm_smem_bytes(bool swiglu, int bn_max, int stages) {
   const size_t stage = (swiglu ? 32768u : 16384u) + static_cast<size_t>(bn_max) * 128u;
-  return stage * stages + kSmemSlack;
+  return stage * stages + kSmemSlack + (swiglu ? 0 : kCombineStaging);
 }
 
 int gemm_max_stages(bool swiglu, int bn_max) {
   const size_t stage = (swiglu ? 32768u : 16384u) + static_cast<size_t>(bn_max) * 128u;
-  int s = static_cast<int>((kSmemLimit - kSmemSlack) / stage);
+  const size_t avail = kSmemLimit - kSmemSlack - (swiglu ? 0 : kCombineStaging);
+  int s = static_cast<int>(avail / stage);
   if (s > kMaxStages) s = kMaxStages;
   return s;
 }

@@ -82,12 +82,14 @@ bool make_tmap(CUtensorMap* m, const void* base, bool bf16, uint64_t k_elems, ui
 int round_up16(long long v) { return static_cast<int>((v + 15) / 16 * 16); }
 
 // Row-tile width (MMA N) of the expert GEMMs: twice the mean rows per touched
-// expert, 64..256.  Any value is correct; wider tiles re-read each weight
-// block fewer times, narrower ones leave more stages of weights in flight.
+// expert, 64..128.  Any value is correct; wider tiles re-read each weight
+// block fewer times, narrower ones leave more stages of weights in flight;
+// up to 128 the gate/up accumulators (2 x N columns) are double-buffered in
+// the 512 TMEM columns.
 int choose_bn_max(long long P, int E) {
   const long long touched = std::min<long long>(E, P);
   const long long mean_rows = touched > 0 ? (P + touched - 1) / touched : 1;
-  return std::min(256, std::max(64, round_up16(2 * mean_rows)));
+  return std::min(128, std::max(64, round_up16(2 * mean_rows)));
 }
 
 // CTAs the persistent GEMMs may use on the current device (also sizes the
