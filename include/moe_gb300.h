@@ -103,6 +103,30 @@ size_t moe_quantize_scratch_size(int T, int H);
 moe_status_t moe_quantize_e4m3(const void* x, int T, int H, uint8_t* x_q, float* scale,
                                void* scratch, size_t scratch_bytes, moe_stream_t stream);
 
+/*
+ * Same operation and results as moe_quantize_e4m3, without the caller scratch
+ * buffer: the scratch (one fp32 partial maximum per amax CTA, at most
+ * MOE_NOALLOC_MAX_PARTIALS of them, 4 KB) lives in a static device array of
+ * the library.  The pages have no counterpart of this entry point; it exists
+ * for callers that cannot allocate device memory where they call it (another
+ * component owns every allocation, or the calling thread must not take
+ * cudaMalloc's implicit synchronisation).
+ *   - Allocates nothing: no cudaMalloc, cudaFree or allocating library call.
+ *   - The first call on a device looks up the array's device address
+ *     (cudaGetSymbolAddress) with that device current and caches it; make
+ *     that first call before any stream capture on the device.
+ *   - The array is shared by every call on the device and keeps the last
+ *     call's contents; calls that overlap on the GPU (other streams, or other
+ *     host threads) race on it and must be serialised by the caller.
+ *   - Every T*H fits (the amax kernel strides over the tensor, using at most
+ *     MOE_NOALLOC_MAX_PARTIALS CTAs); T, H and pointers are checked as in
+ *     moe_quantize_e4m3 (MOE_ERR_INVALID_ARG), and a partial count beyond the
+ *     array would return MOE_ERR_UNSUPPORTED.
+ */
+#define MOE_NOALLOC_MAX_PARTIALS 1024
+moe_status_t moe_quantize_e4m3_noalloc(const void* x, int T, int H, uint8_t* x_q, float* scale,
+                                       moe_stream_t stream);
+
 /* Arguments of the fused layer forward. */
 typedef struct {
   const void* x;             /* bf16 [T, H] */

@@ -78,6 +78,8 @@ def load():
         L.moe_quantize_scratch_size.argtypes = [i, i]
         L.moe_quantize_scratch_size.restype = sz
         L.moe_quantize_e4m3.argtypes = [P, i, i, P, P, P, sz, P]
+        L.moe_quantize_e4m3_noalloc.argtypes = [P, i, i, P, P, P]
+        L.moe_quantize_e4m3_noalloc.restype = ctypes.c_int
         L.moe_fused_trace_offset.argtypes = [i, i, i, i, i, i]
         L.moe_fused_trace_offset.restype = sz
         L.moe_fused_workspace_size.argtypes = [i, i, i, i, i, i]
@@ -179,6 +181,26 @@ def moe_quantize_e4m3(x, stream=None):
     _check(L.moe_quantize_e4m3(_ptr(x), T, H, _ptr(xq), _ptr(scale), _ptr(scratch), nscr,
                                _stream(stream)), "moe_quantize_e4m3")
     return xq, scale
+
+
+def moe_quantize_e4m3_noalloc(x, x_q=None, scale=None, stream=None):
+    """moe_quantize_e4m3 for callers that cannot allocate device scratch: the
+    library's static device array holds the partial maxima (shared by all
+    calls on a device; overlapping calls race).  Outputs may be passed in;
+    when omitted they are allocated here by torch, outside the C call.
+    Returns (codes uint8 [T,H], scale fp32 [1])."""
+    import torch
+    _require(x, torch.bfloat16, "x")
+    T, H = x.shape
+    if x_q is None:
+        x_q = torch.empty(T, H, dtype=torch.uint8, device=x.device)
+    if scale is None:
+        scale = torch.empty(1, dtype=torch.float32, device=x.device)
+    _require(x_q, torch.uint8, "x_q", (T, H))
+    _require(scale, torch.float32, "scale", (1,))
+    _check(load().moe_quantize_e4m3_noalloc(_ptr(x), T, H, _ptr(x_q), _ptr(scale),
+                                            _stream(stream)), "moe_quantize_e4m3_noalloc")
+    return x_q, scale
 
 
 def moe_fused_workspace_size(T: int, H: int, I: int, E: int, top_k: int, dtype: int) -> int:
