@@ -127,60 +127,6 @@ __device__ __forceinline__ float* part_slot(const GemmParams& p, int c, long lon
   return p.part + (static_cast<size_t>(c) * 2 + s) * gemm_part_slot_floats(p.bn_max);
 }
 
-__device__ __forceinline__ uint32_t quant4_e4m3(float4 v, float s) {
-  return static_cast<uint32_t>(cvt_e4m3x2(__fdiv_rn(v.x, s), __fdiv_rn(v.y, s))) |
-         (static_cast<uint32_t>(cvt_e4m3x2(__fdiv_rn(v.z, s), __fdiv_rn(v.w, s))) << 16);
-}
-
-// Work that needs every CTA's results: a grid barrier (all CTAs are resident,
-// one per SM; the wait is bounded), then a grid-wide element-wise pass.
-//   kTailQuantH   s_h = amax(h) / 448; h (fp32) -> E4M3 codes for the down GEMM
-//   kTailFinalize fp32 combine buffer -> bf16 output
-__device__ void gemm_tail(const GemmParams& p) {
-  if (threadIdx.x == 0) {
-    __threadfence();
-    atomicAdd(p.tail_bar, 1u);
-    const bool ok = spin_until_u32_geq(p.tail_bar, gridDim.x, p.timeout_ns);
-    __threadfence();
-    if (!ok) atomicOr(&p.ctrl->err, kDevErrTimeout);
-  }
-  __syncthreads();
-  const long long tid = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
-  const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
-  if (p.tail == kTailQuantH) {
-    const float amax = __uint_as_float(*reinterpret_cast<volatile unsigned*>(&p.ctrl->amax_h));
-    const float s = amax > 0.f ? __fdiv_rn(amax, 448.f) : 1.f;
-    if (blockIdx.x == 0 && threadIdx.x == 0) p.ctrl->s_h = s;
-    const long long n16 = static_cast<long long>(p.ctrl->num_padded) * p.ldh / 16;
-    const float4* src = static_cast<const float4*>(p.h_out);
-    uint4* dst = reinterpret_cast<uint4*>(p.hq_out);
-    for (long long i = tid; i < n16; i += stride) {
-      uint4 r;
-      r.x = quant4_e4m3(__ldcg(src + 4 * i + 0), s);
-      r.y = quant4_e4m3(__ldcg(src + 4 * i + 1), s);
-      r.z = quant4_e4m3(__ldcg(src + 4 * i + 2), s);
-      r.w = quant4_e4m3(__ldcg(src + 4 * i + 3), s);
-      dst[i] = r;
-    }
-  } else {
-    const float4* a = reinterpret_cast<const float4*>(p.acc_out);
-    uint4* o = reinterpret_cast<uint4*>(p.out);
-    for (long long i = tid; i < p.out_elems / 8; i += stride) {
-      const float4 u = __ldcg(a + 2 * i), v = __ldcg(a + 2 * i + 1);
-      __nv_bfloat162 b0 = __floats2bfloat162_rn(u.x, u.y);
-      __nv_bfloat162 b1 = __floats2bfloat162_rn(u.z, u.w);
-      __nv_bfloat162 b2 = __floats2bfloat162_rn(v.x, v.y);
-      __nv_bfloat162 b3 = __floats2bfloat162_rn(v.z, v.w);
-      uint4 r;
-      r.x = *reinterpret_cast<uint32_t*>(&b0);
-      r.y = *reinterpret_cast<uint32_t*>(&b1);
-      r.z = *reinterpret_cast<uint32_t*>(&b2);
-      r.w = *reinterpret_cast<uint32_t*>(&b3);
-      o[i] = r;
-    }
-  }
-}
-
 template <bool kBF16, bool kSwiGLU>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     moe_gemm_kernel(const __grid_constant__ GemmParams p, const __grid_constant__ CUtensorMap tm_a,
@@ -485,10 +431,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       for (int o = 16; o; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
       if (lane == 0 && amax > 0.f) atomicMax(&p.ctrl->amax_h, __float_as_uint(amax));
     }
-    if (!kSwiGLU && lane < 16) {
-      bulk_wait_all();  // reductions done before the CTA leaves or reaches the tail barrier
-      fence_proxy_async_global();
-    }
+    if (!kSwiGLU && lane < 16) bulk_wait_all();  // reductions done before the CTA leaves
     if (!ok && lane == 0) {
       *abort_flag = 1;
       atomicOr(&p.ctrl->err, kDevErrTimeout);
@@ -501,7 +444,6 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     tc_fence_after_sync();
     tmem_dealloc(tmem, static_cast<uint32_t>(p.tmem_cols));
   }
-  if (p.tail != kTailNone) gemm_tail(p);
   if (trace && threadIdx.x == 0) {
     __threadfence();
     trace[3] = global_timer_ns();
@@ -521,9 +463,6 @@ cudaError_t launch_one(const GemmParams& p, const CUtensorMap& ta, const CUtenso
     configured_device = dev;
   }
   const size_t smem = gemm_smem_bytes(kSwiGLU, p.bn_max, p.stages);
-  if (p.tail != kTailNone)
-    return launch_pdl_coop(moe_gemm_kernel<kBF16, kSwiGLU>, dim3(grid), dim3(kGemmThreads), smem,
-                           st, p, ta, tb);
   return launch_pdl(moe_gemm_kernel<kBF16, kSwiGLU>, dim3(grid), dim3(kGemmThreads), smem, st, p,
                     ta, tb);
 }

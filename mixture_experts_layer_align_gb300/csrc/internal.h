@@ -49,34 +49,6 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
   return checked(cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...), "kernel launch");
 }
 
-// Same, also asking for a cooperative launch (every CTA resident at once), for
-// kernels with a grid barrier; where the runtime does not take both
-// attributes together the kernel is launched with the first one only (its
-// grid is at most one CTA per SM, and its barrier waits are bounded).
-template <typename... KArgs, typename... Args>
-cudaError_t launch_pdl_coop(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
-                            cudaStream_t st, Args&&... args) {
-  cudaLaunchConfig_t cfg{};
-  cfg.gridDim = grid;
-  cfg.blockDim = block;
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = st;
-  cudaLaunchAttribute attr[2];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  attr[1].id = cudaLaunchAttributeCooperative;
-  attr[1].val.cooperative = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 2;
-  cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, args...);
-  if (e == cudaErrorInvalidValue || e == cudaErrorNotSupported) {
-    (void)cudaGetLastError();
-    cfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&cfg, kernel, args...);
-  }
-  return checked(e, "kernel launch");
-}
-
 // Per-call control words, at the start of the workspace.
 struct Ctrl {
   int err;          // kDevErr* bits set by device code
@@ -86,10 +58,9 @@ struct Ctrl {
   int num_padded;   // rows of the aligned (sorted, padded) pair list
   int num_mtiles;   // entries of the GEMM row-tile list
   unsigned bar_count;             // grid barrier of the fused front kernel
-  unsigned bar_gemm1;             // grid barrier before the gate/up GEMM's tail
-  unsigned long long bar_epoch;   // per-call tag that arms the front barrier
-  unsigned bar_gemm2;             // grid barrier before the down GEMM's tail
-  int pad[5];
+  int pad0;
+  unsigned long long bar_epoch;   // per-call tag that arms that barrier
+  int pad[6];
 };
 static_assert(sizeof(Ctrl) == 64, "Ctrl layout");
 
@@ -196,18 +167,7 @@ struct GemmParams {
   unsigned long long timeout_ns;
   int debug;
   unsigned long long* trace;  // [MOE_TRACE_MAX_CTAS][4] stamps or null
-  // Work after a grid barrier at the end of the kernel (all CTAs resident):
-  //   kTailQuantH:   h (fp32) -> E4M3 codes with s_h = amax(h) / 448
-  //   kTailFinalize: fp32 combine buffer -> bf16 output
-  int tail;
-  unsigned* tail_bar;    // zeroed at the start of the call
-  uint8_t* hq_out;       // kTailQuantH: [rows, I]
-  __nv_bfloat16* out;    // kTailFinalize: [T, H]
-  long long out_elems;
 };
-constexpr int kTailNone = 0;
-constexpr int kTailQuantH = 1;
-constexpr int kTailFinalize = 2;
 
 // Partial-accumulator slot (gate and up, bn_max columns x 128 rows, fp32).
 __host__ __device__ inline size_t gemm_part_slot_floats(int bn_max) { return static_cast<size_t>(2) * bn_max * 128; }

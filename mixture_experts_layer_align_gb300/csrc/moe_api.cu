@@ -451,18 +451,16 @@ moe_status_t fused_forward_impl(const moe_fused_args* a, void* workspace, size_t
   g1.debug = a->debug_flags;
   unsigned long long* trace = reinterpret_cast<unsigned long long*>(ws + L.trace);
   g1.trace = (a->debug_flags & MOE_DEBUG_TRACE) ? trace : nullptr;
-  // FP8: after a grid barrier the same kernel takes s_h = amax(h)/448 and
-  // writes the E4M3 codes of h for the down GEMM
-  g1.tail = fp8 ? kTailQuantH : kTailNone;
-  g1.tail_bar = &ctrl->bar_gemm1;
-  g1.hq_out = hq;
   const long long work1 = max_tiles * g1.nb_count * g1.k_steps;
   const int grid1 = static_cast<int>(std::max<long long>(1, std::min<long long>(ctas, work1)));
   if (events && cudaEventRecord(events[3], stream) != cudaSuccess) return MOE_ERR_CUDA;
   if (launch_gemm(bf16, true, g1, tm_w13, tm_xs, grid1, s) != cudaSuccess) return MOE_ERR_CUDA;
 
-  // 5. (dynamic scale of h and its E4M3 codes: the gate/up kernel's tail)
+  // 5. dynamic scale of h and its E4M3 codes
   if (events && cudaEventRecord(events[4], stream) != cudaSuccess) return MOE_ERR_CUDA;
+  if (fp8 && launch_quant_h(static_cast<const float*>(h), I, ctrl, hq, L.pad_max, dev.num_sms,
+                            s) != cudaSuccess)
+    return MOE_ERR_CUDA;
 
   // 6. down GEMM + weighted scatter-combine (tiles cut across CTAs add into
   //    the combine buffer like any other partial sum)
@@ -484,20 +482,16 @@ moe_status_t fused_forward_impl(const moe_fused_args* a, void* workspace, size_t
   g2.tile_cnt = nullptr;
   g2.part = nullptr;
   g2.trace = (a->debug_flags & MOE_DEBUG_TRACE) ? trace + MOE_TRACE_MAX_CTAS * 4 : nullptr;
-  // after a grid barrier the same kernel writes the bf16 output
-  g2.tail = kTailFinalize;
-  g2.tail_bar = &ctrl->bar_gemm2;
-  g2.hq_out = nullptr;
-  g2.out = static_cast<__nv_bfloat16*>(a->out);
-  g2.out_elems = static_cast<long long>(T) * H;
   const long long work2 = max_tiles * g2.nb_count * g2.k_steps;
   const int grid2 = static_cast<int>(std::max<long long>(1, std::min<long long>(ctas, work2)));
   if (launch_gemm(bf16, false, g2, tm_w2, tm_h, grid2, s) != cudaSuccess) return MOE_ERR_CUDA;
 
-  // 7. (fp32 combine buffer -> bf16 output: the down kernel's tail)
-  if (events && (cudaEventRecord(events[6], stream) != cudaSuccess ||
-                 cudaEventRecord(events[7], stream) != cudaSuccess))
+  // 7. fp32 combine buffer -> bf16 output
+  if (events && cudaEventRecord(events[6], stream) != cudaSuccess) return MOE_ERR_CUDA;
+  if (launch_finalize(acc, static_cast<__nv_bfloat16*>(a->out), static_cast<long long>(T) * H,
+                      dev.num_sms, s) != cudaSuccess)
     return MOE_ERR_CUDA;
+  if (events && cudaEventRecord(events[7], stream) != cudaSuccess) return MOE_ERR_CUDA;
   return MOE_OK;
 }
 

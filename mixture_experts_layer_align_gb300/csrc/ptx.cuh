@@ -54,36 +54,6 @@ __device__ __forceinline__ bool named_barrier_and(uint32_t id, uint32_t count, b
   return r != 0;
 }
 
-// Bounded spins on global words written by other CTAs (grid barriers).
-// Return false when `limit_ns` ran out.
-__device__ __forceinline__ bool spin_until_u64_eq(const unsigned long long* a, unsigned long long v,
-                                                  uint64_t limit_ns) {
-  const volatile unsigned long long* va = a;
-  const uint64_t t0 = global_timer_ns();
-  while (*va != v) {
-    if (global_timer_ns() - t0 > limit_ns) return false;
-    __nanosleep(32);
-  }
-  return true;
-}
-
-__device__ __forceinline__ bool spin_until_u32_geq(const unsigned* a, unsigned v,
-                                                   uint64_t limit_ns) {
-  const volatile unsigned* va = a;
-  const uint64_t t0 = global_timer_ns();
-  while (*va < v) {
-    if (global_timer_ns() - t0 > limit_ns) return false;
-    __nanosleep(32);
-  }
-  return true;
-}
-
-// Orders this thread's completed bulk-async writes to global memory before
-// its later generic-proxy operations (e.g. the release of a grid barrier).
-__device__ __forceinline__ void fence_proxy_async_global() {
-  asm volatile("fence.proxy.async.global;" ::: "memory");
-}
-
 // ---------------------------------------------------------------- mbarrier
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count)

@@ -172,8 +172,6 @@ __global__ void __launch_bounds__(kRouteWarps * 32)
   if (ctrl != nullptr && blockIdx.x == 0 && threadIdx.x == 0) {
     ctrl->err = 0;
     ctrl->amax_h = 0u;
-    ctrl->bar_gemm1 = 0u;
-    ctrl->bar_gemm2 = 0u;
   }
   for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n_zero; i += gridDim.x * blockDim.x)
     zero_ints[i] = 0;
@@ -347,6 +345,27 @@ __global__ void __launch_bounds__(kAlignThreads) align_kernel(AlignParams p) {
 }
 
 // ------------------------------------------------------------------ fused front (small batches)
+// Bounded waits of the grid barrier below.
+__device__ bool wait_u64_eq(const unsigned long long* a, unsigned long long v, uint64_t limit_ns) {
+  const volatile unsigned long long* va = a;
+  const uint64_t t0 = global_timer_ns();
+  while (*va != v) {
+    if (global_timer_ns() - t0 > limit_ns) return false;
+    __nanosleep(64);
+  }
+  return true;
+}
+
+__device__ bool wait_u32_ge(const unsigned* a, unsigned v, uint64_t limit_ns) {
+  const volatile unsigned* va = a;
+  const uint64_t t0 = global_timer_ns();
+  while (*va < v) {
+    if (global_timer_ns() - t0 > limit_ns) return false;
+    __nanosleep(64);
+  }
+  return true;
+}
+
 // Writes the GEMM row-tile list from the per-expert padded segments (one
 // expert per thread, tid < E; all 1024 threads must call).  Each expert's
 // segment is split into ceil(padded / bn_max) equal tiles (multiples of bm);
@@ -392,8 +411,6 @@ __global__ void __launch_bounds__(kFrontThreads, 1) front_small_kernel(FrontPara
     ctrl->err = 0;
     ctrl->amax_h = 0u;
     ctrl->bar_count = 0u;
-    ctrl->bar_gemm1 = 0u;
-    ctrl->bar_gemm2 = 0u;
     __threadfence();
     atomicExch(&ctrl->bar_epoch, p.epoch);
   }
@@ -421,10 +438,10 @@ __global__ void __launch_bounds__(kFrontThreads, 1) front_small_kernel(FrontPara
     p.amax_partials[blockIdx.x] = m;
     // grid barrier: wait for this call's epoch, arrive, wait for everyone
     __threadfence();
-    bool ok = spin_until_u64_eq(&ctrl->bar_epoch, p.epoch, p.timeout_ns);
+    bool ok = wait_u64_eq(&ctrl->bar_epoch, p.epoch, p.timeout_ns);
     if (ok) {
       atomicAdd(&ctrl->bar_count, 1u);
-      ok = spin_until_u32_geq(&ctrl->bar_count, static_cast<unsigned>(G), p.timeout_ns);
+      ok = wait_u32_ge(&ctrl->bar_count, static_cast<unsigned>(G), p.timeout_ns);
     }
     __threadfence();
     if (!ok) atomicOr(&ctrl->err, kDevErrTimeout);
@@ -433,13 +450,11 @@ __global__ void __launch_bounds__(kFrontThreads, 1) front_small_kernel(FrontPara
   pdl_trigger();  // the next kernel may set itself up; it waits for this one to finish
 
   // phase 2: counts, padded offsets and stable placement of every pair
-  int* s_ids = s_sorted + P + E * (kAlignBlock - 1);  // [T*k]
   for (int e = tid; e < E; e += kFrontThreads) s_cnt[e] = 0;
-  for (int q = tid; q < P; q += kFrontThreads) s_ids[q] = __ldcg(p.ids + q);
   __syncthreads();
   for (int q0 = 0; q0 < P; q0 += kFrontThreads) {
     const int q = q0 + tid;
-    const int e = q < P ? s_ids[q] : -1;
+    const int e = q < P ? __ldcg(p.ids + q) : -1;
     const bool valid = q < P && static_cast<unsigned>(e) < static_cast<unsigned>(E);
     const unsigned mask = __match_any_sync(kFull, valid ? e : -1);
     if (valid && lane == __ffs(mask) - 1) atomicAdd(&s_cnt[e], __popc(mask));
@@ -454,7 +469,7 @@ __global__ void __launch_bounds__(kFrontThreads, 1) front_small_kernel(FrontPara
   if (warp == 0) {
     for (int q0 = 0; q0 < P; q0 += 32) {
       const int q = q0 + lane;
-      const int e = q < P ? s_ids[q] : -1;
+      const int e = q < P ? __ldcg(p.ids + q) : -1;
       const bool valid = q < P && static_cast<unsigned>(e) < static_cast<unsigned>(E);
       const unsigned mask = __match_any_sync(kFull, valid ? e : -1);
       const int leader = __ffs(mask) - 1;
@@ -703,13 +718,13 @@ int front_grid(int T, int k, int E, int num_sms) {
 }
 
 cudaError_t launch_front(const FrontParams& p, int grid, cudaStream_t st) {
-  const size_t smem = (static_cast<size_t>(32) * p.E + 2 * p.E + 2 * static_cast<size_t>(p.T) * p.k +
+  const size_t smem = (static_cast<size_t>(32) * p.E + 2 * p.E + static_cast<size_t>(p.T) * p.k +
                        static_cast<size_t>(p.E) * (kAlignBlock - 1)) * sizeof(int);
   static thread_local int configured_device = -1;
   int dev = 0;
   cudaGetDevice(&dev);
   if (configured_device != dev) {
-    const size_t max_smem = (32 * kFrontMaxExperts + 2 * kFrontMaxExperts + 2 * kFrontMaxPairs +
+    const size_t max_smem = (32 * kFrontMaxExperts + 2 * kFrontMaxExperts + kFrontMaxPairs +
                              kFrontMaxExperts * (kAlignBlock - 1)) * sizeof(int);
     cudaError_t e = checked(cudaFuncSetAttribute(front_small_kernel,
                                                  cudaFuncAttributeMaxDynamicSharedMemorySize,
