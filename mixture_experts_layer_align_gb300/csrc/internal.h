@@ -57,10 +57,7 @@ struct Ctrl {
   float s_h;        // activation scale of h
   int num_padded;   // rows of the aligned (sorted, padded) pair list
   int num_mtiles;   // entries of the GEMM row-tile list
-  unsigned bar_count;             // grid barrier of the fused front kernel
-  int pad0;
-  unsigned long long bar_epoch;   // per-call tag that arms that barrier
-  int pad[6];
+  int pad[10];
 };
 static_assert(sizeof(Ctrl) == 64, "Ctrl layout");
 
@@ -89,36 +86,6 @@ struct AlignParams {
 };
 cudaError_t launch_align(const AlignParams& p, cudaStream_t st);
 int align_chunk();
-
-// Fused front for small batches (router + alignment + gather in one
-// cooperative launch).  Used when T*k <= kFrontMaxPairs and E <= kFrontMaxExperts.
-constexpr int kFrontThreads = 1024;
-constexpr int kFrontMaxPairs = 2048;
-constexpr int kFrontMaxExperts = 256;
-struct FrontParams {
-  const float* logits;
-  int T, E, k, renorm;
-  int32_t* ids;
-  float* wts;
-  const __nv_bfloat16* x;
-  int H, fp8;
-  float* amax_partials;  // [grid]
-  Ctrl* ctrl;
-  int* zero_ints;
-  int n_zero;
-  int32_t* counts;
-  int32_t* offsets;
-  int32_t* sorted_ids;
-  int4* mtiles;
-  int bn_max;
-  void* xs;
-  float* acc;
-  long long acc_elems;
-  unsigned long long epoch;
-  unsigned long long timeout_ns;
-};
-int front_grid(int T, int k, int E, int num_sms);
-cudaError_t launch_front(const FrontParams& p, int grid, cudaStream_t st);
 
 // Gather the routed rows of x into aligned order (E4M3 with s_x, or bf16), zero
 // the fp32 combine buffer.

@@ -8,8 +8,6 @@
 #include <stdio.h>
 
 #include <algorithm>
-#include <atomic>
-#include <chrono>
 #include <mutex>
 
 #include "internal.h"
@@ -111,7 +109,6 @@ struct Layout {
   int n_partials = 0;  // router CTAs
   int bn_max = 0;
   int ctas = 0;
-  int n_front = 0;     // max CTAs of the fused front kernel (amax partials)
   int n_tile_cnt = 0;
   size_t ctrl = 0, trace = 0, partials = 0, ids = 0, wts = 0, counts = 0, offsets = 0,
          sorted = 0, mtiles = 0, tile_cnt = 0, part = 0, xs = 0, h = 0, hq = 0, acc = 0,
@@ -126,7 +123,6 @@ Layout make_layout(int T, int H, int I, int E, int k, bool fp8) {
   L.n_partials = route_grid(T);
   L.bn_max = choose_bn_max(L.P, E);
   L.ctas = gemm_ctas();
-  L.n_front = L.ctas;
   L.n_tile_cnt = L.max_mtiles * (I / 128);
   size_t off = 0;
   auto take = [&](size_t bytes) {
@@ -136,7 +132,7 @@ Layout make_layout(int T, int H, int I, int E, int k, bool fp8) {
   };
   L.ctrl = take(sizeof(Ctrl));
   L.trace = take(sizeof(unsigned long long) * 2 * MOE_TRACE_MAX_CTAS * 4);
-  L.partials = take(sizeof(float) * std::max({L.n_partials, L.n_front, 1}));
+  L.partials = take(sizeof(float) * std::max(L.n_partials, 1));
   L.ids = take(sizeof(int32_t) * L.P);
   L.wts = take(sizeof(float) * L.P);
   L.counts = take(sizeof(int32_t) * E);
@@ -154,16 +150,6 @@ Layout make_layout(int T, int H, int I, int E, int k, bool fp8) {
 }
 
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
-
-// Tag that arms the fused front kernel's grid barrier: unique per call within
-// the process, seeded from the clock so a workspace that still holds a tag
-// from an earlier process does not match.
-unsigned long long next_epoch() {
-  static std::atomic<unsigned long long> counter{
-      (static_cast<unsigned long long>(std::chrono::steady_clock::now().time_since_epoch().count())
-       << 16) | 1ull};
-  return counter.fetch_add(1, std::memory_order_relaxed);
-}
 
 int next_pow2(int v) {
   int p = 32;
@@ -341,42 +327,9 @@ moe_status_t fused_forward_impl(const moe_fused_args* a, void* workspace, size_t
   int* tile_cnt = reinterpret_cast<int*>(ws + L.tile_cnt);
   float* part = reinterpret_cast<float*>(ws + L.part);
 
+  // 1. routing (+ per-CTA amax of x, + reset of the control words)
   cudaStream_t s = stream;
   if (events && cudaEventRecord(events[0], stream) != cudaSuccess) return MOE_ERR_CUDA;
-  if (P <= kFrontMaxPairs && E <= kFrontMaxExperts) {
-    // 1-3 in one cooperative launch: routing, alignment, gather/quantise of x
-    FrontParams fp{};
-    fp.logits = a->router_logits;
-    fp.T = T;
-    fp.E = E;
-    fp.k = k;
-    fp.renorm = a->renormalize;
-    fp.ids = ids;
-    fp.wts = wts;
-    fp.x = static_cast<const __nv_bfloat16*>(a->x);
-    fp.H = H;
-    fp.fp8 = fp8 ? 1 : 0;
-    fp.amax_partials = partials;
-    fp.ctrl = ctrl;
-    fp.zero_ints = tile_cnt;
-    fp.n_zero = L.n_tile_cnt;
-    fp.counts = counts;
-    fp.offsets = offsets;
-    fp.sorted_ids = sorted;
-    fp.mtiles = mtiles;
-    fp.bn_max = bn_max;
-    fp.xs = xs;
-    fp.acc = acc;
-    fp.acc_elems = static_cast<long long>(T) * H;
-    fp.epoch = next_epoch();
-    fp.timeout_ns = kWaitLimitNs;
-    if (launch_front(fp, std::min(L.n_front, front_grid(T, k, E, dev.num_sms)), s) != cudaSuccess)
-      return MOE_ERR_CUDA;
-    if (events && (cudaEventRecord(events[1], stream) != cudaSuccess ||
-                   cudaEventRecord(events[2], stream) != cudaSuccess))
-      return MOE_ERR_CUDA;
-  } else {
-  // 1. routing (+ per-CTA amax of x, + reset of the control words)
   if (launch_route_topk(a->router_logits, T, E, k, a->renormalize, ids, wts,
                         static_cast<const __nv_bfloat16*>(a->x), H, fp8 ? partials : nullptr, ctrl,
                         tile_cnt, L.n_tile_cnt, s) != cudaSuccess)
@@ -406,7 +359,6 @@ moe_status_t fused_forward_impl(const moe_fused_args* a, void* workspace, size_t
                       k, xs, fp8, acc, static_cast<long long>(T) * H, L.pad_max, dev.num_sms,
                       s) != cudaSuccess)
     return MOE_ERR_CUDA;
-  }
 
   // TMA descriptors
   CUtensorMap tm_w13, tm_xs, tm_w2, tm_h;

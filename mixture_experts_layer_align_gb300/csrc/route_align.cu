@@ -92,73 +92,11 @@ __device__ int block_exclusive_scan_1024(int v, int* tmp, int* total) {
 }
 
 // ------------------------------------------------------------------ router
-// One warp per token.  The row of logits is staged in shared memory (`l`, E
-// floats of this warp); each of the k rounds is a warp arg-max under (logit
-// desc, index asc) over the experts not taken yet (one bit per lane per 32
-// experts).  The softmax uses expf on max-subtracted logits.  Writes the k
-// ids and weights of the token.
-__device__ void route_token(const float* __restrict__ src, int E, int k, int renorm, float* l,
-                            int32_t* __restrict__ id_row, float* __restrict__ w_row, int lane) {
-  float m = -INFINITY;
-  for (int e = lane; e < E; e += 32) {
-    const float v = src[e];
-    l[e] = v;
-    m = fmaxf(m, v);
-  }
-  m = warp_max(m);
-  float z = 0.f;
-  for (int e = lane; e < E; e += 32) z += expf(l[e] - m);
-  z = warp_sum(z);
-  __syncwarp();
-
-  uint32_t taken = 0u;  // bit i <=> expert lane + 32 i already selected
-  float sel = 0.f;
-  for (int j = 0; j < k; ++j) {
-    float bv = -INFINITY;
-    int bi = 0x7fffffff;  // "none"
-    for (int e = lane, i = 0; e < E; e += 32, ++i) {
-      if ((taken >> i) & 1u) continue;
-      const float v = l[e];
-      if (bi == 0x7fffffff || v > bv) {  // ascending scan: equal values keep the lower index
-        bv = v;
-        bi = e;
-      }
-    }
-#pragma unroll
-    for (int o = 16; o; o >>= 1) {
-      const float ov = __shfl_xor_sync(kFull, bv, o);
-      const int oi = __shfl_xor_sync(kFull, bi, o);
-      const bool take = oi != 0x7fffffff && (bi == 0x7fffffff || ov > bv || (ov == bv && oi < bi));
-      if (take) {
-        bv = ov;
-        bi = oi;
-      }
-    }
-    if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
-    const float ex = expf(bv - m);
-    sel += ex;
-    if (lane == 0) {
-      id_row[j] = bi;
-      w_row[j] = ex;
-    }
-  }
-  __syncwarp();
-  const float denom = renorm ? sel : z;
-  for (int j = lane; j < k; j += 32) w_row[j] = __fdiv_rn(w_row[j], denom);
-  __syncwarp();
-}
-
-// max |x| over one bf16 row of H elements (warp-wide result).
-__device__ __forceinline__ float row_absmax(const __nv_bfloat16* __restrict__ row, int H,
-                                            int lane) {
-  const uint4* xr = reinterpret_cast<const uint4*>(row);
-  float xmax = 0.f;
-  for (int i = lane; i < H / 8; i += 32) xmax = absmax8(__ldg(xr + i), xmax);
-  return warp_max(xmax);
-}
-
-// Router kernel: one warp per token, plus the per-CTA amax of x (the first
-// half of the dynamic activation scale) and the per-call resets.
+// One warp per token.  The row of logits is staged in shared memory; each of
+// the k rounds is a warp arg-max under (logit desc, index asc) over the
+// experts not taken yet (one bit per lane per 32 experts).  The softmax uses
+// expf on max-subtracted logits.  Optionally also the per-CTA amax of x, the
+// first half of the dynamic activation scale.
 __global__ void __launch_bounds__(kRouteWarps * 32)
     route_topk_kernel(const float* __restrict__ logits, int T, int E, int k, int renorm,
                       int32_t* __restrict__ ids, float* __restrict__ wts,
@@ -178,10 +116,63 @@ __global__ void __launch_bounds__(kRouteWarps * 32)
   const int t = blockIdx.x * kRouteWarps + warp;
   float xmax = 0.f;
   if (t < T) {
-    route_token(logits + static_cast<size_t>(t) * E, E, k, renorm,
-                s_logits + static_cast<size_t>(warp) * E, ids + static_cast<size_t>(t) * k,
-                wts + static_cast<size_t>(t) * k, lane);
-    if (x != nullptr) xmax = row_absmax(x + static_cast<size_t>(t) * H, H, lane);
+    float* l = s_logits + static_cast<size_t>(warp) * E;
+    const float* src = logits + static_cast<size_t>(t) * E;
+    float m = -INFINITY;
+    for (int e = lane; e < E; e += 32) {
+      const float v = src[e];
+      l[e] = v;
+      m = fmaxf(m, v);
+    }
+    m = warp_max(m);
+    float z = 0.f;
+    for (int e = lane; e < E; e += 32) z += expf(l[e] - m);
+    z = warp_sum(z);
+    __syncwarp();
+
+    uint32_t taken = 0u;  // bit i <=> expert lane + 32 i already selected
+    float sel = 0.f;
+    int32_t* id_row = ids + static_cast<size_t>(t) * k;
+    float* w_row = wts + static_cast<size_t>(t) * k;
+    for (int j = 0; j < k; ++j) {
+      float bv = -INFINITY;
+      int bi = 0x7fffffff;  // "none"
+      for (int e = lane, i = 0; e < E; e += 32, ++i) {
+        if ((taken >> i) & 1u) continue;
+        const float v = l[e];
+        if (bi == 0x7fffffff || v > bv) {  // ascending scan: equal values keep the lower index
+          bv = v;
+          bi = e;
+        }
+      }
+#pragma unroll
+      for (int o = 16; o; o >>= 1) {
+        const float ov = __shfl_xor_sync(kFull, bv, o);
+        const int oi = __shfl_xor_sync(kFull, bi, o);
+        const bool take =
+            oi != 0x7fffffff && (bi == 0x7fffffff || ov > bv || (ov == bv && oi < bi));
+        if (take) {
+          bv = ov;
+          bi = oi;
+        }
+      }
+      if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
+      const float ex = expf(bv - m);
+      sel += ex;
+      if (lane == 0) {
+        id_row[j] = bi;
+        w_row[j] = ex;
+      }
+    }
+    __syncwarp();
+    const float denom = renorm ? sel : z;
+    for (int j = lane; j < k; j += 32) w_row[j] = __fdiv_rn(w_row[j], denom);
+
+    if (x != nullptr) {
+      const uint4* xr = reinterpret_cast<const uint4*>(x + static_cast<size_t>(t) * H);
+      for (int i = lane; i < H / 8; i += 32) xmax = absmax8(__ldg(xr + i), xmax);
+      xmax = warp_max(xmax);
+    }
   }
   if (amax_partials != nullptr) {
     if (lane == 0) s_amax[warp] = xmax;
@@ -340,200 +331,6 @@ __global__ void __launch_bounds__(kAlignThreads) align_kernel(AlignParams p) {
       for (int w = 0; w < 32; ++w) a = fmaxf(a, s_red[w]);
       p.ctrl->s_x = p.amax_partials ? scale_from_amax(a) : 1.f;
       p.ctrl->num_mtiles = n_tiles;
-    }
-  }
-}
-
-// ------------------------------------------------------------------ fused front (small batches)
-// Bounded waits of the grid barrier below.
-__device__ bool wait_u64_eq(const unsigned long long* a, unsigned long long v, uint64_t limit_ns) {
-  const volatile unsigned long long* va = a;
-  const uint64_t t0 = global_timer_ns();
-  while (*va != v) {
-    if (global_timer_ns() - t0 > limit_ns) return false;
-    __nanosleep(64);
-  }
-  return true;
-}
-
-__device__ bool wait_u32_ge(const unsigned* a, unsigned v, uint64_t limit_ns) {
-  const volatile unsigned* va = a;
-  const uint64_t t0 = global_timer_ns();
-  while (*va < v) {
-    if (global_timer_ns() - t0 > limit_ns) return false;
-    __nanosleep(64);
-  }
-  return true;
-}
-
-// Writes the GEMM row-tile list from the per-expert padded segments (one
-// expert per thread, tid < E; all 1024 threads must call).  Each expert's
-// segment is split into ceil(padded / bn_max) equal tiles (multiples of bm);
-// every entry also carries the expert's tile count and first tile index.
-__device__ int write_mtiles(int tid, int E, int padded, int seg_off, int bm, int bn_max,
-                            int4* __restrict__ mtiles, int* s_tmp) {
-  const int nt = (tid < E && padded > 0) ? (padded + bn_max - 1) / bn_max : 0;
-  int n_tiles = 0;
-  const int first = block_exclusive_scan_1024(nt, s_tmp, &n_tiles);
-  if (nt > 0) {
-    const int per = ((padded + nt - 1) / nt + bm - 1) / bm * bm;
-    for (int j = 0; j < nt; ++j) {
-      const int rows = min(per, padded - j * per);
-      mtiles[first + j] = make_int4(tid, seg_off + j * per, rows | (nt << 12), first);
-    }
-  }
-  return n_tiles;
-}
-
-// One cooperative launch replaces router + alignment + gather when the batch
-// is small (decode): phase 1 routes the tokens (warp per token) and takes the
-// per-CTA amax of x; a grid barrier; phase 2 has every CTA align all T*k
-// pairs in shared memory (cheap for small T*k), CTA 0 publish the metadata the
-// GEMMs read, and all CTAs gather/quantise their share of the aligned rows.
-// The barrier is armed by CTA 0 with a per-call epoch, so no state has to
-// survive between calls; its waits are bounded (status word on timeout).
-__global__ void __launch_bounds__(kFrontThreads, 1) front_small_kernel(FrontParams p) {
-  extern __shared__ int s_front[];
-  __shared__ int s_tmp[32];
-  __shared__ float s_red[32];
-  const int E = p.E;
-  float* s_logits = reinterpret_cast<float*>(s_front);  // [32][E]
-  int* s_cnt = s_front + 32 * E;                        // [E]
-  int* s_run = s_cnt + E;                               // [E]
-  int* s_sorted = s_run + E;                            // [T*k + 15 E]
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int G = gridDim.x;
-  const int P = p.T * p.k;
-  Ctrl* ctrl = p.ctrl;
-
-  // phase 0: per-call resets; CTA 0 arms the barrier for this call
-  if (blockIdx.x == 0 && tid == 0) {
-    ctrl->err = 0;
-    ctrl->amax_h = 0u;
-    ctrl->bar_count = 0u;
-    __threadfence();
-    atomicExch(&ctrl->bar_epoch, p.epoch);
-  }
-  for (int i = blockIdx.x * kFrontThreads + tid; i < p.n_zero; i += G * kFrontThreads)
-    p.zero_ints[i] = 0;
-  {
-    float4* a4 = reinterpret_cast<float4*>(p.acc);
-    for (long long i = static_cast<long long>(blockIdx.x) * kFrontThreads + tid; i < p.acc_elems / 4;
-         i += static_cast<long long>(G) * kFrontThreads)
-      a4[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-  }
-
-  // phase 1: routing and amax of x
-  float xmax = 0.f;
-  for (int t = blockIdx.x * 32 + warp; t < p.T; t += G * 32) {
-    route_token(p.logits + static_cast<size_t>(t) * E, E, p.k, p.renorm, s_logits + warp * E,
-                p.ids + static_cast<size_t>(t) * p.k, p.wts + static_cast<size_t>(t) * p.k, lane);
-    if (p.fp8) xmax = fmaxf(xmax, row_absmax(p.x + static_cast<size_t>(t) * p.H, p.H, lane));
-  }
-  if (lane == 0) s_red[warp] = xmax;
-  __syncthreads();
-  if (tid == 0) {
-    float m = 0.f;
-    for (int w = 0; w < 32; ++w) m = fmaxf(m, s_red[w]);
-    p.amax_partials[blockIdx.x] = m;
-    // grid barrier: wait for this call's epoch, arrive, wait for everyone
-    __threadfence();
-    bool ok = wait_u64_eq(&ctrl->bar_epoch, p.epoch, p.timeout_ns);
-    if (ok) {
-      atomicAdd(&ctrl->bar_count, 1u);
-      ok = wait_u32_ge(&ctrl->bar_count, static_cast<unsigned>(G), p.timeout_ns);
-    }
-    __threadfence();
-    if (!ok) atomicOr(&ctrl->err, kDevErrTimeout);
-  }
-  __syncthreads();
-  pdl_trigger();  // the next kernel may set itself up; it waits for this one to finish
-
-  // phase 2: counts, padded offsets and stable placement of every pair
-  for (int e = tid; e < E; e += kFrontThreads) s_cnt[e] = 0;
-  __syncthreads();
-  for (int q0 = 0; q0 < P; q0 += kFrontThreads) {
-    const int q = q0 + tid;
-    const int e = q < P ? __ldcg(p.ids + q) : -1;
-    const bool valid = q < P && static_cast<unsigned>(e) < static_cast<unsigned>(E);
-    const unsigned mask = __match_any_sync(kFull, valid ? e : -1);
-    if (valid && lane == __ffs(mask) - 1) atomicAdd(&s_cnt[e], __popc(mask));
-  }
-  __syncthreads();
-  const int c = tid < E ? s_cnt[tid] : 0;
-  const int padded = (c + kAlignBlock - 1) / kAlignBlock * kAlignBlock;
-  int total = 0;
-  const int off = block_exclusive_scan_1024(padded, s_tmp, &total);
-  if (tid < E) s_run[tid] = off;
-  __syncthreads();
-  if (warp == 0) {
-    for (int q0 = 0; q0 < P; q0 += 32) {
-      const int q = q0 + lane;
-      const int e = q < P ? __ldcg(p.ids + q) : -1;
-      const bool valid = q < P && static_cast<unsigned>(e) < static_cast<unsigned>(E);
-      const unsigned mask = __match_any_sync(kFull, valid ? e : -1);
-      const int leader = __ffs(mask) - 1;
-      int slot = 0;
-      if (valid && lane == leader) {
-        slot = s_run[e];
-        s_run[e] = slot + __popc(mask);
-      }
-      slot = __shfl_sync(kFull, slot, leader);
-      if (valid) s_sorted[slot + __popc(mask & ((1u << lane) - 1u))] = q;
-      __syncwarp();
-    }
-  }
-  if (tid < E)
-    for (int i = c; i < padded; ++i) s_sorted[off + i] = P;  // padding sentinels
-  // activation scale of x from every CTA's partial amax
-  float m = 0.f;
-  if (p.fp8)
-    for (int i = tid; i < G; i += kFrontThreads) m = fmaxf(m, __ldcg(p.amax_partials + i));
-  m = warp_max(m);
-  __syncthreads();
-  if (lane == 0) s_red[warp] = m;
-  __syncthreads();
-  float s_x = 1.f;
-  if (p.fp8) {
-    float a = 0.f;
-    for (int w = 0; w < 32; ++w) a = fmaxf(a, s_red[w]);
-    s_x = scale_from_amax(a);
-  }
-
-  if (blockIdx.x == 0) {  // uniform per block: metadata for the GEMMs and the caller
-    if (tid < E) {
-      p.counts[tid] = c;
-      p.offsets[tid] = off;
-    }
-    if (tid == 0) p.offsets[E] = total;
-    for (int r = tid; r < total; r += kFrontThreads) p.sorted_ids[r] = s_sorted[r];
-    const int n_tiles = write_mtiles(tid, E, padded, off, kAlignBlock, p.bn_max, p.mtiles, s_tmp);
-    if (tid == 0) {
-      ctrl->num_padded = total;
-      ctrl->num_mtiles = n_tiles;
-      ctrl->s_x = s_x;
-    }
-  }
-
-  // gather: one warp per aligned row
-  for (int r = blockIdx.x * 32 + warp; r < total; r += G * 32) {
-    const int q = s_sorted[r];
-    if (p.fp8) {
-      uint4* dst = reinterpret_cast<uint4*>(static_cast<uint8_t*>(p.xs) + static_cast<size_t>(r) * p.H);
-      const uint4* src = reinterpret_cast<const uint4*>(p.x + static_cast<size_t>(q / p.k) * p.H);
-      for (int ch = lane; ch < p.H / 16; ch += 32) {
-        uint4 v = make_uint4(0, 0, 0, 0);
-        if (q < P) {
-          const uint2 a = quant8(__ldg(src + 2 * ch), s_x);
-          const uint2 b = quant8(__ldg(src + 2 * ch + 1), s_x);
-          v = make_uint4(a.x, a.y, b.x, b.y);
-        }
-        dst[ch] = v;
-      }
-    } else {
-      uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.xs) + static_cast<size_t>(r) * p.H);
-      const uint4* src = reinterpret_cast<const uint4*>(p.x + static_cast<size_t>(q / p.k) * p.H);
-      for (int ch = lane; ch < p.H / 8; ch += 32) dst[ch] = q < P ? __ldg(src + ch) : make_uint4(0, 0, 0, 0);
     }
   }
 }
@@ -708,44 +505,6 @@ cudaError_t launch_route_topk(const float* logits, int T, int E, int k, int reno
 }
 
 int align_chunk() { return kAlignChunk; }
-
-int front_grid(int T, int k, int E, int num_sms) {
-  // enough warps for one token each and for one aligned row each
-  const long long rows = static_cast<long long>(T) * k + static_cast<long long>(E) * (kAlignBlock - 1);
-  long long g = std::max<long long>((T + 31) / 32, (rows + 31) / 32);
-  g = std::min<long long>(g, num_sms);
-  return static_cast<int>(std::max<long long>(g, 1));
-}
-
-cudaError_t launch_front(const FrontParams& p, int grid, cudaStream_t st) {
-  const size_t smem = (static_cast<size_t>(32) * p.E + 2 * p.E + static_cast<size_t>(p.T) * p.k +
-                       static_cast<size_t>(p.E) * (kAlignBlock - 1)) * sizeof(int);
-  static thread_local int configured_device = -1;
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (configured_device != dev) {
-    const size_t max_smem = (32 * kFrontMaxExperts + 2 * kFrontMaxExperts + kFrontMaxPairs +
-                             kFrontMaxExperts * (kAlignBlock - 1)) * sizeof(int);
-    cudaError_t e = checked(cudaFuncSetAttribute(front_small_kernel,
-                                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                 static_cast<int>(max_smem)),
-                            "smem attribute");
-    if (e != cudaSuccess) return e;
-    configured_device = dev;
-  }
-  // cooperative: every CTA is resident at once, which the grid barrier needs
-  cudaLaunchConfig_t cfg{};
-  cfg.gridDim = dim3(grid);
-  cfg.blockDim = dim3(kFrontThreads);
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = st;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeCooperative;
-  attr[0].val.cooperative = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return checked(cudaLaunchKernelEx(&cfg, front_small_kernel, p), "cooperative launch");
-}
 
 cudaError_t launch_align(const AlignParams& p, cudaStream_t st) {
   const size_t smem = static_cast<size_t>(p.E) * 4 * sizeof(int) + 32u * p.E * sizeof(uint16_t);
