@@ -110,6 +110,15 @@ __device__ __forceinline__ Range cta_range(long long total) {
   return r;
 }
 
+// Same split rounded to whole tiles (no tile is cut between CTAs).
+__device__ __forceinline__ Range cta_range_whole_tiles(int tiles, int K) {
+  Range r;
+  r.total = static_cast<long long>(tiles) * K;
+  r.beg = static_cast<long long>(tiles) * blockIdx.x / gridDim.x * K;
+  r.end = static_cast<long long>(tiles) * (blockIdx.x + 1) / gridDim.x * K;
+  return r;
+}
+
 // CTA whose range holds flat index i.
 __device__ __forceinline__ int owner_of(long long i, long long total) {
   return static_cast<int>(((i + 1) * gridDim.x - 1) / total);
@@ -188,13 +197,18 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 
   const int K = p.k_steps;
   const int tiles = p.ctrl->num_mtiles * p.nb_count;
-  const Range rg = cta_range(static_cast<long long>(tiles) * K);
+  // rows written per pair cannot take partial sums: whole tiles then
+  const Range rg = (!kSwiGLU && p.pair_out != nullptr)
+                       ? cta_range_whole_tiles(tiles, K)
+                       : cta_range(static_cast<long long>(tiles) * K);
   const uint64_t limit = p.timeout_ns;
 
   if (warp == 0) {
     // ------------------------------------------------ TMA producer
     if (lane == 0) {
-      const uint64_t pol_w = policy_evict_first();
+      // decode: a weight block is read once, keep it from displacing reused
+      // lines; prefill: several row tiles of an expert reuse it from L2
+      const uint64_t pol_w = p.weights_evict_first ? policy_evict_first() : policy_evict_last();
       uint32_t it = 0;
       bool ok = true;
       for (long long i = rg.beg; i < rg.end && ok;) {
@@ -387,6 +401,26 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 if (p.sorted_ids[r] < p.P) amax = fmaxf(amax, fabsf(hv));
               }
             }
+          }
+        }
+      } else if (p.pair_out != nullptr) {
+        // large batches: y * s * topk_weight as bf16 at the pair's row (tiles
+        // are whole here, see the range split); the token sum comes after
+        for (int c0 = 0; c0 < t.n; c0 += 16) {
+          float y[16];
+          tmem_ld16(tbase + c0, y);
+          int pid = p.P;
+          float wscale = 0.f;
+          if (lane < 16) {
+            pid = p.sorted_ids[t.row0 + c0 + lane];
+            if (pid < p.P) wscale = sc * p.topk_w[pid];
+          }
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const int pj = __shfl_sync(0xffffffffu, pid, j);
+            const float wj = __shfl_sync(0xffffffffu, wscale, j);
+            if (pj < p.P)
+              p.pair_out[static_cast<size_t>(pj) * p.ldo + col] = __float2bfloat16_rn(y[j] * wj);
           }
         }
       } else {

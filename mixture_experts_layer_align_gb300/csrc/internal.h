@@ -125,16 +125,26 @@ struct GemmParams {
   const float* topk_w;   // [P]
   void* h_out;           // gate/up: [rows, I], fp32 (FP8 path) or bf16 (bf16 path)
   int ldh;
-  float* acc_out;        // down: [T, H] fp32
+  float* acc_out;        // down, combine by reduction: [T, H] fp32
   int ldo;
+  // down, combine by rows (large batches): y * s * topk_weight as bf16 at row
+  // `pair` of [T*k, H]; a separate kernel sums each token's k rows.  Null
+  // selects the bulk reductions into acc_out.
+  __nv_bfloat16* pair_out;
   // gate/up tiles split across CTAs: per-tile arrival counters (zeroed by the
   // router kernel) and two partial-accumulator slots per CTA
   int* tile_cnt;
   float* part;
+  int weights_evict_first;  // 1: each weight block is used by one row tile (decode)
   unsigned long long timeout_ns;
   int debug;
   unsigned long long* trace;  // [MOE_TRACE_MAX_CTAS][4] stamps or null
 };
+
+// Sum of the k weighted expert rows of every token: out[t] = sum_j rows[t*k+j]
+// (fp32 accumulation, bf16 result).
+cudaError_t launch_combine_rows(const __nv_bfloat16* rows, int T, int k, int H,
+                                __nv_bfloat16* out, int num_sms, cudaStream_t st);
 
 // Partial-accumulator slot (gate and up, bn_max columns x 128 rows, fp32).
 __host__ __device__ inline size_t gemm_part_slot_floats(int bn_max) { return static_cast<size_t>(2) * bn_max * 128; }

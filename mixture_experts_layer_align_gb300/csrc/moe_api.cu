@@ -110,6 +110,11 @@ struct Layout {
   int bn_max = 0;
   int ctas = 0;
   int n_tile_cnt = 0;
+  // Combine of the down projection: bulk reductions into an fp32 [T, H]
+  // buffer (small batches), or weighted bf16 rows per pair summed by a
+  // separate kernel (large batches, where the reductions would saturate L2).
+  bool combine_rows = false;
+  size_t rows = 0;
   size_t ctrl = 0, trace = 0, partials = 0, ids = 0, wts = 0, counts = 0, offsets = 0,
          sorted = 0, mtiles = 0, tile_cnt = 0, part = 0, xs = 0, h = 0, hq = 0, acc = 0,
          total = 0;
@@ -144,7 +149,9 @@ Layout make_layout(int T, int H, int I, int E, int k, bool fp8) {
   L.xs = take(static_cast<size_t>(L.pad_max) * H * (fp8 ? 1 : 2));
   L.h = take(static_cast<size_t>(L.pad_max) * I * (fp8 ? 4 : 2));
   L.hq = take(fp8 ? static_cast<size_t>(L.pad_max) * I : 0);
-  L.acc = take(static_cast<size_t>(T) * H * sizeof(float));
+  L.combine_rows = L.P * H > (8ll << 20);
+  L.acc = take(L.combine_rows ? 0 : static_cast<size_t>(T) * H * sizeof(float));
+  L.rows = take(L.combine_rows ? static_cast<size_t>(L.P) * H * 2 : 0);
   L.total = off;
   return L;
 }
@@ -321,6 +328,8 @@ moe_status_t fused_forward_impl(const moe_fused_args* a, void* workspace, size_t
   void* h = ws + L.h;
   uint8_t* hq = ws + L.hq;
   float* acc = reinterpret_cast<float*>(ws + L.acc);
+  __nv_bfloat16* pair_rows = reinterpret_cast<__nv_bfloat16*>(ws + L.rows);
+  const long long acc_elems = L.combine_rows ? 0 : static_cast<long long>(T) * H;
 
   const long long touched = std::min<long long>(E, P);
   const int bn_max = L.bn_max;
@@ -356,7 +365,7 @@ moe_status_t fused_forward_impl(const moe_fused_args* a, void* workspace, size_t
   if (events && cudaEventRecord(events[2], stream) != cudaSuccess) return MOE_ERR_CUDA;
   // 3. gather (+ quantise) the routed rows of x; zero the combine buffer
   if (launch_gather_x(static_cast<const __nv_bfloat16*>(a->x), H, sorted, ctrl, static_cast<int>(P),
-                      k, xs, fp8, acc, static_cast<long long>(T) * H, L.pad_max, dev.num_sms,
+                      k, xs, fp8, acc, acc_elems, L.pad_max, dev.num_sms,
                       s) != cudaSuccess)
     return MOE_ERR_CUDA;
 
@@ -398,6 +407,9 @@ moe_status_t fused_forward_impl(const moe_fused_args* a, void* workspace, size_t
   g1.ldh = I;
   g1.tile_cnt = tile_cnt;
   g1.part = part;
+  // a weight block serves one row tile when an expert's rows fit one tile
+  g1.weights_evict_first = (P + touched - 1) / touched <= bn_max ? 1 : 0;
+  g1.pair_out = nullptr;
   g1.timeout_ns = (a->debug_flags & MOE_DEBUG_FORCE_TIMEOUT) ? MOE_DEBUG_TIMEOUT_MS * 1000000ull
                                                              : kWaitLimitNs;
   g1.debug = a->debug_flags;
@@ -433,16 +445,22 @@ moe_status_t fused_forward_impl(const moe_fused_args* a, void* workspace, size_t
   g2.ldo = H;
   g2.tile_cnt = nullptr;
   g2.part = nullptr;
+  g2.pair_out = L.combine_rows ? pair_rows : nullptr;
   g2.trace = (a->debug_flags & MOE_DEBUG_TRACE) ? trace + MOE_TRACE_MAX_CTAS * 4 : nullptr;
   const long long work2 = max_tiles * g2.nb_count * g2.k_steps;
   const int grid2 = static_cast<int>(std::max<long long>(1, std::min<long long>(ctas, work2)));
   if (launch_gemm(bf16, false, g2, tm_w2, tm_h, grid2, s) != cudaSuccess) return MOE_ERR_CUDA;
 
-  // 7. fp32 combine buffer -> bf16 output
+  // 7. fp32 combine buffer -> bf16 output, or the sum of each token's k rows
   if (events && cudaEventRecord(events[6], stream) != cudaSuccess) return MOE_ERR_CUDA;
-  if (launch_finalize(acc, static_cast<__nv_bfloat16*>(a->out), static_cast<long long>(T) * H,
-                      dev.num_sms, s) != cudaSuccess)
+  if (L.combine_rows) {
+    if (launch_combine_rows(pair_rows, T, k, H, static_cast<__nv_bfloat16*>(a->out), dev.num_sms,
+                            s) != cudaSuccess)
+      return MOE_ERR_CUDA;
+  } else if (launch_finalize(acc, static_cast<__nv_bfloat16*>(a->out),
+                             static_cast<long long>(T) * H, dev.num_sms, s) != cudaSuccess) {
     return MOE_ERR_CUDA;
+  }
   if (events && cudaEventRecord(events[7], stream) != cudaSuccess) return MOE_ERR_CUDA;
   return MOE_OK;
 }

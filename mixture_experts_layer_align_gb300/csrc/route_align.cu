@@ -196,7 +196,8 @@ __global__ void __launch_bounds__(kRouteWarps * 32)
 // order with __match_any_sync ranks.  The resulting order is exactly the
 // ascending pair id order within each expert.
 constexpr int kAlignThreads = 1024;
-constexpr int kAlignChunk = 16384;  // pairs per CTA (<= 65535: per-warp counts are uint16)
+constexpr int kAlignChunk = 4096;  // pairs per CTA (<= 65535: per-warp counts are uint16)
+constexpr int kAlignUnroll = 8;    // id loads in flight per thread in the histogram pass
 
 __global__ void __launch_bounds__(kAlignThreads) align_kernel(AlignParams p) {
   extern __shared__ int s_align[];
@@ -226,17 +227,26 @@ __global__ void __launch_bounds__(kAlignThreads) align_kernel(AlignParams p) {
   for (int i = tid; i < 32 * E; i += kAlignThreads) seg[i] = 0;
   __syncthreads();
 
-  // histograms of every pair, and of the pairs before this chunk
-  for (int p0 = 0; p0 < P; p0 += kAlignThreads) {
-    const int q = p0 + tid;
-    const int e = q < P ? p.ids[q] : -1;
-    const bool valid = q < P && static_cast<unsigned>(e) < static_cast<unsigned>(E);
-    const int key = valid ? e : -1;
-    const unsigned mask = __match_any_sync(kFull, key);
-    if (valid && lane == __ffs(mask) - 1) {
-      const int n = __popc(mask);
-      atomicAdd(&hist_all[e], n);
-      if (q < cs) atomicAdd(&hist_before[e], n);
+  // histograms of every pair, and of the pairs before this chunk (loads of
+  // kAlignUnroll rounds issued together: this pass is latency bound)
+  for (int p0 = 0; p0 < P; p0 += kAlignThreads * kAlignUnroll) {
+    int ev[kAlignUnroll];
+#pragma unroll
+    for (int u = 0; u < kAlignUnroll; ++u) {
+      const int q = p0 + u * kAlignThreads + tid;
+      ev[u] = q < P ? __ldg(p.ids + q) : -1;
+    }
+#pragma unroll
+    for (int u = 0; u < kAlignUnroll; ++u) {
+      const int q = p0 + u * kAlignThreads + tid;
+      const int e = ev[u];
+      const bool valid = q < P && static_cast<unsigned>(e) < static_cast<unsigned>(E);
+      const unsigned mask = __match_any_sync(kFull, valid ? e : -1);
+      if (valid && lane == __ffs(mask) - 1) {
+        const int n = __popc(mask);
+        atomicAdd(&hist_all[e], n);
+        if (q < cs) atomicAdd(&hist_before[e], n);
+      }
     }
   }
   // per-warp counts of this CTA's chunk
@@ -436,6 +446,47 @@ __global__ void __launch_bounds__(256)
   }
 }
 
+// ------------------------------------------------------------------ combine rows
+// out[t] = sum over the k slots of the weighted expert rows of token t, fp32
+// accumulation in slot order, one bf16 rounding.  8 columns per thread.
+__global__ void __launch_bounds__(256)
+    combine_rows_kernel(const __nv_bfloat16* __restrict__ rows, int T, int k, int H,
+                        __nv_bfloat16* __restrict__ out) {
+  pdl_wait();
+  pdl_trigger();
+  const int per_row = H / 8;
+  const long long n8 = static_cast<long long>(T) * per_row;
+  const uint4* src = reinterpret_cast<const uint4*>(rows);
+  uint4* dst = reinterpret_cast<uint4*>(out);
+  for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < n8;
+       i += static_cast<long long>(gridDim.x) * blockDim.x) {
+    const long long t = i / per_row;
+    const long long c = i - t * per_row;
+    float a[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    for (int j = 0; j < k; ++j) {
+      const uint4 v = __ldg(src + (t * k + j) * per_row + c);
+      a[0] += bf16_lo(v.x);
+      a[1] += bf16_hi(v.x);
+      a[2] += bf16_lo(v.y);
+      a[3] += bf16_hi(v.y);
+      a[4] += bf16_lo(v.z);
+      a[5] += bf16_hi(v.z);
+      a[6] += bf16_lo(v.w);
+      a[7] += bf16_hi(v.w);
+    }
+    __nv_bfloat162 b0 = __floats2bfloat162_rn(a[0], a[1]);
+    __nv_bfloat162 b1 = __floats2bfloat162_rn(a[2], a[3]);
+    __nv_bfloat162 b2 = __floats2bfloat162_rn(a[4], a[5]);
+    __nv_bfloat162 b3 = __floats2bfloat162_rn(a[6], a[7]);
+    uint4 r;
+    r.x = *reinterpret_cast<uint32_t*>(&b0);
+    r.y = *reinterpret_cast<uint32_t*>(&b1);
+    r.z = *reinterpret_cast<uint32_t*>(&b2);
+    r.w = *reinterpret_cast<uint32_t*>(&b3);
+    dst[i] = r;
+  }
+}
+
 // ------------------------------------------------------------------ quantize (standalone)
 __global__ void __launch_bounds__(256)
     amax_kernel(const __nv_bfloat16* __restrict__ x, long long n8, float* __restrict__ partials) {
@@ -540,6 +591,12 @@ cudaError_t launch_finalize(const float* acc, __nv_bfloat16* out, long long n, i
                             cudaStream_t st) {
   const int grid = capped_grid(n / 8, 256, num_sms, 8);
   return launch_pdl(finalize_kernel, dim3(grid), dim3(256), 0, st, acc, out, n / 8);
+}
+
+cudaError_t launch_combine_rows(const __nv_bfloat16* rows, int T, int k, int H,
+                                __nv_bfloat16* out, int num_sms, cudaStream_t st) {
+  const int grid = capped_grid(static_cast<long long>(T) * H / 8, 256, num_sms, 8);
+  return launch_pdl(combine_rows_kernel, dim3(grid), dim3(256), 0, st, rows, T, k, H, out);
 }
 
 cudaError_t launch_quantize_e4m3(const __nv_bfloat16* x, long long n, uint8_t* xq, float* scale,
