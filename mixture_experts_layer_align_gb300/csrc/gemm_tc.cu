@@ -136,6 +136,12 @@ __device__ __forceinline__ float* part_slot(const GemmParams& p, int c, long lon
   return p.part + (static_cast<size_t>(c) * 2 + s) * gemm_part_slot_floats(p.bn_max);
 }
 
+// v[s] for a warp-uniform runtime s in [0, 4) without local-memory indexing.
+template <typename V>
+__device__ __forceinline__ V pick4(const V (&v)[4], int s) {
+  return s == 0 ? v[0] : (s == 1 ? v[1] : (s == 2 ? v[2] : v[3]));
+}
+
 template <bool kBF16, bool kSwiGLU>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     moe_gemm_kernel(const __grid_constant__ GemmParams p, const __grid_constant__ CUtensorMap tm_a,
@@ -321,6 +327,17 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       const Tile t = decode_tile(p, tile_of_seq(u, tiles));
       const uint32_t a = tt % static_cast<uint32_t>(p.num_acc);
       const uint32_t aph = (tt / static_cast<uint32_t>(p.num_acc)) & 1u;
+      // column metadata of the tile, fetched while the MMAs run: lane l holds
+      // columns l, l+32, l+64, l+96 (row tiles have at most 128 columns)
+      int cpid[4];
+      float cw[4];
+#pragma unroll
+      for (int s4 = 0; s4 < 4; ++s4) {
+        const int c = s4 * 32 + lane;
+        cpid[s4] = c < t.n ? p.sorted_ids[t.row0 + c] : p.P;
+        cw[s4] = (!kSwiGLU && cpid[s4] < p.P) ? p.topk_w[cpid[s4]] : 0.f;
+      }
+      const float wsc = kBF16 ? 1.f : p.w_scale[t.e];
       int got = 0;
       if (lane == 0) got = mbar_wait(tfull + a, aph, abort_flag, limit) ? 1 : 0;
       got = __shfl_sync(0xffffffffu, got, 0);
@@ -330,7 +347,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         break;
       }
       tc_fence_after_sync();
-      const float sc = kBF16 ? 1.f : act_s * p.w_scale[t.e];
+      const float sc = act_s * wsc;
       const uint32_t tbase = tmem + (static_cast<uint32_t>(q * 32) << 16) +
                              a * static_cast<uint32_t>(p.acc_stride);
       const int col = t.nb * 128 + row_l;
@@ -368,6 +385,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         }
         if (finish) {
           for (int c0 = 0; c0 < t.n; c0 += 16) {
+            const int pid_c = pick4(cpid, c0 >> 5);  // column (c0 & 31) + lane of this block
             float g[16], v[16];
             tmem_ld16x2(tbase + c0, tbase + p.bn_max + c0, g, v);
             if (!whole) {
@@ -398,7 +416,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 // intermediate bf16 rounding would move values across E4M3
                 // rounding boundaries and cost percent-level output error
                 static_cast<float*>(p.h_out)[at] = hv;
-                if (p.sorted_ids[r] < p.P) amax = fmaxf(amax, fabsf(hv));
+                const int pid = __shfl_sync(0xffffffffu, pid_c, (c0 & 31) + j);
+                if (pid < p.P) amax = fmaxf(amax, fabsf(hv));
               }
             }
           }
@@ -409,16 +428,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         for (int c0 = 0; c0 < t.n; c0 += 16) {
           float y[16];
           tmem_ld16(tbase + c0, y);
-          int pid = p.P;
-          float wscale = 0.f;
-          if (lane < 16) {
-            pid = p.sorted_ids[t.row0 + c0 + lane];
-            if (pid < p.P) wscale = sc * p.topk_w[pid];
-          }
+          const int pid_c = pick4(cpid, c0 >> 5);
+          const float w_c = sc * pick4(cw, c0 >> 5);
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
-            const int pj = __shfl_sync(0xffffffffu, pid, j);
-            const float wj = __shfl_sync(0xffffffffu, wscale, j);
+            const int pj = __shfl_sync(0xffffffffu, pid_c, (c0 & 31) + j);
+            const float wj = __shfl_sync(0xffffffffu, w_c, (c0 & 31) + j);
             if (pj < p.P)
               p.pair_out[static_cast<size_t>(pj) * p.ldo + col] = __float2bfloat16_rn(y[j] * wj);
           }
@@ -432,13 +447,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           float y[16];
           tmem_ld16(tbase + c0, y);
           float* buf = wstage + (n_chunks & 1u) * 16 * 32;
-          int pid = p.P;
-          float wscale = 0.f;
-          if (lane < 16) {
-            pid = p.sorted_ids[t.row0 + c0 + lane];
-            if (pid < p.P) wscale = sc * p.topk_w[pid];
-            bulk_wait_read<1>();  // this buffer's reductions from two chunks ago have read it
-          }
+          // lane j < 16 handles column c0 + j
+          const int pid = __shfl_sync(0xffffffffu, pick4(cpid, c0 >> 5), (c0 & 31) + (lane & 15));
+          const float wscale =
+              sc * __shfl_sync(0xffffffffu, pick4(cw, c0 >> 5), (c0 & 31) + (lane & 15));
+          if (lane < 16) bulk_wait_read<1>();  // this buffer's reductions from two chunks ago have read it
           __syncwarp();
 #pragma unroll
           for (int j = 0; j < 16; ++j) buf[j * 32 + lane] = y[j] * __shfl_sync(0xffffffffu, wscale, j);
