@@ -145,7 +145,8 @@ __device__ __forceinline__ V pick4(const V (&v)[4], int s) {
 template <bool kBF16, bool kSwiGLU>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     moe_gemm_kernel(const __grid_constant__ GemmParams p, const __grid_constant__ CUtensorMap tm_a,
-                    const __grid_constant__ CUtensorMap tm_b) {
+                    const __grid_constant__ CUtensorMap tm_b,
+                    const __grid_constant__ CUtensorMap tm_b64) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -186,6 +187,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   if (warp == 0 && lane == 0) {
     prefetch_tensormap(&tm_a);
     prefetch_tensormap(&tm_b);
+    prefetch_tensormap(&tm_b64);
   }
   if (warp == 1) {
     tmem_alloc(tmem_slot, static_cast<uint32_t>(p.tmem_cols));
@@ -236,7 +238,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           const int kc = kk * p.k_elems;
           tma_load_2d_hint(sa, &tm_a, full + s, kc, wrow, pol_w);
           if (kSwiGLU) tma_load_2d_hint(sa + 16384, &tm_a, full + s, kc, wrow + p.up_offset, pol_w);
-          for (int j = 0; j < t.n; j += 16) tma_load_2d(sb + j * 128, &tm_b, full + s, kc, t.row0 + j);
+          // token rows: 64-row boxes, then 16-row boxes for the remainder
+          int j = 0;
+          for (; j + 64 <= t.n; j += 64) tma_load_2d(sb + j * 128, &tm_b64, full + s, kc, t.row0 + j);
+          for (; j < t.n; j += 16) tma_load_2d(sb + j * 128, &tm_b, full + s, kc, t.row0 + j);
         }
         i += k1 - k0;
       }
@@ -498,8 +503,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 }
 
 template <bool kBF16, bool kSwiGLU>
-cudaError_t launch_one(const GemmParams& p, const CUtensorMap& ta, const CUtensorMap& tb, int grid,
-                       cudaStream_t st) {
+cudaError_t launch_one(const GemmParams& p, const CUtensorMap& ta, const CUtensorMap& tb,
+                       const CUtensorMap& tb64, int grid, cudaStream_t st) {
   static thread_local int configured_device = -1;
   int dev = 0;
   cudaGetDevice(&dev);
@@ -511,7 +516,7 @@ cudaError_t launch_one(const GemmParams& p, const CUtensorMap& ta, const CUtenso
   }
   const size_t smem = gemm_smem_bytes(kSwiGLU, p.bn_max, p.stages);
   return launch_pdl(moe_gemm_kernel<kBF16, kSwiGLU>, dim3(grid), dim3(kGemmThreads), smem, st, p,
-                    ta, tb);
+                    ta, tb, tb64);
 }
 
 }  // namespace
@@ -533,13 +538,14 @@ int gemm_max_stages(bool swiglu, int bn_max) {
 }
 
 cudaError_t launch_gemm(bool bf16, bool swiglu, const GemmParams& p, const CUtensorMap& ta,
-                        const CUtensorMap& tb, int grid, cudaStream_t st) {
+                        const CUtensorMap& tb, const CUtensorMap& tb64, int grid,
+                        cudaStream_t st) {
   if (bf16) {
-    return swiglu ? launch_one<true, true>(p, ta, tb, grid, st)
-                  : launch_one<true, false>(p, ta, tb, grid, st);
+    return swiglu ? launch_one<true, true>(p, ta, tb, tb64, grid, st)
+                  : launch_one<true, false>(p, ta, tb, tb64, grid, st);
   }
-  return swiglu ? launch_one<false, true>(p, ta, tb, grid, st)
-                : launch_one<false, false>(p, ta, tb, grid, st);
+  return swiglu ? launch_one<false, true>(p, ta, tb, tb64, grid, st)
+                : launch_one<false, false>(p, ta, tb, tb64, grid, st);
 }
 
 }  // namespace moe

@@ -152,7 +152,9 @@ __host__ __device__ inline size_t gemm_part_slot_floats(int bn_max) { return sta
 constexpr int kGemmThreads = 192;  // warp 0 TMA, warp 1 MMA, warps 2..5 epilogue
 size_t gemm_smem_bytes(bool swiglu, int bn_max, int stages);
 int gemm_max_stages(bool swiglu, int bn_max);
+// tmb / tmb64: the token operand with 16-row and 64-row boxes.
 cudaError_t launch_gemm(bool bf16, bool swiglu, const GemmParams& p, const CUtensorMap& tma,
-                        const CUtensorMap& tmb, int grid, cudaStream_t st);
+                        const CUtensorMap& tmb, const CUtensorMap& tmb64, int grid,
+                        cudaStream_t st);
 
 }  // namespace moe

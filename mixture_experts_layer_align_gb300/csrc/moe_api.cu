@@ -370,13 +370,15 @@ moe_status_t fused_forward_impl(const moe_fused_args* a, void* workspace, size_t
     return MOE_ERR_CUDA;
 
   // TMA descriptors
-  CUtensorMap tm_w13, tm_xs, tm_w2, tm_h;
+  CUtensorMap tm_w13, tm_xs, tm_xs64, tm_w2, tm_h, tm_h64;
   const bool bf16 = !fp8;
+  const void* hb = fp8 ? static_cast<const void*>(hq) : static_cast<const void*>(h);
   if (!make_tmap(&tm_w13, a->w13, bf16, H, static_cast<uint64_t>(E) * 2 * I, 128) ||
       !make_tmap(&tm_xs, xs, bf16, H, L.pad_max, 16) ||
+      !make_tmap(&tm_xs64, xs, bf16, H, L.pad_max, 64) ||
       !make_tmap(&tm_w2, a->w2, bf16, I, static_cast<uint64_t>(E) * H, 128) ||
-      !make_tmap(&tm_h, fp8 ? static_cast<const void*>(hq) : static_cast<const void*>(h), bf16, I,
-                 L.pad_max, 16))
+      !make_tmap(&tm_h, hb, bf16, I, L.pad_max, 16) ||
+      !make_tmap(&tm_h64, hb, bf16, I, L.pad_max, 64))
     return MOE_ERR_CUDA;
 
   const int k_elems = fp8 ? 128 : 64;
@@ -418,7 +420,8 @@ moe_status_t fused_forward_impl(const moe_fused_args* a, void* workspace, size_t
   const long long work1 = max_tiles * g1.nb_count * g1.k_steps;
   const int grid1 = static_cast<int>(std::max<long long>(1, std::min<long long>(ctas, work1)));
   if (events && cudaEventRecord(events[3], stream) != cudaSuccess) return MOE_ERR_CUDA;
-  if (launch_gemm(bf16, true, g1, tm_w13, tm_xs, grid1, s) != cudaSuccess) return MOE_ERR_CUDA;
+  if (launch_gemm(bf16, true, g1, tm_w13, tm_xs, tm_xs64, grid1, s) != cudaSuccess)
+    return MOE_ERR_CUDA;
 
   // 5. dynamic scale of h and its E4M3 codes
   if (events && cudaEventRecord(events[4], stream) != cudaSuccess) return MOE_ERR_CUDA;
@@ -449,7 +452,8 @@ moe_status_t fused_forward_impl(const moe_fused_args* a, void* workspace, size_t
   g2.trace = (a->debug_flags & MOE_DEBUG_TRACE) ? trace + MOE_TRACE_MAX_CTAS * 4 : nullptr;
   const long long work2 = max_tiles * g2.nb_count * g2.k_steps;
   const int grid2 = static_cast<int>(std::max<long long>(1, std::min<long long>(ctas, work2)));
-  if (launch_gemm(bf16, false, g2, tm_w2, tm_h, grid2, s) != cudaSuccess) return MOE_ERR_CUDA;
+  if (launch_gemm(bf16, false, g2, tm_w2, tm_h, tm_h64, grid2, s) != cudaSuccess)
+    return MOE_ERR_CUDA;
 
   // 7. fp32 combine buffer -> bf16 output, or the sum of each token's k rows
   if (events && cudaEventRecord(events[6], stream) != cudaSuccess) return MOE_ERR_CUDA;
