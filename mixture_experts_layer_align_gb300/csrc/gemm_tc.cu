@@ -49,7 +49,7 @@ constexpr int kSmemLimit = 232448;  // 227 KB opt-in per CTA
 constexpr int kSmemSlack = 1024 + 256;
 constexpr int kMaxStages = 8;
 constexpr uint32_t kEpiBarrier = 1;  // named barrier of the 4 epilogue warps
-constexpr uint32_t kEpiThreads = 128;
+constexpr uint32_t kEpiThreads = 32 * kGemmEpiWarps;
 
 struct Tile {
   int e, row0, n, nb;
@@ -178,7 +178,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(tfull + a, 1);
-      mbar_init(tempty + a, 4);
+      mbar_init(tempty + a, kGemmEpiWarps);
     }
     mbar_init(never, 1);
     *abort_flag = 0;
@@ -318,6 +318,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   } else {
     // ------------------------------------------------ epilogue (4 warps)
     const int q = warp & 3;  // TMEM lane quarter this warp may read
+    // the two warps of a quarter split a tile's 16-column chunks: this one
+    // takes chunks c0 = 16 * (2 m + half)
+    const int half = (warp - 2) >> 2;
+    const int c_begin = 16 * half;
     const int row_l = q * 32 + lane;
     float act_s = 1.f;
     if (!kBF16) act_s = p.act_scale_sel == 1 ? p.ctrl->s_x : p.ctrl->s_h;
@@ -366,7 +370,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           c_first = owner_of(t0, rg.total);
           c_last = owner_of(t0 + K - 1, rg.total);
           float* mine = part_slot(p, blockIdx.x, t0, rg.total);
-          for (int c0 = 0; c0 < t.n; c0 += 16) {
+          for (int c0 = c_begin; c0 < t.n; c0 += 32) {
             float g[16], v[16];
             tmem_ld16x2(tbase + c0, tbase + p.bn_max + c0, g, v);
 #pragma unroll
@@ -389,7 +393,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           if (finish) __threadfence();
         }
         if (finish) {
-          for (int c0 = 0; c0 < t.n; c0 += 16) {
+          for (int c0 = c_begin; c0 < t.n; c0 += 32) {
             const int pid_c = pick4(cpid, c0 >> 5);  // column (c0 & 31) + lane of this block
             float g[16], v[16];
             tmem_ld16x2(tbase + c0, tbase + p.bn_max + c0, g, v);
@@ -411,7 +415,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
               const int r = t.row0 + c0 + j;
               const float gv = g[j] * sc;
               const float uv = v[j] * sc;
-              const float hv = gv / (1.f + __expf(-gv)) * uv;
+              const float hv = __fdividef(gv, 1.f + __expf(-gv)) * uv;  // SiLU(g) * u
               const size_t at = static_cast<size_t>(r) * p.ldh + col;
               if (kBF16) {
                 // bf16 weights: h feeds the bf16 down-projection MMA directly
@@ -430,7 +434,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       } else if (p.pair_out != nullptr) {
         // large batches: y * s * topk_weight as bf16 at the pair's row (tiles
         // are whole here, see the range split); the token sum comes after
-        for (int c0 = 0; c0 < t.n; c0 += 16) {
+        for (int c0 = c_begin; c0 < t.n; c0 += 32) {
           float y[16];
           tmem_ld16(tbase + c0, y);
           const int pid_c = pick4(cpid, c0 >> 5);
@@ -447,8 +451,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         // combine: y * s * topk_weight for 16 token columns at a time, staged
         // in shared memory and added into the token rows of the fp32 combine
         // buffer with one bulk asynchronous reduction (128 B) per column
-        float* wstage = stage_out + static_cast<size_t>(q) * 2 * 16 * 32;
-        for (int c0 = 0; c0 < t.n; c0 += 16) {
+        float* wstage = stage_out + static_cast<size_t>(warp - 2) * 2 * 16 * 32;
+        for (int c0 = c_begin; c0 < t.n; c0 += 32) {
           float y[16];
           tmem_ld16(tbase + c0, y);
           float* buf = wstage + (n_chunks & 1u) * 16 * 32;
@@ -521,8 +525,8 @@ cudaError_t launch_one(const GemmParams& p, const CUtensorMap& ta, const CUtenso
 
 }  // namespace
 
-// Combine staging of the down projection: 4 warps x 2 buffers x 16 x 32 fp32.
-constexpr size_t kCombineStaging = 4 * 2 * 16 * 32 * sizeof(float);
+// Combine staging of the down projection: per epilogue warp 2 buffers x 16 x 32 fp32.
+constexpr size_t kCombineStaging = kGemmEpiWarps * 2 * 16 * 32 * sizeof(float);
 
 size_t gemm_smem_bytes(bool swiglu, int bn_max, int stages) {
   const size_t stage = (swiglu ? 32768u : 16384u) + static_cast<size_t>(bn_max) * 128u;

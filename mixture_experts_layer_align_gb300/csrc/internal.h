@@ -149,7 +149,10 @@ cudaError_t launch_combine_rows(const __nv_bfloat16* rows, int T, int k, int H,
 // Partial-accumulator slot (gate and up, bn_max columns x 128 rows, fp32).
 __host__ __device__ inline size_t gemm_part_slot_floats(int bn_max) { return static_cast<size_t>(2) * bn_max * 128; }
 
-constexpr int kGemmThreads = 192;  // warp 0 TMA, warp 1 MMA, warps 2..5 epilogue
+// warp 0 TMA, warp 1 MMA, warps 2..9 epilogue (two warps per TMEM lane
+// quarter, each taking every other 16-column chunk of a tile)
+constexpr int kGemmEpiWarps = 8;
+constexpr int kGemmThreads = 64 + 32 * kGemmEpiWarps;
 size_t gemm_smem_bytes(bool swiglu, int bn_max, int stages);
 int gemm_max_stages(bool swiglu, int bn_max);
 // tmb / tmb64: the token operand with 16-row and 64-row boxes.
