@@ -77,6 +77,9 @@ struct AlignParams {
   int32_t* sorted_ids;
   int32_t* tile_expert;  // may be null
   int32_t* num_padded;   // may be null
+  // per-chunk expert histograms [gridDim][E] from align_hist (large batches);
+  // null: every CTA counts all pairs itself
+  const int32_t* chunk_hist;
   // fused-path extras (null when unused)
   int4* mtiles;          // GEMM row tiles {expert, first row, rows, 0}
   int bn_max;            // max rows of one row tile
@@ -86,12 +89,21 @@ struct AlignParams {
 };
 cudaError_t launch_align(const AlignParams& p, cudaStream_t st);
 int align_chunk();
+// First pass of the two-pass alignment: expert histogram of each chunk of
+// align_chunk() pairs into hist[chunk][E].
+cudaError_t launch_align_hist(const int32_t* ids, int P, int E, int32_t* hist, cudaStream_t st);
+// x (bf16) -> E4M3 codes in token order with ctrl->s_x (large batches quantise
+// each token once, the gather then copies bytes).
+cudaError_t launch_quant_tokens(const __nv_bfloat16* x, long long n, const Ctrl* ctrl,
+                                uint8_t* xq, int num_sms, cudaStream_t st);
 
 // Gather the routed rows of x into aligned order (E4M3 with s_x, or bf16), zero
 // the fp32 combine buffer.
-cudaError_t launch_gather_x(const __nv_bfloat16* x, int H, const int32_t* sorted_ids,
-                            const Ctrl* ctrl, int P, int k, void* xs, bool fp8, float* acc,
-                            long long acc_elems, int max_rows, int num_sms, cudaStream_t st);
+// xq_tok: E4M3 codes of x in token order (FP8 path, large batches) or null.
+cudaError_t launch_gather_x(const __nv_bfloat16* x, const uint8_t* xq_tok, int H,
+                            const int32_t* sorted_ids, const Ctrl* ctrl, int P, int k, void* xs,
+                            bool fp8, float* acc, long long acc_elems, int max_rows, int num_sms,
+                            cudaStream_t st);
 // h (fp32) -> E4M3 with s_h = amax_h / 448 (stored into ctrl->s_h).
 cudaError_t launch_quant_h(const float* h, int I, Ctrl* ctrl, uint8_t* hq, int max_rows,
                            int num_sms, cudaStream_t st);

@@ -115,6 +115,10 @@ struct Layout {
   // separate kernel (large batches, where the reductions would saturate L2).
   bool combine_rows = false;
   size_t rows = 0;
+  // Large batches: two-pass alignment (per-chunk histograms) and x quantised
+  // once per token before the gather.
+  bool large = false;
+  size_t chunk_hist = 0, xq_tok = 0;
   size_t ctrl = 0, trace = 0, partials = 0, ids = 0, wts = 0, counts = 0, offsets = 0,
          sorted = 0, mtiles = 0, tile_cnt = 0, part = 0, xs = 0, h = 0, hq = 0, acc = 0,
          total = 0;
@@ -149,6 +153,9 @@ Layout make_layout(int T, int H, int I, int E, int k, bool fp8) {
   L.xs = take(static_cast<size_t>(L.pad_max) * H * (fp8 ? 1 : 2));
   L.h = take(static_cast<size_t>(L.pad_max) * I * (fp8 ? 4 : 2));
   L.hq = take(fp8 ? static_cast<size_t>(L.pad_max) * I : 0);
+  L.large = L.P > align_chunk();
+  L.chunk_hist = take(L.large ? sizeof(int32_t) * E * ((L.P + align_chunk() - 1) / align_chunk()) : 0);
+  L.xq_tok = take(L.large && fp8 ? static_cast<size_t>(T) * H : 0);
   L.combine_rows = L.P * H > (8ll << 20);
   L.acc = take(L.combine_rows ? 0 : static_cast<size_t>(T) * H * sizeof(float));
   L.rows = take(L.combine_rows ? static_cast<size_t>(L.P) * H * 2 : 0);
@@ -361,11 +368,22 @@ moe_status_t fused_forward_impl(const moe_fused_args* a, void* workspace, size_t
   ap.ctrl = ctrl;
   ap.amax_partials = fp8 ? partials : nullptr;
   ap.n_partials = fp8 ? L.n_partials : 0;
+  int32_t* chunk_hist = reinterpret_cast<int32_t*>(ws + L.chunk_hist);
+  if (L.large) {
+    if (launch_align_hist(ids, static_cast<int>(P), E, chunk_hist, s) != cudaSuccess)
+      return MOE_ERR_CUDA;
+    ap.chunk_hist = chunk_hist;
+  }
   if (launch_align(ap, s) != cudaSuccess) return MOE_ERR_CUDA;
   if (events && cudaEventRecord(events[2], stream) != cudaSuccess) return MOE_ERR_CUDA;
   // 3. gather (+ quantise) the routed rows of x; zero the combine buffer
-  if (launch_gather_x(static_cast<const __nv_bfloat16*>(a->x), H, sorted, ctrl, static_cast<int>(P),
-                      k, xs, fp8, acc, acc_elems, L.pad_max, dev.num_sms,
+  uint8_t* xq_tok = (L.large && fp8) ? ws + L.xq_tok : nullptr;
+  if (xq_tok && launch_quant_tokens(static_cast<const __nv_bfloat16*>(a->x),
+                                    static_cast<long long>(T) * H, ctrl, xq_tok, dev.num_sms,
+                                    s) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  if (launch_gather_x(static_cast<const __nv_bfloat16*>(a->x), xq_tok, H, sorted, ctrl,
+                      static_cast<int>(P), k, xs, fp8, acc, acc_elems, L.pad_max, dev.num_sms,
                       s) != cudaSuccess)
     return MOE_ERR_CUDA;
 

@@ -227,9 +227,23 @@ __global__ void __launch_bounds__(kAlignThreads) align_kernel(AlignParams p) {
   for (int i = tid; i < 32 * E; i += kAlignThreads) seg[i] = 0;
   __syncthreads();
 
+  if (p.chunk_hist != nullptr) {
+    // totals and the pairs before this chunk from the per-chunk histograms
+    for (int e = tid; e < E; e += kAlignThreads) {
+      int tot = 0, bef = 0;
+#pragma unroll 8
+      for (int b = 0; b < static_cast<int>(gridDim.x); ++b) {
+        const int v = p.chunk_hist[static_cast<size_t>(b) * E + e];
+        tot += v;
+        bef += b < static_cast<int>(blockIdx.x) ? v : 0;
+      }
+      hist_all[e] = tot;
+      hist_before[e] = bef;
+    }
+  }
   // histograms of every pair, and of the pairs before this chunk (loads of
   // kAlignUnroll rounds issued together: this pass is latency bound)
-  for (int p0 = 0; p0 < P; p0 += kAlignThreads * kAlignUnroll) {
+  for (int p0 = 0; p.chunk_hist == nullptr && p0 < P; p0 += kAlignThreads * kAlignUnroll) {
     int ev[kAlignUnroll];
 #pragma unroll
     for (int u = 0; u < kAlignUnroll; ++u) {
@@ -345,14 +359,64 @@ __global__ void __launch_bounds__(kAlignThreads) align_kernel(AlignParams p) {
   }
 }
 
+// First pass of the two-pass alignment for large batches: each CTA counts the
+// experts of its own chunk of pairs only.
+__global__ void __launch_bounds__(kAlignThreads)
+    align_hist_kernel(const int32_t* __restrict__ ids, int P, int E, int chunk,
+                      int32_t* __restrict__ hist) {
+  extern __shared__ int s_hist[];
+  const int tid = threadIdx.x, lane = tid & 31;
+  pdl_wait();
+  pdl_trigger();
+  for (int e = tid; e < E; e += kAlignThreads) s_hist[e] = 0;
+  __syncthreads();
+  const int cs = blockIdx.x * chunk;
+  const int ce = min(cs + chunk, P);
+  for (int q0 = cs; q0 < ce; q0 += kAlignThreads * kAlignUnroll) {
+    int ev[kAlignUnroll];
+#pragma unroll
+    for (int u = 0; u < kAlignUnroll; ++u) {
+      const int q = q0 + u * kAlignThreads + tid;
+      ev[u] = q < ce ? __ldg(ids + q) : -1;
+    }
+#pragma unroll
+    for (int u = 0; u < kAlignUnroll; ++u) {
+      const int e = ev[u];
+      const bool valid = static_cast<unsigned>(e) < static_cast<unsigned>(E);
+      const unsigned mask = __match_any_sync(kFull, valid ? e : -1);
+      if (valid && lane == __ffs(mask) - 1) atomicAdd(&s_hist[e], __popc(mask));
+    }
+  }
+  __syncthreads();
+  for (int e = tid; e < E; e += kAlignThreads) hist[static_cast<size_t>(blockIdx.x) * E + e] = s_hist[e];
+}
+
+// x -> E4M3 codes in token order, 16 elements per thread.
+__global__ void __launch_bounds__(256)
+    quant_tokens_kernel(const __nv_bfloat16* __restrict__ x, long long n16, const Ctrl* ctrl,
+                        uint8_t* __restrict__ xq) {
+  pdl_wait();
+  pdl_trigger();
+  const float s = ctrl->s_x;
+  const uint4* src = reinterpret_cast<const uint4*>(x);
+  uint4* dst = reinterpret_cast<uint4*>(xq);
+  for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < n16;
+       i += static_cast<long long>(gridDim.x) * blockDim.x) {
+    const uint2 a = quant8(__ldg(src + 2 * i), s);
+    const uint2 b = quant8(__ldg(src + 2 * i + 1), s);
+    dst[i] = make_uint4(a.x, a.y, b.x, b.y);
+  }
+}
+
 // ------------------------------------------------------------------ gather
 // One thread per 16 elements of an aligned row: the pair's token row of x,
 // quantised to E4M3 with s_x (or copied as bf16); padding rows are zero.  The
 // same grid zeroes the fp32 combine buffer.
 __global__ void __launch_bounds__(256)
-    gather_x_kernel(const __nv_bfloat16* __restrict__ x, int H, const int32_t* __restrict__ sorted_ids,
-                    const Ctrl* __restrict__ ctrl, int P, int k, void* __restrict__ xs, int fp8,
-                    float* __restrict__ acc, long long acc_elems) {
+    gather_x_kernel(const __nv_bfloat16* __restrict__ x, const uint8_t* __restrict__ xq_tok, int H,
+                    const int32_t* __restrict__ sorted_ids, const Ctrl* __restrict__ ctrl, int P,
+                    int k, void* __restrict__ xs, int fp8, float* __restrict__ acc,
+                    long long acc_elems) {
   pdl_wait();
   pdl_trigger();
   const long long rows = ctrl->num_padded;
@@ -360,7 +424,17 @@ __global__ void __launch_bounds__(256)
   const long long n = rows * per_row;
   const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
   const long long tid = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
-  if (fp8) {
+  if (fp8 && xq_tok != nullptr) {
+    // codes already made per token: copy 16 bytes
+    uint4* dst = static_cast<uint4*>(xs);
+    const uint4* codes = reinterpret_cast<const uint4*>(xq_tok);
+    for (long long i = tid; i < n; i += stride) {
+      const long long r = i / per_row;
+      const int c = static_cast<int>(i - r * per_row);
+      const int q = sorted_ids[r];
+      dst[i] = q < P ? codes[static_cast<size_t>(q / k) * per_row + c] : make_uint4(0, 0, 0, 0);
+    }
+  } else if (fp8) {
     const float s = ctrl->s_x;
     uint4* dst = static_cast<uint4*>(xs);
     for (long long i = tid; i < n; i += stride) {
@@ -572,13 +646,26 @@ cudaError_t launch_align(const AlignParams& p, cudaStream_t st) {
   return launch_pdl(align_kernel, dim3(grid), dim3(kAlignThreads), smem, st, p);
 }
 
-cudaError_t launch_gather_x(const __nv_bfloat16* x, int H, const int32_t* sorted_ids,
-                            const Ctrl* ctrl, int P, int k, void* xs, bool fp8, float* acc,
-                            long long acc_elems, int max_rows, int num_sms, cudaStream_t st) {
+cudaError_t launch_gather_x(const __nv_bfloat16* x, const uint8_t* xq_tok, int H,
+                            const int32_t* sorted_ids, const Ctrl* ctrl, int P, int k, void* xs,
+                            bool fp8, float* acc, long long acc_elems, int max_rows, int num_sms,
+                            cudaStream_t st) {
   const long long work = std::max(static_cast<long long>(max_rows) * (H / 16), acc_elems / 4);
   const int grid = capped_grid(work, 256, num_sms, 8);
-  return launch_pdl(gather_x_kernel, dim3(grid), dim3(256), 0, st, x, H, sorted_ids, ctrl, P, k,
-                    xs, fp8 ? 1 : 0, acc, acc_elems);
+  return launch_pdl(gather_x_kernel, dim3(grid), dim3(256), 0, st, x, xq_tok, H, sorted_ids, ctrl,
+                    P, k, xs, fp8 ? 1 : 0, acc, acc_elems);
+}
+
+cudaError_t launch_align_hist(const int32_t* ids, int P, int E, int32_t* hist, cudaStream_t st) {
+  const int grid = (P + kAlignChunk - 1) / kAlignChunk;
+  return launch_pdl(align_hist_kernel, dim3(grid), dim3(kAlignThreads), E * sizeof(int), st, ids,
+                    P, E, kAlignChunk, hist);
+}
+
+cudaError_t launch_quant_tokens(const __nv_bfloat16* x, long long n, const Ctrl* ctrl,
+                                uint8_t* xq, int num_sms, cudaStream_t st) {
+  const int grid = capped_grid(n / 16, 256, num_sms, 8);
+  return launch_pdl(quant_tokens_kernel, dim3(grid), dim3(256), 0, st, x, n / 16, ctrl, xq);
 }
 
 cudaError_t launch_quant_h(const float* h, int I, Ctrl* ctrl, uint8_t* hq, int max_rows,

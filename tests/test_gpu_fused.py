@@ -62,6 +62,16 @@ def test_fused_small(gpu_lib, T, H, I, E, k, renorm, dtype):
     run_case(gpu_lib, w, a, k, renorm, repeat=2)
 
 
+@pytest.mark.parametrize("T,H,I,E,k", [
+    (2600, 256, 128, 16, 2),    # > 4096 pairs: two-pass alignment, tokens quantised once
+    (2048, 1024, 128, 32, 8),   # pairs x H > 8M: combine through per-pair rows
+])
+def test_fused_large_batch_paths(gpu_lib, T, H, I, E, k):
+    w = inputs.make_weights(H, I, E, "fp8", seed=T)
+    a = inputs.make_activations(T, H, E, "zipf", seed=T)
+    run_case(gpu_lib, w, a, k, True, rows=sample_rows(T, 64, seed=3))
+
+
 def test_fused_zipf_skew(gpu_lib):
     T, H, I, E, k = 300, 256, 256, 64, 8
     w = inputs.make_weights(H, I, E, "fp8", seed=5)
