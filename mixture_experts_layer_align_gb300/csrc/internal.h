@@ -89,6 +89,29 @@ struct AlignParams {
 };
 cudaError_t launch_align(const AlignParams& p, cudaStream_t st);
 int align_chunk();
+// Router + alignment in one CTA for small batches (decode).  Used when
+// T*k <= kSmallMaxPairs, E <= kSmallMaxExperts and T*H <= kSmallMaxXElems.
+constexpr int kSmallMaxPairs = 2048;
+constexpr int kSmallMaxExperts = 256;
+constexpr long long kSmallMaxXElems = 1ll << 19;
+struct SmallFrontParams {
+  const float* logits;
+  int T, E, k, renorm;
+  int32_t* ids;
+  float* wts;
+  const __nv_bfloat16* x;  // null: no activation scale (bf16 path)
+  int H;
+  Ctrl* ctrl;
+  int* zero_ints;
+  int n_zero;
+  int32_t* counts;
+  int32_t* offsets;
+  int32_t* sorted_ids;
+  int4* mtiles;
+  int bn_max;
+};
+cudaError_t launch_route_align_small(const SmallFrontParams& p, cudaStream_t st);
+
 // First pass of the two-pass alignment: expert histogram of each chunk of
 // align_chunk() pairs into hist[chunk][E].
 cudaError_t launch_align_hist(const int32_t* ids, int P, int E, int32_t* hist, cudaStream_t st);

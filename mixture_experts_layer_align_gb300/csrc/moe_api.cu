@@ -343,9 +343,36 @@ moe_status_t fused_forward_impl(const moe_fused_args* a, void* workspace, size_t
   int* tile_cnt = reinterpret_cast<int*>(ws + L.tile_cnt);
   float* part = reinterpret_cast<float*>(ws + L.part);
 
-  // 1. routing (+ per-CTA amax of x, + reset of the control words)
   cudaStream_t s = stream;
   if (events && cudaEventRecord(events[0], stream) != cudaSuccess) return MOE_ERR_CUDA;
+  const bool small = P <= kSmallMaxPairs && E <= kSmallMaxExperts &&
+                     static_cast<long long>(T) * H <= kSmallMaxXElems;
+  if (small) {
+    // 1-2 in one CTA: routing, amax of x, alignment, tile list, s_x
+    SmallFrontParams sp{};
+    sp.logits = a->router_logits;
+    sp.T = T;
+    sp.E = E;
+    sp.k = k;
+    sp.renorm = a->renormalize;
+    sp.ids = ids;
+    sp.wts = wts;
+    sp.x = fp8 ? static_cast<const __nv_bfloat16*>(a->x) : nullptr;
+    sp.H = H;
+    sp.ctrl = ctrl;
+    sp.zero_ints = tile_cnt;
+    sp.n_zero = L.n_tile_cnt;
+    sp.counts = counts;
+    sp.offsets = offsets;
+    sp.sorted_ids = sorted;
+    sp.mtiles = mtiles;
+    sp.bn_max = bn_max;
+    if (launch_route_align_small(sp, s) != cudaSuccess) return MOE_ERR_CUDA;
+    if (events && (cudaEventRecord(events[1], stream) != cudaSuccess ||
+                   cudaEventRecord(events[2], stream) != cudaSuccess))
+      return MOE_ERR_CUDA;
+  } else {
+  // 1. routing (+ per-CTA amax of x, + reset of the control words)
   if (launch_route_topk(a->router_logits, T, E, k, a->renormalize, ids, wts,
                         static_cast<const __nv_bfloat16*>(a->x), H, fp8 ? partials : nullptr, ctrl,
                         tile_cnt, L.n_tile_cnt, s) != cudaSuccess)
@@ -376,6 +403,7 @@ moe_status_t fused_forward_impl(const moe_fused_args* a, void* workspace, size_t
   }
   if (launch_align(ap, s) != cudaSuccess) return MOE_ERR_CUDA;
   if (events && cudaEventRecord(events[2], stream) != cudaSuccess) return MOE_ERR_CUDA;
+  }
   // 3. gather (+ quantise) the routed rows of x; zero the combine buffer
   uint8_t* xq_tok = (L.large && fp8) ? ws + L.xq_tok : nullptr;
   if (xq_tok && launch_quant_tokens(static_cast<const __nv_bfloat16*>(a->x),

@@ -92,11 +92,64 @@ __device__ int block_exclusive_scan_1024(int v, int* tmp, int* total) {
 }
 
 // ------------------------------------------------------------------ router
-// One warp per token.  The row of logits is staged in shared memory; each of
-// the k rounds is a warp arg-max under (logit desc, index asc) over the
-// experts not taken yet (one bit per lane per 32 experts).  The softmax uses
-// expf on max-subtracted logits.  Optionally also the per-CTA amax of x, the
-// first half of the dynamic activation scale.
+// One warp per token.  The row of logits is staged in shared memory (`l`, E
+// floats of this warp); each of the k rounds is a warp arg-max under (logit
+// desc, index asc) over the experts not taken yet (one bit per lane per 32
+// experts).  The softmax uses expf on max-subtracted logits.  Writes the k
+// ids and weights of the token (id_row / w_row may be shared or global).
+__device__ void route_token(const float* __restrict__ src, int E, int k, int renorm, float* l,
+                            int32_t* id_row, float* w_row, int lane) {
+  float m = -INFINITY;
+  for (int e = lane; e < E; e += 32) {
+    const float v = src[e];
+    l[e] = v;
+    m = fmaxf(m, v);
+  }
+  m = warp_max(m);
+  float z = 0.f;
+  for (int e = lane; e < E; e += 32) z += expf(l[e] - m);
+  z = warp_sum(z);
+  __syncwarp();
+
+  uint32_t taken = 0u;  // bit i <=> expert lane + 32 i already selected
+  float sel = 0.f;
+  for (int j = 0; j < k; ++j) {
+    float bv = -INFINITY;
+    int bi = 0x7fffffff;  // "none"
+    for (int e = lane, i = 0; e < E; e += 32, ++i) {
+      if ((taken >> i) & 1u) continue;
+      const float v = l[e];
+      if (bi == 0x7fffffff || v > bv) {  // ascending scan: equal values keep the lower index
+        bv = v;
+        bi = e;
+      }
+    }
+#pragma unroll
+    for (int o = 16; o; o >>= 1) {
+      const float ov = __shfl_xor_sync(kFull, bv, o);
+      const int oi = __shfl_xor_sync(kFull, bi, o);
+      const bool take = oi != 0x7fffffff && (bi == 0x7fffffff || ov > bv || (ov == bv && oi < bi));
+      if (take) {
+        bv = ov;
+        bi = oi;
+      }
+    }
+    if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
+    const float ex = expf(bv - m);
+    sel += ex;
+    if (lane == 0) {
+      id_row[j] = bi;
+      w_row[j] = ex;
+    }
+  }
+  __syncwarp();
+  const float denom = renorm ? sel : z;
+  for (int j = lane; j < k; j += 32) w_row[j] = __fdiv_rn(w_row[j], denom);
+  __syncwarp();
+}
+
+// Router kernel: one warp per token, plus the per-CTA amax of x (the first
+// half of the dynamic activation scale) and the per-call resets.
 __global__ void __launch_bounds__(kRouteWarps * 32)
     route_topk_kernel(const float* __restrict__ logits, int T, int E, int k, int renorm,
                       int32_t* __restrict__ ids, float* __restrict__ wts,
@@ -116,58 +169,9 @@ __global__ void __launch_bounds__(kRouteWarps * 32)
   const int t = blockIdx.x * kRouteWarps + warp;
   float xmax = 0.f;
   if (t < T) {
-    float* l = s_logits + static_cast<size_t>(warp) * E;
-    const float* src = logits + static_cast<size_t>(t) * E;
-    float m = -INFINITY;
-    for (int e = lane; e < E; e += 32) {
-      const float v = src[e];
-      l[e] = v;
-      m = fmaxf(m, v);
-    }
-    m = warp_max(m);
-    float z = 0.f;
-    for (int e = lane; e < E; e += 32) z += expf(l[e] - m);
-    z = warp_sum(z);
-    __syncwarp();
-
-    uint32_t taken = 0u;  // bit i <=> expert lane + 32 i already selected
-    float sel = 0.f;
-    int32_t* id_row = ids + static_cast<size_t>(t) * k;
-    float* w_row = wts + static_cast<size_t>(t) * k;
-    for (int j = 0; j < k; ++j) {
-      float bv = -INFINITY;
-      int bi = 0x7fffffff;  // "none"
-      for (int e = lane, i = 0; e < E; e += 32, ++i) {
-        if ((taken >> i) & 1u) continue;
-        const float v = l[e];
-        if (bi == 0x7fffffff || v > bv) {  // ascending scan: equal values keep the lower index
-          bv = v;
-          bi = e;
-        }
-      }
-#pragma unroll
-      for (int o = 16; o; o >>= 1) {
-        const float ov = __shfl_xor_sync(kFull, bv, o);
-        const int oi = __shfl_xor_sync(kFull, bi, o);
-        const bool take =
-            oi != 0x7fffffff && (bi == 0x7fffffff || ov > bv || (ov == bv && oi < bi));
-        if (take) {
-          bv = ov;
-          bi = oi;
-        }
-      }
-      if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
-      const float ex = expf(bv - m);
-      sel += ex;
-      if (lane == 0) {
-        id_row[j] = bi;
-        w_row[j] = ex;
-      }
-    }
-    __syncwarp();
-    const float denom = renorm ? sel : z;
-    for (int j = lane; j < k; j += 32) w_row[j] = __fdiv_rn(w_row[j], denom);
-
+    route_token(logits + static_cast<size_t>(t) * E, E, k, renorm,
+                s_logits + static_cast<size_t>(warp) * E, ids + static_cast<size_t>(t) * k,
+                wts + static_cast<size_t>(t) * k, lane);
     if (x != nullptr) {
       const uint4* xr = reinterpret_cast<const uint4*>(x + static_cast<size_t>(t) * H);
       for (int i = lane; i < H / 8; i += 32) xmax = absmax8(__ldg(xr + i), xmax);
@@ -356,6 +360,129 @@ __global__ void __launch_bounds__(kAlignThreads) align_kernel(AlignParams p) {
       p.ctrl->s_x = p.amax_partials ? scale_from_amax(a) : 1.f;
       p.ctrl->num_mtiles = n_tiles;
     }
+  }
+}
+
+// Writes the GEMM row-tile list from the per-expert padded segments (one
+// expert per thread, tid < E; all 1024 threads of the block must call).
+// Each expert's segment is split into ceil(padded / bn_max) equal tiles
+// (multiples of bm); every entry also carries the expert's tile count and the
+// index of its first tile.  Returns the number of tiles.
+__device__ int write_mtiles(int tid, int E, int padded, int seg_off, int bm, int bn_max,
+                            int4* __restrict__ mtiles, int* s_tmp) {
+  const int nt = (tid < E && padded > 0) ? (padded + bn_max - 1) / bn_max : 0;
+  int n_tiles = 0;
+  const int first = block_exclusive_scan_1024(nt, s_tmp, &n_tiles);
+  if (nt > 0) {
+    const int per = ((padded + nt - 1) / nt + bm - 1) / bm * bm;
+    for (int j = 0; j < nt; ++j) {
+      const int rows = min(per, padded - j * per);
+      mtiles[first + j] = make_int4(tid, seg_off + j * per, rows | (nt << 12), first);
+    }
+  }
+  return n_tiles;
+}
+
+// Small batches (decode): one CTA routes every token, takes amax |x|, aligns
+// the pairs and writes the GEMM tile list, with everything in shared memory
+// between the steps: the router and alignment kernels in one launch and
+// without their global-memory round trips.
+__global__ void __launch_bounds__(kAlignThreads, 1) route_align_small_kernel(SmallFrontParams p) {
+  extern __shared__ int s_small[];
+  __shared__ int s_tmp[32];
+  __shared__ float s_red[32];
+  const int E = p.E, k = p.k, T = p.T;
+  const int P = T * k;
+  float* s_logits = reinterpret_cast<float*>(s_small);  // [32][E]
+  int32_t* s_ids = s_small + 32 * E;                     // [P]
+  float* s_w = reinterpret_cast<float*>(s_ids + P);      // [P]
+  int* s_cnt = reinterpret_cast<int*>(s_w + P);          // [E]
+  int* s_run = s_cnt + E;                                // [E]
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  Ctrl* ctrl = p.ctrl;
+  pdl_wait();
+  pdl_trigger();
+  if (tid == 0) {
+    ctrl->err = 0;
+    ctrl->amax_h = 0u;
+  }
+  for (int i = tid; i < p.n_zero; i += kAlignThreads) p.zero_ints[i] = 0;
+  for (int e = tid; e < E; e += kAlignThreads) s_cnt[e] = 0;
+
+  // routing, one warp per token
+  for (int t = warp; t < T; t += 32)
+    route_token(p.logits + static_cast<size_t>(t) * E, E, k, p.renorm, s_logits + warp * E,
+                s_ids + t * k, s_w + t * k, lane);
+  // amax |x| (FP8), 8 vector loads in flight per thread
+  float xmax = 0.f;
+  if (p.x != nullptr) {
+    const uint4* xv = reinterpret_cast<const uint4*>(p.x);
+    const long long n8 = static_cast<long long>(T) * p.H / 8;
+    for (long long i0 = 0; i0 < n8; i0 += 8 * kAlignThreads) {
+      uint4 v[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const long long i = i0 + u * kAlignThreads + tid;
+        v[u] = i < n8 ? __ldg(xv + i) : make_uint4(0, 0, 0, 0);
+      }
+#pragma unroll
+      for (int u = 0; u < 8; ++u) xmax = absmax8(v[u], xmax);
+    }
+  }
+  xmax = warp_max(xmax);
+  if (lane == 0) s_red[warp] = xmax;
+  __syncthreads();
+
+  // counts and padded offsets
+  for (int q0 = 0; q0 < P; q0 += kAlignThreads) {
+    const int q = q0 + tid;
+    const int e = q < P ? s_ids[q] : -1;
+    const bool valid = q < P && static_cast<unsigned>(e) < static_cast<unsigned>(E);
+    const unsigned mask = __match_any_sync(kFull, valid ? e : -1);
+    if (valid && lane == __ffs(mask) - 1) atomicAdd(&s_cnt[e], __popc(mask));
+  }
+  __syncthreads();
+  const int c = tid < E ? s_cnt[tid] : 0;
+  const int padded = (c + kAlignBlock - 1) / kAlignBlock * kAlignBlock;
+  int total = 0;
+  const int off = block_exclusive_scan_1024(padded, s_tmp, &total);
+  if (tid < E) s_run[tid] = off;
+  __syncthreads();
+  // stable placement in pair-id order (one warp), padding sentinels
+  if (warp == 0) {
+    for (int q0 = 0; q0 < P; q0 += 32) {
+      const int q = q0 + lane;
+      const int e = q < P ? s_ids[q] : -1;
+      const bool valid = q < P && static_cast<unsigned>(e) < static_cast<unsigned>(E);
+      const unsigned mask = __match_any_sync(kFull, valid ? e : -1);
+      const int leader = __ffs(mask) - 1;
+      int slot = 0;
+      if (valid && lane == leader) {
+        slot = s_run[e];
+        s_run[e] = slot + __popc(mask);
+      }
+      slot = __shfl_sync(kFull, slot, leader);
+      if (valid) p.sorted_ids[slot + __popc(mask & ((1u << lane) - 1u))] = q;
+      __syncwarp();
+    }
+  }
+  if (tid < E) {
+    for (int i = c; i < padded; ++i) p.sorted_ids[off + i] = P;
+    p.counts[tid] = c;
+    p.offsets[tid] = off;
+  }
+  for (int q = tid; q < P; q += kAlignThreads) {
+    p.ids[q] = s_ids[q];
+    p.wts[q] = s_w[q];
+  }
+  const int n_tiles = write_mtiles(tid, E, padded, off, kAlignBlock, p.bn_max, p.mtiles, s_tmp);
+  if (tid == 0) {
+    float a = 0.f;
+    for (int w = 0; w < 32; ++w) a = fmaxf(a, s_red[w]);
+    p.offsets[E] = total;
+    ctrl->num_padded = total;
+    ctrl->num_mtiles = n_tiles;
+    ctrl->s_x = p.x != nullptr ? scale_from_amax(a) : 1.f;
   }
 }
 
@@ -654,6 +781,25 @@ cudaError_t launch_gather_x(const __nv_bfloat16* x, const uint8_t* xq_tok, int H
   const int grid = capped_grid(work, 256, num_sms, 8);
   return launch_pdl(gather_x_kernel, dim3(grid), dim3(256), 0, st, x, xq_tok, H, sorted_ids, ctrl,
                     P, k, xs, fp8 ? 1 : 0, acc, acc_elems);
+}
+
+cudaError_t launch_route_align_small(const SmallFrontParams& p, cudaStream_t st) {
+  const size_t smem =
+      (static_cast<size_t>(32) * p.E + 2 * static_cast<size_t>(p.T) * p.k + 2 * p.E) * sizeof(int);
+  static thread_local int configured_device = -1;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (configured_device != dev) {
+    const int max_smem =
+        (32 * kSmallMaxExperts + 2 * kSmallMaxPairs + 2 * kSmallMaxExperts) * sizeof(int);
+    cudaError_t e = checked(cudaFuncSetAttribute(route_align_small_kernel,
+                                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                 max_smem),
+                            "smem attribute");
+    if (e != cudaSuccess) return e;
+    configured_device = dev;
+  }
+  return launch_pdl(route_align_small_kernel, dim3(1), dim3(kAlignThreads), smem, st, p);
 }
 
 cudaError_t launch_align_hist(const int32_t* ids, int P, int E, int32_t* hist, cudaStream_t st) {
