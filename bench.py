@@ -77,9 +77,10 @@ def kernel_source_hash():
     return h.hexdigest()[:16]
 
 
-def recorded_traffic(workload):
-    """DRAM bytes per launch of the dominant kernel from the committed ncu
-    summary, if it was taken on the current kernel source (else None)."""
+def recorded_traffic(workload, Ts):
+    """DRAM bytes per launch of the gate/up GEMM from the committed ncu summary,
+    averaged over the T values of one step (one launch each), if it was taken
+    on the current kernel source (else None)."""
     p = os.path.join(ROOT, "profiles", f"gemm1_swiglu_{workload}_traffic.txt")
     if not os.path.exists(p):
         return None
@@ -92,7 +93,7 @@ def recorded_traffic(workload):
     if kv.get("kernel_source_hash") != kernel_source_hash():
         return None
     try:
-        return float(kv["dram_bytes_per_launch"])
+        return sum(float(kv[f"dram_bytes_T{T}"]) for T in Ts) / len(Ts)
     except (KeyError, ValueError):
         return None
 
@@ -284,7 +285,7 @@ def run_ours(args, rank, local_rank, world):
             layer_bytes=touched * 3 * H * I * esize + 8 * E + T * E * 4 + 2 * T * H * 2)
 
     calls_per_step = len(Ts)
-    launches_per_call = 7 if fp8 else 6
+    launches_per_step = sum(moe.moe_fused_launch_count(T, H, I, E, k, dtype) for T in Ts)
 
     def one_step(step_idx, events=None):
         for j, T in enumerate(Ts):
@@ -369,7 +370,7 @@ def run_ours(args, rank, local_rank, world):
         dom_bytes = sum(stats[T]["gemm1_bytes"] for T in Ts) * K
         dom_ms = sum(sum(gemm1_ms[T]) for T in Ts)
     achieved = dom_bytes / (dom_ms * 1e-3) / 1e9
-    traffic = recorded_traffic(args.workload) if dominant == "gemm1_swiglu" else None
+    traffic = recorded_traffic(args.workload, Ts) if dominant == "gemm1_swiglu" else None
 
     tokens_per_step = sum(Ts)
     value = world * tokens_per_step * K / (elapsed_ms * 1e-3)
@@ -466,7 +467,7 @@ def run_ours(args, rank, local_rank, world):
                      "algorithmic_bytes": "touched experts' weight bytes + routed activation "
                                           "rows in + h out, per launch"},
         "clocks": clocks,
-        "gpu_launches": K * calls_per_step * launches_per_call,
+        "gpu_launches": K * launches_per_step,
         "e2e": e2e,
         "cpu_baseline": cpu,
     }

@@ -163,6 +163,11 @@ size_t moe_fused_trace_offset(int T, int H, int I, int E, int top_k, moe_dtype_t
 /* Workspace bytes moe_fused_forward needs for these sizes (0 if invalid). */
 size_t moe_fused_workspace_size(int T, int H, int I, int E, int top_k, moe_dtype_t dtype);
 
+/* Number of kernels one moe_fused_forward call with these sizes launches on
+ * its stream (0 for T = 0, -1 if the sizes are invalid or unsupported).  Host
+ * only: no CUDA call. */
+int moe_fused_launch_count(int T, int H, int I, int E, int top_k, moe_dtype_t dtype);
+
 /*
  * Fused MoE layer forward: routing -> alignment by expert -> grouped gate/up
  * GEMM with the SiLU*up epilogue -> grouped down GEMM with the top-k weighted

@@ -84,6 +84,8 @@ def load():
         L.moe_fused_trace_offset.restype = sz
         L.moe_fused_workspace_size.argtypes = [i, i, i, i, i, i]
         L.moe_fused_workspace_size.restype = sz
+        L.moe_fused_launch_count.argtypes = [i, i, i, i, i, i]
+        L.moe_fused_launch_count.restype = i
         L.moe_fused_forward.argtypes = [ctypes.POINTER(MoeFusedArgs), P, sz, P]
         L.moe_fused_forward_timed.argtypes = [ctypes.POINTER(MoeFusedArgs), P, sz, P,
                                                ctypes.POINTER(ctypes.c_void_p), i]
@@ -207,6 +209,11 @@ def moe_fused_workspace_size(T: int, H: int, I: int, E: int, top_k: int, dtype: 
     return int(load().moe_fused_workspace_size(T, H, I, E, top_k, dtype))
 
 
+def moe_fused_launch_count(T: int, H: int, I: int, E: int, top_k: int, dtype: int) -> int:
+    """Kernels one moe_fused_forward call launches (-1: invalid sizes)."""
+    return int(load().moe_fused_launch_count(T, H, I, E, top_k, dtype))
+
+
 def alloc_workspace(T, H, I, E, top_k, dtype, device="cuda"):
     import torch
     n = moe_fused_workspace_size(T, H, I, E, top_k, dtype)
@@ -309,6 +316,6 @@ def moe_check_status(workspace, stream=None) -> int:
 
 
 __all__ = ["load", "moe_route_topk", "moe_align_by_expert", "moe_quantize_e4m3",
-           "moe_fused_workspace_size", "moe_fused_forward", "moe_check_status", "alloc_workspace",
+           "moe_fused_workspace_size", "moe_fused_launch_count", "moe_fused_forward", "moe_check_status", "alloc_workspace",
            "status_string", "MoeError", "make_step_events", "MoeFusedArgs", "MOE_DT_BF16", "MOE_DT_FP8_E4M3",
            "MOE_DEBUG_FORCE_TIMEOUT", "LIB_PATH"]

@@ -291,6 +291,13 @@ size_t moe_fused_workspace_size(int T, int H, int I, int E, int top_k, moe_dtype
 
 namespace {
 
+// Small batches take the single-CTA router + alignment kernel.
+bool small_front(int T, int H, int E, int k) {
+  const long long P = static_cast<long long>(T) * k;
+  return P <= kSmallMaxPairs && E <= kSmallMaxExperts &&
+         static_cast<long long>(T) * H <= kSmallMaxXElems;
+}
+
 // The launch sequence.  When `events` is non-null, events[i] is recorded on
 // the stream before step i (i = 0..6) and events[7] after the last step.
 moe_status_t fused_forward_impl(const moe_fused_args* a, void* workspace, size_t workspace_bytes,
@@ -345,9 +352,7 @@ moe_status_t fused_forward_impl(const moe_fused_args* a, void* workspace, size_t
 
   cudaStream_t s = stream;
   if (events && cudaEventRecord(events[0], stream) != cudaSuccess) return MOE_ERR_CUDA;
-  const bool small = P <= kSmallMaxPairs && E <= kSmallMaxExperts &&
-                     static_cast<long long>(T) * H <= kSmallMaxXElems;
-  if (small) {
+  if (small_front(T, H, E, k)) {
     // 1-2 in one CTA: routing, amax of x, alignment, tile list, s_x
     SmallFrontParams sp{};
     sp.logits = a->router_logits;
@@ -527,6 +532,27 @@ moe_status_t moe_fused_forward(const moe_fused_args* a, void* workspace, size_t 
 size_t moe_fused_trace_offset(int T, int H, int I, int E, int top_k, moe_dtype_t dtype) {
   if (moe_fused_workspace_size(T, H, I, E, top_k, dtype) == 0) return 0;
   return make_layout(T, H, I, E, top_k, dtype == MOE_DT_FP8_E4M3).trace;
+}
+
+int moe_fused_launch_count(int T, int H, int I, int E, int top_k, moe_dtype_t dtype) {
+  if (moe_fused_workspace_size(T, H, I, E, top_k, dtype) == 0) return -1;
+  if (H % 128 != 0 || I % 128 != 0) return -1;
+  if (T == 0) return 0;
+  const bool fp8 = dtype == MOE_DT_FP8_E4M3;
+  const Layout L = make_layout(T, H, I, E, top_k, fp8);
+  int n = 0;
+  if (small_front(T, H, E, top_k)) {
+    n += 1;                          // router + alignment
+  } else {
+    n += 2 + (L.large ? 1 : 0);      // router, (chunk histograms), alignment
+    n += (L.large && fp8) ? 1 : 0;   // per-token quantisation of x
+  }
+  n += 1;                            // gather of x
+  n += 1;                            // gate/up GEMM
+  n += fp8 ? 1 : 0;                  // quantisation of h
+  n += 1;                            // down GEMM
+  n += 1;                            // finalize or row combine
+  return n;
 }
 
 moe_status_t moe_fused_forward_timed(const moe_fused_args* a, void* workspace,

@@ -54,6 +54,20 @@ def test_workspace_size_grows_with_tokens(lib):
     assert moe.moe_fused_workspace_size(1, 128, 128, 2000, 2, moe.MOE_DT_FP8_E4M3) == 0
 
 
+def test_launch_count(lib):
+    fp8, bf16 = moe.MOE_DT_FP8_E4M3, moe.MOE_DT_BF16
+    # decode: one front kernel, gather, GEMM, quant h, GEMM, finalize
+    assert moe.moe_fused_launch_count(64, 4096, 14336, 8, 2, fp8) == 6
+    assert moe.moe_fused_launch_count(4, 128, 256, 8, 2, bf16) == 5   # no quant of h
+    # 512 x 8 pairs: separate router and alignment kernels
+    assert moe.moe_fused_launch_count(512, 2048, 768, 128, 8, fp8) == 7
+    # > 4096 pairs: chunk histograms and per-token quantisation of x as well
+    assert moe.moe_fused_launch_count(8192, 2048, 768, 128, 8, fp8) == 9
+    assert moe.moe_fused_launch_count(0, 2048, 768, 128, 8, fp8) == 0
+    assert moe.moe_fused_launch_count(4, 100, 256, 8, 2, fp8) == -1
+    assert moe.moe_fused_launch_count(4, 128, 256, 8, 9, fp8) == -1
+
+
 def _args(**kw):
     base = dict(x=16, router_logits=16, w13=16, w2=16, w13_scale=16, w2_scale=16,
                 weight_dtype=1, T=4, H=128, I=256, E=8, top_k=2, renormalize=1, out=16,
