@@ -40,6 +40,8 @@ METRIC = "fused-MoE layer tokens/s & µs/call; % of HBM BW (decode) or FP8 TC pe
 STEP_NAMES = ["route", "align", "gather_quant_x", "gemm1_swiglu", "quant_h", "gemm2_combine",
               "finalize"]
 FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+FP8_OVER_BF16 = 2.0  # nominal dense FP8 / bf16 tensor rate
 
 
 def parse():
@@ -52,6 +54,10 @@ def parse():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--shape-sweep", action="store_true",
+                    help="first-call vs steady-state time for every T in 1..--max-tokens "
+                         "in one process, plus CUDA-graph capture per T bucket")
+    ap.add_argument("--max-tokens", type=int, default=8192)
     return ap.parse_args()
 
 
@@ -61,12 +67,14 @@ def dist_env():
 
 
 def measured_peaks():
+    """(HBM GB/s, bf16 dense TFLOP/s burst, 'measured' | 'fallback')."""
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
         with open(p) as f:
             d = json.load(f)
-        return float(d.get("hbm_gbs", FALLBACK_HBM_GBS)), "measured"
-    return FALLBACK_HBM_GBS, "fallback"
+        return (float(d.get("hbm_gbs", FALLBACK_HBM_GBS)),
+                float(d.get("bf16_tflops", FALLBACK_BF16_TFLOPS)), "measured")
+    return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, "fallback"
 
 
 def kernel_source_hash():
@@ -282,6 +290,7 @@ def run_ours(args, rank, local_rank, world):
             touched=touched, max_rows=int(c.max()),
             gemm1_bytes=touched * 2 * I * H * esize + P * H * esize + P * I * (4 if fp8 else 2),
             gemm2_bytes=touched * H * I * esize + P * I * esize + P * H * 4,
+            gemm1_flops=2.0 * P * 2 * I * H, gemm2_flops=2.0 * P * H * I,
             layer_bytes=touched * 3 * H * I * esize + 8 * E + T * E * 4 + 2 * T * H * 2)
 
     calls_per_step = len(Ts)
@@ -359,18 +368,35 @@ def run_ours(args, rank, local_rank, world):
             gemm1_ms[T].append(e[3].elapsed_time(e[4]))
             gemm2_ms[T].append(e[5].elapsed_time(e[6]))
     total_kernel_ms = sum(step_ms.values())
-    hbm_peak, peak_kind = measured_peaks()
-    # roofline of the heavier expert GEMM: algorithmic bytes over its launches
-    if step_ms["gemm2_combine"] > step_ms["gemm1_swiglu"]:
-        dominant = "gemm2_combine"
-        dom_bytes = sum(stats[T]["gemm2_bytes"] for T in Ts) * K
-        dom_ms = sum(sum(gemm2_ms[T]) for T in Ts)
-    else:
-        dominant = "gemm1_swiglu"
-        dom_bytes = sum(stats[T]["gemm1_bytes"] for T in Ts) * K
-        dom_ms = sum(sum(gemm1_ms[T]) for T in Ts)
-    achieved = dom_bytes / (dom_ms * 1e-3) / 1e9
+    hbm_peak, bf16_peak, peak_kind = measured_peaks()
+    tc_peak = bf16_peak * (FP8_OVER_BF16 if fp8 else 1.0)
+    tc_kind = (f"{peak_kind} bf16_tflops x {FP8_OVER_BF16:g} (nominal FP8/bf16)" if fp8
+               else f"{peak_kind} bf16_tflops")
+    # roofline of the heavier expert GEMM over its launches, against the
+    # binding limit: HBM bytes / bandwidth or FLOPs / tensor peak
+    dominant = ("gemm2_combine" if step_ms["gemm2_combine"] > step_ms["gemm1_swiglu"]
+                else "gemm1_swiglu")
+    g = "gemm2" if dominant == "gemm2_combine" else "gemm1"
+    dom_ms = sum(sum((gemm2_ms if g == "gemm2" else gemm1_ms)[T]) for T in Ts)
+    dom_bytes = sum(stats[T][f"{g}_bytes"] for T in Ts) * K
+    dom_flops = sum(stats[T][f"{g}_flops"] for T in Ts) * K
+    tensor_bound = dom_flops / (tc_peak * 1e12) > dom_bytes / (hbm_peak * 1e9)
+    achieved_gbs = dom_bytes / (dom_ms * 1e-3) / 1e9
+    achieved_tfs = dom_flops / (dom_ms * 1e-3) / 1e12
     traffic = recorded_traffic(args.workload, Ts) if dominant == "gemm1_swiglu" else None
+    if tensor_bound:
+        roofline = {"kernel": dominant, "bound": "tensor", "achieved": round(achieved_tfs, 1),
+                    "peak": round(tc_peak, 1), "peak_kind": tc_kind, "unit": "TFLOP/s",
+                    "frac": round(achieved_tfs / tc_peak, 4), "traffic": traffic,
+                    "algorithmic_flops": "2 x routed pairs x weight rows x K, per launch",
+                    "hbm_frac": round(achieved_gbs / hbm_peak, 4)}
+    else:
+        roofline = {"kernel": dominant, "bound": "hbm", "achieved": round(achieved_gbs, 1),
+                    "peak": hbm_peak, "peak_kind": f"{peak_kind} hbm_gbs", "unit": "GB/s",
+                    "frac": round(achieved_gbs / hbm_peak, 4), "traffic": traffic,
+                    "algorithmic_bytes": "touched experts' weight bytes + routed activation "
+                                         "rows in + h out, per launch",
+                    "tensor_frac": round(achieved_tfs / tc_peak, 4)}
 
     tokens_per_step = sum(Ts)
     value = world * tokens_per_step * K / (elapsed_ms * 1e-3)
@@ -382,6 +408,8 @@ def run_ours(args, rank, local_rank, world):
             "touched_experts": stats[T]["touched"], "max_rows_per_expert": stats[T]["max_rows"],
             "layer_bytes": stats[T]["layer_bytes"],
             "layer_hbm_frac": round(stats[T]["layer_bytes"] / (us * 1e-6) / 1e9 / hbm_peak, 4),
+            "layer_tensor_frac": round((stats[T]["gemm1_flops"] + stats[T]["gemm2_flops"])
+                                       / (us * 1e-6) / 1e12 / tc_peak, 4),
             "gemm1_us": round(statistics.median(gemm1_ms[T]) * 1e3, 2),
             "gemm2_us": round(statistics.median(gemm2_ms[T]) * 1e3, 2)})
 
@@ -461,11 +489,7 @@ def run_ours(args, rank, local_rank, world):
         "kernel_share": {n: round(step_ms[n] / total_kernel_ms, 4) for n in STEP_NAMES},
         "kernel_timing": "CUDA events between the kernels of every call, second pass of the "
                          f"same {K} steps ({instrumented_ms / K:.3f} ms/step with events)",
-        "roofline": {"kernel": dominant, "bound": "hbm", "achieved": round(achieved, 1),
-                     "peak": hbm_peak, "peak_kind": f"{peak_kind} hbm_gbs",
-                     "unit": "GB/s", "frac": round(achieved / hbm_peak, 4), "traffic": traffic,
-                     "algorithmic_bytes": "touched experts' weight bytes + routed activation "
-                                          "rows in + h out, per launch"},
+        "roofline": roofline,
         "clocks": clocks,
         "gpu_launches": K * launches_per_step,
         "e2e": e2e,
@@ -476,9 +500,147 @@ def run_ours(args, rank, local_rank, world):
         dist.destroy_process_group()
 
 
+# --------------------------------------------------------------------------- shapes
+def run_shape_sweep(args, rank, local_rank):
+    """Every T in 1..max_tokens (shuffled) through one process: the first call
+    at each T against the median of three more.  There is no per-shape
+    compilation or plan, so a first call costs what a later one does.  Then one
+    CUDA graph per power-of-two T bucket is captured, replayed on new inputs
+    written into its static buffers, and checked against an eager call."""
+    import random
+
+    import torch
+    import mixture_experts_layer_align_gb300 as moe
+    from mixture_experts_layer_align_gb300 import inputs
+
+    if rank != 0:
+        return
+    moe.load()
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    wl = args.workload if args.workload != "decode_e8_top2" else "finegrained_e128"
+    cfg = inputs.workload(wl)
+    H, I, E, k = cfg["H"], cfg["I"], cfg["E"], cfg["top_k"]
+    fp8 = cfg["dtype"] == "fp8"
+    dtype = moe.MOE_DT_FP8_E4M3 if fp8 else moe.MOE_DT_BF16
+    Tmax = args.max_tokens
+    w = inputs.make_weights(H, I, E, cfg["dtype"], seed=0, device=dev)
+    a = inputs.make_activations(Tmax, H, E, cfg["routing"], seed=0, device=dev)
+    out = torch.empty(Tmax, H, dtype=torch.bfloat16, device=dev)
+    ws = moe.alloc_workspace(Tmax, H, I, E, k, dtype, dev)
+
+    def call(T, o=None, x=None, lg=None):
+        moe.moe_fused_forward(a.x[:T] if x is None else x, a.logits[:T] if lg is None else lg,
+                              w.w13, w.w2, w.w13_scale, w.w2_scale, k, True,
+                              out=out[:T] if o is None else o, workspace=ws)
+
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(5)]
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    ev[0].record()
+    call(1)
+    ev[1].record()
+    torch.cuda.synchronize()
+    process_first = {"host_us": (time.perf_counter() - t0) * 1e6,
+                     "device_us": ev[0].elapsed_time(ev[1]) * 1e3}
+
+    # Each first call is enqueued behind the previous T's calls, so the GPU is
+    # busy while the host prepares it (as in steady use); results are read
+    # after every chunk of T values.
+    Ts = list(range(2, Tmax + 1))
+    random.Random(0).shuffle(Ts)
+    rows = []
+    chunk = 64
+    prev = 1
+    for c0 in range(0, len(Ts), chunk):
+        part = Ts[c0:c0 + chunk]
+        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in part]
+        host = []
+        call(prev)  # keeps the GPU busy while the first measured call is enqueued
+        for T, e in zip(part, evs):
+            h0 = time.perf_counter()
+            e[0].record()
+            call(T)
+            e[1].record()
+            host.append((time.perf_counter() - h0) * 1e6)
+            for i in range(3):
+                call(T)
+                e[2 + i].record()
+        torch.cuda.synchronize()
+        for T, e, h in zip(part, evs, host):
+            first = e[0].elapsed_time(e[1]) * 1e3
+            steady = sorted([e[1].elapsed_time(e[2]), e[2].elapsed_time(e[3]),
+                             e[3].elapsed_time(e[4])])[1] * 1e3
+            rows.append((T, first, steady, h))
+        prev = part[-1]
+    st = moe.moe_check_status(ws)
+    if st != 0:
+        raise RuntimeError(f"device status {moe.status_string(st)}")
+    ratios = sorted(r[1] / r[2] for r in rows)
+    host = sorted(r[3] for r in rows)
+    rows.sort()
+    pick = {1 << i for i in range(14)} | {3, 37, 100, 1000, 3000, 5000, 7777}
+    per_T = [{"T": T, "first_us": round(f, 1), "steady_us": round(s_, 1),
+              "host_first_us": round(h, 1)} for T, f, s_, h in rows if T in pick]
+
+    # one CUDA graph per bucket: capture, replay on fresh inputs, compare
+    graphs = []
+    for T in [1 << i for i in range(14) if (1 << i) <= Tmax]:
+        gx = torch.empty(T, H, dtype=torch.bfloat16, device=dev)
+        gl = torch.empty(T, E, dtype=torch.float32, device=dev)
+        go = torch.empty(T, H, dtype=torch.bfloat16, device=dev)
+        gx.copy_(a.x[:T])
+        gl.copy_(a.logits[:T])
+        s_ = torch.cuda.Stream(device=dev)
+        s_.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s_):
+            call(T, go, gx, gl)  # eager call on the capture stream first
+        torch.cuda.current_stream().wait_stream(s_)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s_):
+            call(T, go, gx, gl)
+        fresh = inputs.make_activations(T, H, E, cfg["routing"], seed=T + 1, device=dev)
+        gx.copy_(fresh.x)
+        gl.copy_(fresh.logits)
+        g.replay()
+        ref = torch.empty_like(go)
+        call(T, ref, fresh.x, fresh.logits)
+        torch.cuda.synchronize()
+        err = ((go.float() - ref.float()).abs().max() /
+               ref.float().abs().max().clamp_min(1e-30)).item()
+        g0 = torch.cuda.Event(enable_timing=True)
+        g1 = torch.cuda.Event(enable_timing=True)
+        g0.record()
+        for _ in range(20):
+            g.replay()
+        g1.record()
+        torch.cuda.synchronize()
+        graphs.append({"T": T, "replay_us": round(g0.elapsed_time(g1) * 1e3 / 20, 1),
+                       "max_rel_diff_vs_eager": err})
+        del g
+    line = {
+        "metric": "first-call vs steady-state us per moe_fused_forward, every T in 1..%d" % Tmax,
+        "workload": f"{wl}: H={H}, I={I}, E={E}, top_k={k}, {cfg['routing']} routing, "
+                    f"{'FP8 E4M3' if fp8 else 'bf16'}",
+        "order": "T = 2..%d in seeded random order after the process's first call (T=1)" % Tmax,
+        "process_first_call": {k_: round(v, 1) for k_, v in process_first.items()},
+        "first_over_steady": {"median": round(statistics.median(ratios), 3),
+                              "p99": round(ratios[int(0.99 * (len(ratios) - 1))], 3),
+                              "max": round(ratios[-1], 3)},
+        "host_us_per_first_call": {"median": round(statistics.median(host), 1),
+                                   "max": round(host[-1], 1)},
+        "per_T": per_T,
+        "cuda_graphs": graphs,
+    }
+    print(json.dumps(line), flush=True)
+
+
 def main():
     args = parse()
     rank, local_rank, world = dist_env()
+    if args.shape_sweep:
+        run_shape_sweep(args, rank, local_rank)
+        return
     if args.impl == "reference":
         run_reference(args, rank, world)
     else:

@@ -187,7 +187,9 @@ moe_status_t moe_fused_forward(const moe_fused_args* args, void* workspace, size
  * measurable: events[i] (a cudaEvent_t created by the caller) is recorded on
  * `stream` before step i and events[7] after the last step.  Steps: 0 routing,
  * 1 alignment, 2 gather/quantise x, 3 gate/up GEMM + SiLU*up, 4 quantise h
- * (empty for bf16), 5 down GEMM + combine, 6 bf16 output.  Requires
+ * (empty for bf16), 5 down GEMM + combine, 6 bf16 output.  Small batches
+ * route and align in one kernel: events[1] and events[2] are then both
+ * recorded after it (step 1 is empty).  Requires
  * n_events >= MOE_TIMED_EVENTS and non-null events; otherwise as
  * moe_fused_forward.
  */

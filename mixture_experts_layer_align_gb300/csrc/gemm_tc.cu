@@ -96,30 +96,77 @@ __device__ __forceinline__ int tile_of_seq(int s, int tiles) {
   return row * G + col;
 }
 
-// Segments of this CTA: contiguous range [beg, end) of the flat
-// (tile sequence, K step) index space.
-struct Range {
-  long long beg, end, total;
+// Work split over the flat (tile, K step) space, in two parts.
+//  - The first `rr` tiles go whole and round-robin: CTA c takes tiles c, c+G,
+//    c+2G, ... in natural (expert, weight block, row tile) order, so at any
+//    moment the CTAs work on G consecutive tiles and the weight blocks and
+//    token rows those share are read from HBM once and then hit in L2.
+//  - The remaining tiles (the tail) are cut evenly over the CTAs, one
+//    contiguous range of the flat tail space each (stream-K); a tile cut
+//    between CTAs is finished from partial sums.
+// With no reuse to keep (decode: every weight block serves one row tile) the
+// whole space is tail, visited in the column-major order of tile_of_seq.
+// Rows written per pair cannot take partial sums: then every tile is whole.
+struct Sched {
+  int tiles, K, rr;
+  bool permute;          // tail order: tile_of_seq (no reuse) or natural
+  long long tail_total;  // (tiles - rr) * K
+  long long beg, end;    // this CTA's range of the tail space
 };
 
-__device__ __forceinline__ Range cta_range(long long total) {
-  Range r;
-  r.total = total;
-  r.beg = total * blockIdx.x / gridDim.x;
-  r.end = total * (blockIdx.x + 1) / gridDim.x;
-  return r;
+__device__ __forceinline__ Sched make_sched(int tiles, int K, bool reuse, bool whole) {
+  const int G = static_cast<int>(gridDim.x);
+  Sched s;
+  s.tiles = tiles;
+  s.K = K;
+  s.rr = whole ? tiles : (reuse ? tiles / G * G : 0);
+  s.permute = !reuse;
+  s.tail_total = static_cast<long long>(tiles - s.rr) * K;
+  s.beg = s.tail_total * blockIdx.x / G;
+  s.end = s.tail_total * (blockIdx.x + 1) / G;
+  return s;
 }
 
-// Same split rounded to whole tiles (no tile is cut between CTAs).
-__device__ __forceinline__ Range cta_range_whole_tiles(int tiles, int K) {
-  Range r;
-  r.total = static_cast<long long>(tiles) * K;
-  r.beg = static_cast<long long>(tiles) * blockIdx.x / gridDim.x * K;
-  r.end = static_cast<long long>(tiles) * (blockIdx.x + 1) / gridDim.x * K;
-  return r;
+// One segment: K steps [k0, k1) of `tile`; t0 = flat start of the tile in the
+// tail space (meaningful for tail tiles only).
+struct Seg {
+  int tile, k0, k1;
+  long long t0;
+};
+
+struct SegIt {
+  int u;        // next round-robin tile
+  long long i;  // next flat tail index
+};
+
+__device__ __forceinline__ SegIt seg_begin(const Sched& s) {
+  SegIt it;
+  it.u = static_cast<int>(blockIdx.x);
+  it.i = s.beg;
+  return it;
 }
 
-// CTA whose range holds flat index i.
+__device__ __forceinline__ bool seg_next(const Sched& s, SegIt& it, Seg& g) {
+  if (it.u < s.rr) {
+    g.tile = it.u;
+    g.k0 = 0;
+    g.k1 = s.K;
+    g.t0 = 0;
+    it.u += static_cast<int>(gridDim.x);
+    return true;
+  }
+  if (it.i >= s.end) return false;
+  const int v = static_cast<int>(it.i / s.K);
+  g.k0 = static_cast<int>(it.i - static_cast<long long>(v) * s.K);
+  const long long rem = s.end - it.i;
+  g.k1 = (static_cast<long long>(s.K) < g.k0 + rem) ? s.K : static_cast<int>(g.k0 + rem);
+  g.t0 = static_cast<long long>(v) * s.K;
+  g.tile = s.rr + (s.permute ? tile_of_seq(v, s.tiles - s.rr) : v);
+  it.i += g.k1 - g.k0;
+  return true;
+}
+
+// CTA whose tail range holds flat index i.
 __device__ __forceinline__ int owner_of(long long i, long long total) {
   return static_cast<int>(((i + 1) * gridDim.x - 1) / total);
 }
@@ -198,17 +245,23 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   tc_fence_after_sync();
   const uint32_t tmem = *tmem_slot;
 
-  // everything above overlaps the previous kernel; from here on its outputs are read
-  pdl_wait();
-  pdl_trigger();
+  // Everything above overlaps the previous kernel.  The weights are inputs of
+  // the call, so the producer also puts the first stages' weight blocks in
+  // flight before that kernel has finished (below); the row-tile list it reads
+  // for that was written two or more kernels back, and every kernel of the
+  // library signals its dependents only after its own wait, so its writers
+  // have completed.  All other threads wait here.
+  const bool early_producer = (warp == 0 && lane == 0);
+  if (!early_producer) {
+    pdl_wait();
+    pdl_trigger();
+  }
   if (trace && threadIdx.x == 0) trace[1] = global_timer_ns();
 
   const int K = p.k_steps;
   const int tiles = p.ctrl->num_mtiles * p.nb_count;
-  // rows written per pair cannot take partial sums: whole tiles then
-  const Range rg = (!kSwiGLU && p.pair_out != nullptr)
-                       ? cta_range_whole_tiles(tiles, K)
-                       : cta_range(static_cast<long long>(tiles) * K);
+  const Sched sch = make_sched(tiles, K, p.weights_evict_first == 0,
+                               !kSwiGLU && p.pair_out != nullptr);
   const uint64_t limit = p.timeout_ns;
 
   if (warp == 0) {
@@ -219,31 +272,52 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       const uint64_t pol_w = p.weights_evict_first ? policy_evict_first() : policy_evict_last();
       uint32_t it = 0;
       bool ok = true;
-      for (long long i = rg.beg; i < rg.end && ok;) {
-        const int u = static_cast<int>(i / K);
-        const int k0 = static_cast<int>(i - static_cast<long long>(u) * K);
-        const int k1 = static_cast<int>((K < k0 + (rg.end - i) ? static_cast<long long>(K) : k0 + (rg.end - i)));
-        const Tile t = decode_tile(p, tile_of_seq(u, tiles));
+      SegIt si = seg_begin(sch);
+      Seg g;
+      // weight blocks of the first S stages (fresh stages: no wait on `empty`)
+      uint32_t pre = 0;
+      {
+        SegIt sj = si;
+        Seg gj;
+        while (pre < static_cast<uint32_t>(S) && seg_next(sch, sj, gj)) {
+          const Tile t = decode_tile(p, gj.tile);
+          const int wrow = t.e * p.rows_per_expert + t.nb * 128;
+          for (int kk = gj.k0; kk < gj.k1 && pre < static_cast<uint32_t>(S); ++kk, ++pre) {
+            uint8_t* sa = smem + static_cast<size_t>(pre) * stage_bytes;
+            mbar_arrive_expect_tx(full + pre, kABytes + static_cast<uint32_t>(t.n) * 128u);
+            const int kc = kk * p.k_elems;
+            tma_load_2d_hint(sa, &tm_a, full + pre, kc, wrow, pol_w);
+            if (kSwiGLU)
+              tma_load_2d_hint(sa + 16384, &tm_a, full + pre, kc, wrow + p.up_offset, pol_w);
+          }
+        }
+      }
+      // token rows are the previous kernels' output
+      pdl_wait();
+      pdl_trigger();
+      while (ok && seg_next(sch, si, g)) {
+        const Tile t = decode_tile(p, g.tile);
         const int wrow = t.e * p.rows_per_expert + t.nb * 128;
-        for (int kk = k0; kk < k1; ++kk, ++it) {
+        for (int kk = g.k0; kk < g.k1; ++kk, ++it) {
           const uint32_t s = it % S;
           const uint32_t ph = (it / S) & 1u;
-          if (!mbar_wait(empty + s, ph ^ 1u, abort_flag, limit)) {
-            ok = false;
-            break;
-          }
           uint8_t* sa = smem + static_cast<size_t>(s) * stage_bytes;
           uint8_t* sb = sa + kABytes;
-          mbar_arrive_expect_tx(full + s, kABytes + static_cast<uint32_t>(t.n) * 128u);
           const int kc = kk * p.k_elems;
-          tma_load_2d_hint(sa, &tm_a, full + s, kc, wrow, pol_w);
-          if (kSwiGLU) tma_load_2d_hint(sa + 16384, &tm_a, full + s, kc, wrow + p.up_offset, pol_w);
+          if (it >= pre) {
+            if (!mbar_wait(empty + s, ph ^ 1u, abort_flag, limit)) {
+              ok = false;
+              break;
+            }
+            mbar_arrive_expect_tx(full + s, kABytes + static_cast<uint32_t>(t.n) * 128u);
+            tma_load_2d_hint(sa, &tm_a, full + s, kc, wrow, pol_w);
+            if (kSwiGLU) tma_load_2d_hint(sa + 16384, &tm_a, full + s, kc, wrow + p.up_offset, pol_w);
+          }
           // token rows: 64-row boxes, then 16-row boxes for the remainder
           int j = 0;
           for (; j + 64 <= t.n; j += 64) tma_load_2d(sb + j * 128, &tm_b64, full + s, kc, t.row0 + j);
           for (; j < t.n; j += 16) tma_load_2d(sb + j * 128, &tm_b, full + s, kc, t.row0 + j);
         }
-        i += k1 - k0;
       }
       if (!ok) {
         *abort_flag = 1;
@@ -263,11 +337,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       uint32_t it = 0, tt = 0;
       bool ok = true;
       if (p.debug & MOE_DEBUG_FORCE_TIMEOUT) ok = mbar_wait(never, 0, abort_flag, limit);
-      for (long long i = rg.beg; i < rg.end && ok;) {
-        const int u = static_cast<int>(i / K);
-        const int k0 = static_cast<int>(i - static_cast<long long>(u) * K);
-        const int k1 = static_cast<int>((K < k0 + (rg.end - i) ? static_cast<long long>(K) : k0 + (rg.end - i)));
-        const Tile t = decode_tile(p, tile_of_seq(u, tiles));
+      SegIt si = seg_begin(sch);
+      Seg g;
+      while (ok && seg_next(sch, si, g)) {
+        const int k0 = g.k0, k1 = g.k1;
+        const Tile t = decode_tile(p, g.tile);
         const uint32_t a = tt % static_cast<uint32_t>(p.num_acc);
         const uint32_t aph = (tt / static_cast<uint32_t>(p.num_acc)) & 1u;
         if (!mbar_wait(tempty + a, aph ^ 1u, abort_flag, limit)) {
@@ -308,7 +382,6 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         if (!ok) break;
         umma_commit(tfull + a);
         ++tt;
-        i += k1 - k0;
       }
       if (!ok) {
         *abort_flag = 1;
@@ -329,11 +402,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     uint32_t n_chunks = 0;  // combine staging chunks issued by this warp
     uint32_t tt = 0;
     bool ok = true;
-    for (long long i = rg.beg; i < rg.end;) {
-      const int u = static_cast<int>(i / K);
-      const int k0 = static_cast<int>(i - static_cast<long long>(u) * K);
-      const int k1 = static_cast<int>((K < k0 + (rg.end - i) ? static_cast<long long>(K) : k0 + (rg.end - i)));
-      const Tile t = decode_tile(p, tile_of_seq(u, tiles));
+    SegIt si = seg_begin(sch);
+    Seg g;
+    while (seg_next(sch, si, g)) {
+      const int k0 = g.k0, k1 = g.k1;
+      const Tile t = decode_tile(p, g.tile);
       const uint32_t a = tt % static_cast<uint32_t>(p.num_acc);
       const uint32_t aph = (tt / static_cast<uint32_t>(p.num_acc)) & 1u;
       // column metadata of the tile, fetched while the MMAs run: lane l holds
@@ -363,13 +436,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       if (kSwiGLU) {
         const bool whole = (k0 == 0 && k1 == K);
         bool finish = whole;
-        long long t0 = static_cast<long long>(u) * K;
+        const long long t0 = g.t0;  // split tiles lie in the tail
         int c_first = 0, c_last = 0;
         if (!whole) {
           // store this contributor's partial, then count arrivals on the tile
-          c_first = owner_of(t0, rg.total);
-          c_last = owner_of(t0 + K - 1, rg.total);
-          float* mine = part_slot(p, blockIdx.x, t0, rg.total);
+          c_first = owner_of(t0, sch.tail_total);
+          c_last = owner_of(t0 + K - 1, sch.tail_total);
+          float* mine = part_slot(p, blockIdx.x, t0, sch.tail_total);
           for (int c0 = c_begin; c0 < t.n; c0 += 32) {
             float g[16], v[16];
             tmem_ld16x2(tbase + c0, tbase + p.bn_max + c0, g, v);
@@ -385,8 +458,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             // contributors: CTAs in [c_first, c_last] whose range is not empty
             int n_seg = 0;
             for (int c = c_first; c <= c_last; ++c)
-              n_seg += range_begin(c, rg.total) < range_begin(c + 1, rg.total) ? 1 : 0;
-            *s_last = (atomicAdd(p.tile_cnt + u, 1) == n_seg - 1) ? 1 : 0;
+              n_seg += range_begin(c, sch.tail_total) < range_begin(c + 1, sch.tail_total) ? 1 : 0;
+            *s_last = (atomicAdd(p.tile_cnt + g.tile, 1) == n_seg - 1) ? 1 : 0;
           }
           named_barrier(kEpiBarrier, kEpiThreads);
           finish = *s_last != 0;
@@ -400,9 +473,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             if (!whole) {
               for (int c = c_first; c <= c_last; ++c) {
                 if (c == static_cast<int>(blockIdx.x) ||
-                    range_begin(c, rg.total) == range_begin(c + 1, rg.total))
+                    range_begin(c, sch.tail_total) == range_begin(c + 1, sch.tail_total))
                   continue;
-                const float* other = part_slot(p, c, t0, rg.total);
+                const float* other = part_slot(p, c, t0, sch.tail_total);
 #pragma unroll
                 for (int j = 0; j < 16; ++j) {
                   g[j] += __ldcg(other + static_cast<size_t>(c0 + j) * 128 + row_l);
@@ -480,7 +553,6 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(tempty + a);
       ++tt;
-      i += k1 - k0;
     }
     if (kSwiGLU && !kBF16) {
 #pragma unroll

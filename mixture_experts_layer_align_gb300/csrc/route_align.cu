@@ -92,20 +92,34 @@ __device__ int block_exclusive_scan_1024(int v, int* tmp, int* total) {
 }
 
 // ------------------------------------------------------------------ router
-// One warp per token.  The row of logits is staged in shared memory (`l`, E
-// floats of this warp); each of the k rounds is a warp arg-max under (logit
-// desc, index asc) over the experts not taken yet (one bit per lane per 32
-// experts).  The softmax uses expf on max-subtracted logits.  Writes the k
-// ids and weights of the token (id_row / w_row may be shared or global).
+// Order-preserving map of a finite float to uint32 (larger float, larger
+// key; every key is > 0); -0.0 maps like +0.0 so that the two compare equal.
+__device__ __forceinline__ uint32_t float_key(float v) {
+  uint32_t u = __float_as_uint(v);
+  if ((u << 1) == 0u) u = 0u;
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+__device__ __forceinline__ float key_float(uint32_t key) {
+  return __uint_as_float((key & 0x80000000u) ? (key & 0x7fffffffu) : ~key);
+}
+
+// One token, one warp.  The row of logits is staged in shared memory (`l`, E
+// floats of this warp); softmax with expf on max-subtracted logits; each of
+// the k rounds takes the arg-max under (logit desc, index asc) over the
+// experts not taken yet (one bit per lane per 32 experts) with two warp
+// reductions: the largest key among the lanes' best remaining logits, then
+// the lowest expert index holding it.  Writes the k ids and weights (divided
+// by their sum when renormalising; id_row / w_row may be shared or global).
 __device__ void route_token(const float* __restrict__ src, int E, int k, int renorm, float* l,
                             int32_t* id_row, float* w_row, int lane) {
-  float m = -INFINITY;
+  uint32_t km = 0u;
   for (int e = lane; e < E; e += 32) {
     const float v = src[e];
     l[e] = v;
-    m = fmaxf(m, v);
+    km = max(km, float_key(v));
   }
-  m = warp_max(m);
+  const float m = key_float(__reduce_max_sync(kFull, km));
   float z = 0.f;
   for (int e = lane; e < E; e += 32) z += expf(l[e] - m);
   z = warp_sum(z);
@@ -114,31 +128,24 @@ __device__ void route_token(const float* __restrict__ src, int E, int k, int ren
   uint32_t taken = 0u;  // bit i <=> expert lane + 32 i already selected
   float sel = 0.f;
   for (int j = 0; j < k; ++j) {
-    float bv = -INFINITY;
-    int bi = 0x7fffffff;  // "none"
+    uint32_t bk = 0u;  // 0: no candidate left in this lane
+    int bi = 0;
     for (int e = lane, i = 0; e < E; e += 32, ++i) {
       if ((taken >> i) & 1u) continue;
-      const float v = l[e];
-      if (bi == 0x7fffffff || v > bv) {  // ascending scan: equal values keep the lower index
-        bv = v;
+      const uint32_t key = float_key(l[e]);
+      if (key > bk) {  // ascending scan: equal keys keep the lower index
+        bk = key;
         bi = e;
       }
     }
-#pragma unroll
-    for (int o = 16; o; o >>= 1) {
-      const float ov = __shfl_xor_sync(kFull, bv, o);
-      const int oi = __shfl_xor_sync(kFull, bi, o);
-      const bool take = oi != 0x7fffffff && (bi == 0x7fffffff || ov > bv || (ov == bv && oi < bi));
-      if (take) {
-        bv = ov;
-        bi = oi;
-      }
-    }
-    if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
-    const float ex = expf(bv - m);
+    const uint32_t kmax = __reduce_max_sync(kFull, bk);
+    const int win = static_cast<int>(
+        __reduce_min_sync(kFull, bk == kmax ? static_cast<uint32_t>(bi) : 0xffffffffu));
+    if ((win & 31) == lane) taken |= 1u << (win >> 5);
+    const float ex = expf(key_float(kmax) - m);
     sel += ex;
     if (lane == 0) {
-      id_row[j] = bi;
+      id_row[j] = win;
       w_row[j] = ex;
     }
   }
