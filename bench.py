@@ -58,6 +58,9 @@ def parse():
                     help="first-call vs steady-state time for every T in 1..--max-tokens "
                          "in one process, plus CUDA-graph capture per T bucket")
     ap.add_argument("--max-tokens", type=int, default=8192)
+    ap.add_argument("--placement", default="auto", choices=["auto", "weights", "tokens"],
+                    help="MMA operand placement of both expert GEMMs: weight rows in M (the "
+                         "swap), tokens in M (ablation), or the library's default choice")
     return ap.parse_args()
 
 
@@ -263,6 +266,8 @@ def run_ours(args, rank, local_rank, world):
     H, I, E, k = cfg["H"], cfg["I"], cfg["E"], cfg["top_k"]
     fp8 = cfg["dtype"] == "fp8"
     dtype = moe.MOE_DT_FP8_E4M3 if fp8 else moe.MOE_DT_BF16
+    flags = {"auto": 0, "weights": moe.MOE_FLAG_WEIGHTS_IN_M,
+             "tokens": moe.MOE_FLAG_TOKENS_IN_M}[args.placement]
     w = inputs.make_weights(H, I, E, cfg["dtype"], seed=0, device=dev)
     # second copy of the same weights in other buffers: consecutive calls
     # alternate, so no call finds its weights in L2
@@ -279,7 +284,7 @@ def run_ours(args, rank, local_rank, world):
         counts = torch.empty(E, dtype=torch.int32, device=dev)
         a = acts[T]
         moe.moe_fused_forward(a.x, a.logits, w.w13, w.w2, w.w13_scale, w.w2_scale, k, True,
-                              out=outs[T], workspace=wss[T], counts_out=counts)
+                              out=outs[T], workspace=wss[T], counts_out=counts, debug_flags=flags)
         st = moe.moe_check_status(wss[T])
         if st != 0:
             raise RuntimeError(f"device status {moe.status_string(st)}")
@@ -301,7 +306,7 @@ def run_ours(args, rank, local_rank, world):
             ww = copies[(step_idx * calls_per_step + j) % 2]
             a = acts[T]
             moe.moe_fused_forward(a.x, a.logits, ww.w13, ww.w2, ww.w13_scale, ww.w2_scale, k,
-                                  True, out=outs[T], workspace=wss[T],
+                                  True, out=outs[T], workspace=wss[T], debug_flags=flags,
                                   events=None if events is None else events[j])
 
     for i in range(max(args.warmup, 3)):
@@ -430,7 +435,7 @@ def run_ours(args, rank, local_rank, world):
                 dx[T].copy_(hx, non_blocking=True)
                 dl[T].copy_(hl, non_blocking=True)
                 moe.moe_fused_forward(dx[T], dl[T], ww.w13, ww.w2, ww.w13_scale, ww.w2_scale, k,
-                                      True, out=outs[T], workspace=wss[T])
+                                      True, out=outs[T], workspace=wss[T], debug_flags=flags)
                 ho.copy_(outs[T], non_blocking=True)
 
         for i in range(3):
@@ -484,7 +489,12 @@ def run_ours(args, rank, local_rank, world):
             "l2": "inputs larger than L2: two copies of the "
                   f"{(w.w13.numel() + w.w2.numel()) * esize / 1e9:.2f} GB weights alternate "
                   "call to call",
-            "parallelism": f"replicas x{world}"},
+            "parallelism": f"replicas x{world}",
+            "placement": {"auto": "gate/up: weights in the MMA M slot; down: weights in M "
+                                   "if I > 2048 else tokens in M",
+                           "weights": "weights in the MMA M slot for both GEMMs (swap-AB)",
+                           "tokens": "tokens in the MMA M slot for both GEMMs (no swap)"}[
+                              args.placement]},
         "sweep": sweep,
         "kernel_share": {n: round(step_ms[n] / total_kernel_ms, 4) for n in STEP_NAMES},
         "kernel_timing": "CUDA events between the kernels of every call, second pass of the "

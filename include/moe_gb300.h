@@ -157,6 +157,15 @@ typedef struct {
  * They go to uint64 [2][MOE_TRACE_MAX_CTAS][4] at byte offset
  * moe_fused_trace_offset() of the workspace (gate/up kernel first). */
 #define MOE_DEBUG_TRACE 0x2
+/* Operand placement (section "Swap-AB for WGMMA utilization").  By default
+ * the gate/up GEMM puts the expert's weight rows in the MMA's M slot (the
+ * swap) and the down GEMM does so when I > 2048; with I <= 2048 the down GEMM
+ * puts the tokens (128-row tiles) in M.  MOE_FLAG_TOKENS_IN_M forces tokens
+ * in M and MOE_FLAG_WEIGHTS_IN_M forces weights in M for both GEMMs (the
+ * ablation of the swap); both together are MOE_ERR_INVALID_ARG.  Results are
+ * the same within fp32 summation order. */
+#define MOE_FLAG_TOKENS_IN_M 0x4
+#define MOE_FLAG_WEIGHTS_IN_M 0x8
 #define MOE_TRACE_MAX_CTAS 256
 size_t moe_fused_trace_offset(int T, int H, int I, int E, int top_k, moe_dtype_t dtype);
 

@@ -5,17 +5,18 @@
 // and the digest page's B^T[N,K] x A^T[K,M] -> C^T[N,M]): the expert weight
 // block (128 output rows) is the MMA's A operand and fills the M = 128 slot
 // (128 TMEM lanes); the tokens routed to the expert are the B operand, N =
-// 16..256 columns.  When an expert sees one token (decode) the MMA still does
+// 16..128 columns.  When an expert sees one token (decode) the MMA still does
 // useful work on all 128 lanes, and the weight stream is what the kernel
-// waits on.  The same tiling serves prefill, where N grows to 256.
+// waits on.
 //
-// Work split ("stream-K"): a tile is (row tile of one expert's tokens) x
-// (128-row weight block) with K/128B steps; the flat (tile, K step) space is
-// cut into one contiguous range per CTA, so every SM streams the same number
-// of weight bytes whatever the expert and tile counts.  Tiles of one expert
-// are ordered weight-block-major so a weight block is reused by all of the
-// expert's row tiles back to back (L2 hits in prefill).  A tile cut by a CTA
-// boundary is finished by its last contributor: in the down projection the
+// Work split: a tile is (row tile of one expert's tokens) x (128-row weight
+// block) with K/128B steps; tiles of one expert are ordered weight-block-major
+// so a weight block serves all of the expert's row tiles back to back.  When
+// tiles share data through L2 (prefill) full waves of whole tiles go
+// round-robin and only the last partial wave is split over the CTAs
+// (stream-K); with nothing to share (decode) the whole (tile, K step) space is
+// split, so every SM streams the same number of weight bytes.  A tile cut by a
+// CTA boundary is finished by its last contributor: in the down projection the
 // partial sums simply add into the combine buffer (the combine is linear); in
 // the gate/up projection every contributor stores its partial accumulators and
 // the last to arrive (per-tile counter) adds them and runs SiLU*up.
@@ -25,13 +26,14 @@
 //               ring of shared-memory stages (128-byte swizzle, K-major);
 //   warp 1      allocates TMEM and issues tcgen05.mma (one thread), commits
 //               stage release and accumulator-ready barriers;
-//   warps 2..5  epilogue: tcgen05.ld of the accumulator, then either
+//   warps 2..9  epilogue (two warps per TMEM lane quarter): tcgen05.ld of the
+//               accumulator, then either
 //               gate/up:  h = SiLU(g * s) * (u * s) -> fp32 (FP8 path, with a
 //                         running amax|h|) or bf16 (bf16 path)
-//               down:     y * s * topk_weight staged in shared memory and
-//                         added into the fp32 combine buffer with bulk
-//                         asynchronous reductions (expert aggregation fused
-//                         into the GEMM).
+//               down:     y * s * topk_weight added into the fp32 combine
+//                         buffer with bulk asynchronous reductions staged in
+//                         shared memory, or written as bf16 rows per pair
+//                         (expert aggregation fused into the GEMM).
 // The accumulator is double-buffered in TMEM when it fits, so the epilogue of
 // one segment overlaps the MMAs of the next.  Every wait is bounded; on
 // timeout the CTA records kDevErrTimeout and leaves.
@@ -47,7 +49,7 @@ namespace {
 
 constexpr int kSmemLimit = 232448;  // 227 KB opt-in per CTA
 constexpr int kSmemSlack = 1024 + 256;
-constexpr int kMaxStages = 8;
+constexpr int kMaxStages = 12;  // 2 * 12 + 5 barriers + 3 words fit the 256-byte area
 constexpr uint32_t kEpiBarrier = 1;  // named barrier of the 4 epilogue warps
 constexpr uint32_t kEpiThreads = 32 * kGemmEpiWarps;
 
@@ -189,7 +191,11 @@ __device__ __forceinline__ V pick4(const V (&v)[4], int s) {
   return s == 0 ? v[0] : (s == 1 ? v[1] : (s == 2 ? v[2] : v[3]));
 }
 
-template <bool kBF16, bool kSwiGLU>
+// kTokM selects the unswapped placement (the ablation of the operand swap):
+// the 128-row token tile is the A operand in the M slot and the weight block
+// is B with N = 128 weight rows; lanes then hold tokens and TMEM columns hold
+// weight rows.
+template <bool kBF16, bool kSwiGLU, bool kTokM>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     moe_gemm_kernel(const __grid_constant__ GemmParams p, const __grid_constant__ CUtensorMap tm_a,
                     const __grid_constant__ CUtensorMap tm_b,
@@ -197,9 +203,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
-  const int S = p.stages;
+  // Pipeline depth from the largest row tile of this call (written by the
+  // alignment kernel two or more launches back, see below): a stage holds the
+  // weight block(s) and that many token rows, and as many stages as fit are
+  // used, so decode (tiles of a few rows) keeps more weight bytes in flight.
   constexpr uint32_t kABytes = kSwiGLU ? 32768u : 16384u;
-  const uint32_t stage_bytes = kABytes + static_cast<uint32_t>(p.bn_max) * 128u;
+  const int rows_b = kTokM ? 128 : min(p.bn_max, max(16, p.ctrl->max_tile_rows));
+  const uint32_t stage_bytes = kABytes + static_cast<uint32_t>(rows_b) * 128u;
+  const int S = min(kMaxStages, static_cast<int>(p.stage_smem / stage_bytes));
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + static_cast<size_t>(S) * stage_bytes);
   uint64_t* empty = full + S;
   uint64_t* tfull = empty + S;
@@ -284,7 +295,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           const int wrow = t.e * p.rows_per_expert + t.nb * 128;
           for (int kk = gj.k0; kk < gj.k1 && pre < static_cast<uint32_t>(S); ++kk, ++pre) {
             uint8_t* sa = smem + static_cast<size_t>(pre) * stage_bytes;
-            mbar_arrive_expect_tx(full + pre, kABytes + static_cast<uint32_t>(t.n) * 128u);
+            mbar_arrive_expect_tx(full + pre, kABytes + static_cast<uint32_t>(kTokM ? 128 : t.n) * 128u);
             const int kc = kk * p.k_elems;
             tma_load_2d_hint(sa, &tm_a, full + pre, kc, wrow, pol_w);
             if (kSwiGLU)
@@ -309,14 +320,22 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
               ok = false;
               break;
             }
-            mbar_arrive_expect_tx(full + s, kABytes + static_cast<uint32_t>(t.n) * 128u);
+            mbar_arrive_expect_tx(full + s, kABytes + static_cast<uint32_t>(kTokM ? 128 : t.n) * 128u);
             tma_load_2d_hint(sa, &tm_a, full + s, kc, wrow, pol_w);
             if (kSwiGLU) tma_load_2d_hint(sa + 16384, &tm_a, full + s, kc, wrow + p.up_offset, pol_w);
           }
-          // token rows: 64-row boxes, then 16-row boxes for the remainder
-          int j = 0;
-          for (; j + 64 <= t.n; j += 64) tma_load_2d(sb + j * 128, &tm_b64, full + s, kc, t.row0 + j);
-          for (; j < t.n; j += 16) tma_load_2d(sb + j * 128, &tm_b, full + s, kc, t.row0 + j);
+          if (kTokM) {
+            // tokens fill the M = 128 slot: 128 rows from the tile's first row
+            // (rows past the tile belong to other tiles and are not stored;
+            // rows past the buffer read as zero)
+            tma_load_2d(sb, &tm_b64, full + s, kc, t.row0);
+            tma_load_2d(sb + 64 * 128, &tm_b64, full + s, kc, t.row0 + 64);
+          } else {
+            // token rows: 64-row boxes, then 16-row boxes for the remainder
+            int j = 0;
+            for (; j + 64 <= t.n; j += 64) tma_load_2d(sb + j * 128, &tm_b64, full + s, kc, t.row0 + j);
+            for (; j < t.n; j += 16) tma_load_2d(sb + j * 128, &tm_b, full + s, kc, t.row0 + j);
+          }
         }
       }
       if (!ok) {
@@ -349,7 +368,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           break;
         }
         tc_fence_after_sync();
-        const uint32_t idesc = umma_idesc(kBF16, 128, t.n);
+        const uint32_t idesc = umma_idesc(kBF16, 128, kTokM ? 128 : t.n);
         const uint32_t d0 = tmem + a * static_cast<uint32_t>(p.acc_stride);
         const uint32_t d1 = d0 + static_cast<uint32_t>(p.bn_max);
         for (int kk = k0; kk < k1; ++kk, ++it) {
@@ -369,12 +388,15 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           for (int k4 = 0; k4 < 4; ++k4) {
             const uint32_t acc = (kk > k0 || k4 > 0) ? 1u : 0u;
             // +2 in the start-address field = +32 bytes of K inside the swizzle atom
+            // swap: A = weight block, B = tokens; unswapped: A = tokens, B = weights
+            const uint64_t a0 = kTokM ? db : da0, b0 = kTokM ? da0 : db;
+            const uint64_t a1 = kTokM ? db : da1, b1 = kTokM ? da1 : db;
             if (kBF16) {
-              umma_bf16(d0, da0 + 2 * k4, db + 2 * k4, idesc, acc);
-              if (kSwiGLU) umma_bf16(d1, da1 + 2 * k4, db + 2 * k4, idesc, acc);
+              umma_bf16(d0, a0 + 2 * k4, b0 + 2 * k4, idesc, acc);
+              if (kSwiGLU) umma_bf16(d1, a1 + 2 * k4, b1 + 2 * k4, idesc, acc);
             } else {
-              umma_f8(d0, da0 + 2 * k4, db + 2 * k4, idesc, acc);
-              if (kSwiGLU) umma_f8(d1, da1 + 2 * k4, db + 2 * k4, idesc, acc);
+              umma_f8(d0, a0 + 2 * k4, b0 + 2 * k4, idesc, acc);
+              if (kSwiGLU) umma_f8(d1, a1 + 2 * k4, b1 + 2 * k4, idesc, acc);
             }
           }
           umma_commit(empty + s);
@@ -409,21 +431,33 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       const Tile t = decode_tile(p, g.tile);
       const uint32_t a = tt % static_cast<uint32_t>(p.num_acc);
       const uint32_t aph = (tt / static_cast<uint32_t>(p.num_acc)) & 1u;
-      // column metadata of the tile, fetched while the MMAs run: lane l holds
-      // columns l, l+32, l+64, l+96 (row tiles have at most 128 columns)
+      // Tile metadata, fetched while the MMAs run.  Swap: lane l holds the
+      // pair ids / router weights of columns l, l+32, l+64, l+96 (row tiles
+      // have at most 128 columns).  Unswapped: the thread's lane is token row
+      // row_l of the tile; entry 0 holds its pair.
       int cpid[4];
       float cw[4];
+      if (kTokM) {
+        cpid[0] = row_l < t.n ? p.sorted_ids[t.row0 + row_l] : p.P;
+        cw[0] = (!kSwiGLU && cpid[0] < p.P) ? p.topk_w[cpid[0]] : 0.f;
 #pragma unroll
-      for (int s4 = 0; s4 < 4; ++s4) {
-        const int c = s4 * 32 + lane;
-        cpid[s4] = c < t.n ? p.sorted_ids[t.row0 + c] : p.P;
-        cw[s4] = (!kSwiGLU && cpid[s4] < p.P) ? p.topk_w[cpid[s4]] : 0.f;
+        for (int s4 = 1; s4 < 4; ++s4) {
+          cpid[s4] = p.P;
+          cw[s4] = 0.f;
+        }
+      } else {
+#pragma unroll
+        for (int s4 = 0; s4 < 4; ++s4) {
+          const int c = s4 * 32 + lane;
+          cpid[s4] = c < t.n ? p.sorted_ids[t.row0 + c] : p.P;
+          cw[s4] = (!kSwiGLU && cpid[s4] < p.P) ? p.topk_w[cpid[s4]] : 0.f;
+        }
       }
       const float wsc = kBF16 ? 1.f : p.w_scale[t.e];
       int got = 0;
       if (lane == 0) got = mbar_wait(tfull + a, aph, abort_flag, limit) ? 1 : 0;
       got = __shfl_sync(0xffffffffu, got, 0);
-      // all four epilogue warps take the same branch (they share named barriers below)
+      // all epilogue warps take the same branch (they share named barriers below)
       if (!named_barrier_and(kEpiBarrier, kEpiThreads, got != 0)) {
         ok = false;
         break;
@@ -432,7 +466,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       const float sc = act_s * wsc;
       const uint32_t tbase = tmem + (static_cast<uint32_t>(q * 32) << 16) +
                              a * static_cast<uint32_t>(p.acc_stride);
-      const int col = t.nb * 128 + row_l;
+      const int col = t.nb * 128 + row_l;  // swap: this lane's output row of the block
+      const int ncols = kTokM ? 128 : t.n;  // accumulator columns in use
+      // unswapped: this thread's token row, if it belongs to the tile
+      const bool row_ok = kTokM && row_l < t.n;
       if (kSwiGLU) {
         const bool whole = (k0 == 0 && k1 == K);
         bool finish = whole;
@@ -443,12 +480,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           c_first = owner_of(t0, sch.tail_total);
           c_last = owner_of(t0 + K - 1, sch.tail_total);
           float* mine = part_slot(p, blockIdx.x, t0, sch.tail_total);
-          for (int c0 = c_begin; c0 < t.n; c0 += 32) {
-            float g[16], v[16];
-            tmem_ld16x2(tbase + c0, tbase + p.bn_max + c0, g, v);
+          for (int c0 = c_begin; c0 < ncols; c0 += 32) {
+            float gg[16], v[16];
+            tmem_ld16x2(tbase + c0, tbase + p.bn_max + c0, gg, v);
 #pragma unroll
             for (int j = 0; j < 16; ++j) {
-              mine[static_cast<size_t>(c0 + j) * 128 + row_l] = g[j];
+              mine[static_cast<size_t>(c0 + j) * 128 + row_l] = gg[j];
               mine[static_cast<size_t>(p.bn_max + c0 + j) * 128 + row_l] = v[j];
             }
           }
@@ -466,10 +503,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           if (finish) __threadfence();
         }
         if (finish) {
-          for (int c0 = c_begin; c0 < t.n; c0 += 32) {
-            const int pid_c = pick4(cpid, c0 >> 5);  // column (c0 & 31) + lane of this block
-            float g[16], v[16];
-            tmem_ld16x2(tbase + c0, tbase + p.bn_max + c0, g, v);
+          for (int c0 = c_begin; c0 < ncols; c0 += 32) {
+            const int pid_c = pick4(cpid, c0 >> 5);  // swap: column (c0 & 31) + lane of this block
+            float gg[16], v[16];
+            tmem_ld16x2(tbase + c0, tbase + p.bn_max + c0, gg, v);
             if (!whole) {
               for (int c = c_first; c <= c_last; ++c) {
                 if (c == static_cast<int>(blockIdx.x) ||
@@ -478,28 +515,59 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 const float* other = part_slot(p, c, t0, sch.tail_total);
 #pragma unroll
                 for (int j = 0; j < 16; ++j) {
-                  g[j] += __ldcg(other + static_cast<size_t>(c0 + j) * 128 + row_l);
+                  gg[j] += __ldcg(other + static_cast<size_t>(c0 + j) * 128 + row_l);
                   v[j] += __ldcg(other + static_cast<size_t>(p.bn_max + c0 + j) * 128 + row_l);
                 }
               }
             }
+            float hv[16];
 #pragma unroll
             for (int j = 0; j < 16; ++j) {
-              const int r = t.row0 + c0 + j;
-              const float gv = g[j] * sc;
+              const float gv = gg[j] * sc;
               const float uv = v[j] * sc;
-              const float hv = __fdividef(gv, 1.f + __expf(-gv)) * uv;  // SiLU(g) * u
-              const size_t at = static_cast<size_t>(r) * p.ldh + col;
-              if (kBF16) {
-                // bf16 weights: h feeds the bf16 down-projection MMA directly
-                static_cast<__nv_bfloat16*>(p.h_out)[at] = __float2bfloat16_rn(hv);
-              } else {
-                // FP8: h stays fp32 until its per-tensor scale is known; an
-                // intermediate bf16 rounding would move values across E4M3
-                // rounding boundaries and cost percent-level output error
-                static_cast<float*>(p.h_out)[at] = hv;
-                const int pid = __shfl_sync(0xffffffffu, pid_c, (c0 & 31) + j);
-                if (pid < p.P) amax = fmaxf(amax, fabsf(hv));
+              hv[j] = __fdividef(gv, 1.f + __expf(-gv)) * uv;  // SiLU(g) * u
+            }
+            // bf16 weights: h feeds the bf16 down-projection MMA directly.
+            // FP8: h stays fp32 until its per-tensor scale is known; an
+            // intermediate bf16 rounding would move values across E4M3
+            // rounding boundaries and cost percent-level output error.
+            if (kTokM) {
+              if (row_ok) {
+                // 16 consecutive h values of one token row
+                const size_t at = static_cast<size_t>(t.row0 + row_l) * p.ldh + t.nb * 128 + c0;
+                if (kBF16) {
+                  uint4 o[2];
+                  uint32_t* ow = reinterpret_cast<uint32_t*>(o);
+#pragma unroll
+                  for (int j = 0; j < 8; ++j) {
+                    __nv_bfloat162 b2 = __floats2bfloat162_rn(hv[2 * j], hv[2 * j + 1]);
+                    ow[j] = *reinterpret_cast<uint32_t*>(&b2);
+                  }
+                  uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.h_out) + at);
+                  dst[0] = o[0];
+                  dst[1] = o[1];
+                } else {
+                  float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.h_out) + at);
+#pragma unroll
+                  for (int j = 0; j < 4; ++j)
+                    dst[j] = make_float4(hv[4 * j], hv[4 * j + 1], hv[4 * j + 2], hv[4 * j + 3]);
+                  if (cpid[0] < p.P) {
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) amax = fmaxf(amax, fabsf(hv[j]));
+                  }
+                }
+              }
+            } else {
+#pragma unroll
+              for (int j = 0; j < 16; ++j) {
+                const size_t at = static_cast<size_t>(t.row0 + c0 + j) * p.ldh + col;
+                if (kBF16) {
+                  static_cast<__nv_bfloat16*>(p.h_out)[at] = __float2bfloat16_rn(hv[j]);
+                } else {
+                  static_cast<float*>(p.h_out)[at] = hv[j];
+                  const int pid = __shfl_sync(0xffffffffu, pid_c, (c0 & 31) + j);
+                  if (pid < p.P) amax = fmaxf(amax, fabsf(hv[j]));
+                }
               }
             }
           }
@@ -507,17 +575,50 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       } else if (p.pair_out != nullptr) {
         // large batches: y * s * topk_weight as bf16 at the pair's row (tiles
         // are whole here, see the range split); the token sum comes after
-        for (int c0 = c_begin; c0 < t.n; c0 += 32) {
+        for (int c0 = c_begin; c0 < ncols; c0 += 32) {
           float y[16];
           tmem_ld16(tbase + c0, y);
-          const int pid_c = pick4(cpid, c0 >> 5);
-          const float w_c = sc * pick4(cw, c0 >> 5);
+          if (kTokM) {
+            // 16 consecutive output columns of this thread's pair
+            if (row_ok && cpid[0] < p.P) {
+              const float w_r = sc * cw[0];
+              uint4 o[2];
+              uint32_t* ow = reinterpret_cast<uint32_t*>(o);
 #pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            const int pj = __shfl_sync(0xffffffffu, pid_c, (c0 & 31) + j);
-            const float wj = __shfl_sync(0xffffffffu, w_c, (c0 & 31) + j);
-            if (pj < p.P)
-              p.pair_out[static_cast<size_t>(pj) * p.ldo + col] = __float2bfloat16_rn(y[j] * wj);
+              for (int j = 0; j < 8; ++j) {
+                __nv_bfloat162 b2 = __floats2bfloat162_rn(y[2 * j] * w_r, y[2 * j + 1] * w_r);
+                ow[j] = *reinterpret_cast<uint32_t*>(&b2);
+              }
+              uint4* dst = reinterpret_cast<uint4*>(
+                  p.pair_out + static_cast<size_t>(cpid[0]) * p.ldo + t.nb * 128 + c0);
+              dst[0] = o[0];
+              dst[1] = o[1];
+            }
+          } else {
+            const int pid_c = pick4(cpid, c0 >> 5);
+            const float w_c = sc * pick4(cw, c0 >> 5);
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+              const int pj = __shfl_sync(0xffffffffu, pid_c, (c0 & 31) + j);
+              const float wj = __shfl_sync(0xffffffffu, w_c, (c0 & 31) + j);
+              if (pj < p.P)
+                p.pair_out[static_cast<size_t>(pj) * p.ldo + col] = __float2bfloat16_rn(y[j] * wj);
+            }
+          }
+        }
+      } else if (kTokM) {
+        // combine, unswapped: 16 consecutive columns of this thread's token
+        // row, added with four 16-byte vector reductions
+        for (int c0 = c_begin; c0 < ncols; c0 += 32) {
+          float y[16];
+          tmem_ld16(tbase + c0, y);
+          if (row_ok && cpid[0] < p.P) {
+            const float w_r = sc * cw[0];
+            float* dst = p.acc_out + static_cast<size_t>(cpid[0] / p.top_k) * p.ldo + t.nb * 128 + c0;
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+              red_add_v4_f32(dst + 4 * j, y[4 * j] * w_r, y[4 * j + 1] * w_r, y[4 * j + 2] * w_r,
+                             y[4 * j + 3] * w_r);
           }
         }
       } else {
@@ -578,20 +679,20 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   }
 }
 
-template <bool kBF16, bool kSwiGLU>
+template <bool kBF16, bool kSwiGLU, bool kTokM>
 cudaError_t launch_one(const GemmParams& p, const CUtensorMap& ta, const CUtensorMap& tb,
                        const CUtensorMap& tb64, int grid, cudaStream_t st) {
   static thread_local int configured_device = -1;
   int dev = 0;
   cudaGetDevice(&dev);
   if (configured_device != dev) {
-    cudaError_t e = checked(cudaFuncSetAttribute(moe_gemm_kernel<kBF16, kSwiGLU>,
+    cudaError_t e = checked(cudaFuncSetAttribute(moe_gemm_kernel<kBF16, kSwiGLU, kTokM>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit), "smem attribute");
     if (e != cudaSuccess) return e;
     configured_device = dev;
   }
-  const size_t smem = gemm_smem_bytes(kSwiGLU, p.bn_max, p.stages);
-  return launch_pdl(moe_gemm_kernel<kBF16, kSwiGLU>, dim3(grid), dim3(kGemmThreads), smem, st, p,
+  const size_t smem = kSmemLimit;
+  return launch_pdl(moe_gemm_kernel<kBF16, kSwiGLU, kTokM>, dim3(grid), dim3(kGemmThreads), smem, st, p,
                     ta, tb, tb64);
 }
 
@@ -600,28 +701,25 @@ cudaError_t launch_one(const GemmParams& p, const CUtensorMap& ta, const CUtenso
 // Combine staging of the down projection: per epilogue warp 2 buffers x 16 x 32 fp32.
 constexpr size_t kCombineStaging = kGemmEpiWarps * 2 * 16 * 32 * sizeof(float);
 
-size_t gemm_smem_bytes(bool swiglu, int bn_max, int stages) {
-  const size_t stage = (swiglu ? 32768u : 16384u) + static_cast<size_t>(bn_max) * 128u;
-  return stage * stages + kSmemSlack + (swiglu ? 0 : kCombineStaging);
+size_t gemm_stage_smem(bool swiglu) {
+  return kSmemLimit - kSmemSlack - (swiglu ? 0 : kCombineStaging);
 }
 
-int gemm_max_stages(bool swiglu, int bn_max) {
-  const size_t stage = (swiglu ? 32768u : 16384u) + static_cast<size_t>(bn_max) * 128u;
-  const size_t avail = kSmemLimit - kSmemSlack - (swiglu ? 0 : kCombineStaging);
-  int s = static_cast<int>(avail / stage);
-  if (s > kMaxStages) s = kMaxStages;
-  return s;
-}
-
-cudaError_t launch_gemm(bool bf16, bool swiglu, const GemmParams& p, const CUtensorMap& ta,
-                        const CUtensorMap& tb, const CUtensorMap& tb64, int grid,
-                        cudaStream_t st) {
-  if (bf16) {
-    return swiglu ? launch_one<true, true>(p, ta, tb, tb64, grid, st)
-                  : launch_one<true, false>(p, ta, tb, tb64, grid, st);
+cudaError_t launch_gemm(bool bf16, bool swiglu, bool tok_m, const GemmParams& p,
+                        const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tb64,
+                        int grid, cudaStream_t st) {
+  if (tok_m) {
+    if (bf16)
+      return swiglu ? launch_one<true, true, true>(p, ta, tb, tb64, grid, st)
+                    : launch_one<true, false, true>(p, ta, tb, tb64, grid, st);
+    return swiglu ? launch_one<false, true, true>(p, ta, tb, tb64, grid, st)
+                  : launch_one<false, false, true>(p, ta, tb, tb64, grid, st);
   }
-  return swiglu ? launch_one<false, true>(p, ta, tb, tb64, grid, st)
-                : launch_one<false, false>(p, ta, tb, tb64, grid, st);
+  if (bf16)
+    return swiglu ? launch_one<true, true, false>(p, ta, tb, tb64, grid, st)
+                  : launch_one<true, false, false>(p, ta, tb, tb64, grid, st);
+  return swiglu ? launch_one<false, true, false>(p, ta, tb, tb64, grid, st)
+                : launch_one<false, false, false>(p, ta, tb, tb64, grid, st);
 }
 
 }  // namespace moe

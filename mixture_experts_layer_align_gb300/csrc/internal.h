@@ -57,7 +57,8 @@ struct Ctrl {
   float s_h;        // activation scale of h
   int num_padded;   // rows of the aligned (sorted, padded) pair list
   int num_mtiles;   // entries of the GEMM row-tile list
-  int pad[10];
+  int max_tile_rows;  // rows of the largest row tile
+  int pad[9];
 };
 static_assert(sizeof(Ctrl) == 64, "Ctrl layout");
 
@@ -147,7 +148,7 @@ struct GemmParams {
   int k_steps;          // K / (128 bytes of K)
   int k_elems;          // elements of K per step: 128 (E4M3) or 64 (bf16)
   int bn_max;           // max tokens (MMA N) per row tile
-  int stages;           // shared-memory pipeline depth
+  unsigned stage_smem;  // shared-memory bytes for the pipeline stages
   int acc_stride;       // TMEM columns per accumulator buffer
   int num_acc;          // accumulator buffers (1 or 2)
   int tmem_cols;        // allocated TMEM columns (power of two >= 32)
@@ -188,11 +189,15 @@ __host__ __device__ inline size_t gemm_part_slot_floats(int bn_max) { return sta
 // quarter, each taking every other 16-column chunk of a tile)
 constexpr int kGemmEpiWarps = 8;
 constexpr int kGemmThreads = 64 + 32 * kGemmEpiWarps;
-size_t gemm_smem_bytes(bool swiglu, int bn_max, int stages);
-int gemm_max_stages(bool swiglu, int bn_max);
-// tmb / tmb64: the token operand with 16-row and 64-row boxes.
-cudaError_t launch_gemm(bool bf16, bool swiglu, const GemmParams& p, const CUtensorMap& tma,
-                        const CUtensorMap& tmb, const CUtensorMap& tmb64, int grid,
-                        cudaStream_t st);
+// Shared-memory bytes left for the pipeline stages (the kernel picks its
+// depth from the largest row tile of the call).
+size_t gemm_stage_smem(bool swiglu);
+// tmb / tmb64: the token operand with 16-row and 64-row boxes.  tok_m: tokens
+// in the MMA M slot (the unswapped placement; row tiles of up to 128 rows).
+cudaError_t launch_gemm(bool bf16, bool swiglu, bool tok_m, const GemmParams& p,
+                        const CUtensorMap& tma, const CUtensorMap& tmb, const CUtensorMap& tmb64,
+                        int grid, cudaStream_t st);
+// Row-tile width of the unswapped placement (the token tile fills M = 128).
+constexpr int kTokMRows = 128;
 
 }  // namespace moe

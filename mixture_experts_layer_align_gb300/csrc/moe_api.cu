@@ -79,18 +79,13 @@ bool make_tmap(CUtensorMap* m, const void* base, bool bf16, uint64_t k_elems, ui
   return r == CUDA_SUCCESS;
 }
 
-int round_up16(long long v) { return static_cast<int>((v + 15) / 16 * 16); }
-
-// Row-tile width (MMA N) of the expert GEMMs: twice the mean rows per touched
-// expert, 64..128.  Any value is correct; wider tiles re-read each weight
-// block fewer times, narrower ones leave more stages of weights in flight;
-// up to 128 the gate/up accumulators (2 x N columns) are double-buffered in
-// the 512 TMEM columns.
-int choose_bn_max(long long P, int E) {
-  const long long touched = std::min<long long>(E, P);
-  const long long mean_rows = touched > 0 ? (P + touched - 1) / touched : 1;
-  return std::min(128, std::max(64, round_up16(2 * mean_rows)));
-}
+// Row-tile width of the expert GEMMs: 128 rows, the widest tile whose gate/up
+// accumulators (2 x 128 columns) are still double-buffered in the 512 TMEM
+// columns.  The routing is not known when the launch is planned, and a
+// narrower tile would split a busy expert's rows and read its weight blocks
+// once per piece (skewed routing); the weight-in-M placement only loads the
+// rows a tile has, so the width costs decode nothing but shared memory.
+int choose_bn_max(long long, int) { return kTokMRows; }
 
 // CTAs the persistent GEMMs may use on the current device (also sizes the
 // split-tile partial slots); 256 when no device can be queried.
@@ -149,7 +144,8 @@ Layout make_layout(int T, int H, int I, int E, int k, bool fp8) {
   L.sorted = take(sizeof(int32_t) * L.pad_max);
   L.mtiles = take(sizeof(int4) * L.max_mtiles);
   L.tile_cnt = take(sizeof(int) * static_cast<size_t>(L.n_tile_cnt));
-  L.part = take(sizeof(float) * 2 * static_cast<size_t>(L.ctas) * gemm_part_slot_floats(L.bn_max));
+  // sized for the widest row tile (the unswapped placement uses 128 rows)
+  L.part = take(sizeof(float) * 2 * static_cast<size_t>(L.ctas) * gemm_part_slot_floats(kTokMRows));
   L.xs = take(static_cast<size_t>(L.pad_max) * H * (fp8 ? 1 : 2));
   L.h = take(static_cast<size_t>(L.pad_max) * I * (fp8 ? 4 : 2));
   L.hq = take(fp8 ? static_cast<size_t>(L.pad_max) * I : 0);
@@ -308,6 +304,8 @@ moe_status_t fused_forward_impl(const moe_fused_args* a, void* workspace, size_t
     return MOE_ERR_INVALID_ARG;
   if (a->weight_dtype != MOE_DT_BF16 && a->weight_dtype != MOE_DT_FP8_E4M3)
     return MOE_ERR_INVALID_ARG;
+  if ((a->debug_flags & MOE_FLAG_TOKENS_IN_M) && (a->debug_flags & MOE_FLAG_WEIGHTS_IN_M))
+    return MOE_ERR_INVALID_ARG;
   const bool fp8 = a->weight_dtype == MOE_DT_FP8_E4M3;
   if (fp8 && (!a->w13_scale || !a->w2_scale)) return MOE_ERR_INVALID_ARG;
   if (!fp8 && (a->w13_scale || a->w2_scale)) return MOE_ERR_INVALID_ARG;
@@ -346,6 +344,15 @@ moe_status_t fused_forward_impl(const moe_fused_args* a, void* workspace, size_t
   const long long acc_elems = L.combine_rows ? 0 : static_cast<long long>(T) * H;
 
   const long long touched = std::min<long long>(E, P);
+  // Operand placement.  Gate/up: the weight block in M (the swap).  Down:
+  // the weight block in M when K = I is long; with short K (I <= 2048) the
+  // MMA time per tile is small and the token-in-M epilogue, which writes 16
+  // consecutive outputs of one token per thread, is the cheaper one.  The two
+  // flags force one placement on both GEMMs (ablation of the swap).
+  const bool force_tok = (a->debug_flags & MOE_FLAG_TOKENS_IN_M) != 0;
+  const bool force_w = (a->debug_flags & MOE_FLAG_WEIGHTS_IN_M) != 0;
+  const bool tok_m1 = force_tok;
+  const bool tok_m2 = force_tok || (!force_w && I / 128 <= 16);
   const int bn_max = L.bn_max;
   int* tile_cnt = reinterpret_cast<int*>(ws + L.tile_cnt);
   float* part = reinterpret_cast<float*>(ws + L.part);
@@ -444,7 +451,7 @@ moe_status_t fused_forward_impl(const moe_fused_args* a, void* workspace, size_t
   g1.k_steps = H / k_elems;
   g1.k_elems = k_elems;
   g1.bn_max = bn_max;
-  g1.stages = gemm_max_stages(true, bn_max);
+  g1.stage_smem = static_cast<unsigned>(gemm_stage_smem(true));
   g1.acc_stride = 2 * bn_max;
   g1.num_acc = (4 * bn_max <= 512) ? 2 : 1;
   g1.tmem_cols = next_pow2(g1.acc_stride * g1.num_acc);
@@ -471,7 +478,7 @@ moe_status_t fused_forward_impl(const moe_fused_args* a, void* workspace, size_t
   const long long work1 = max_tiles * g1.nb_count * g1.k_steps;
   const int grid1 = static_cast<int>(std::max<long long>(1, std::min<long long>(ctas, work1)));
   if (events && cudaEventRecord(events[3], stream) != cudaSuccess) return MOE_ERR_CUDA;
-  if (launch_gemm(bf16, true, g1, tm_w13, tm_xs, tm_xs64, grid1, s) != cudaSuccess)
+  if (launch_gemm(bf16, true, tok_m1, g1, tm_w13, tm_xs, tm_xs64, grid1, s) != cudaSuccess)
     return MOE_ERR_CUDA;
 
   // 5. dynamic scale of h and its E4M3 codes
@@ -486,7 +493,7 @@ moe_status_t fused_forward_impl(const moe_fused_args* a, void* workspace, size_t
   GemmParams g2 = g1;
   g2.nb_count = H / 128;
   g2.k_steps = I / k_elems;
-  g2.stages = gemm_max_stages(false, bn_max);
+  g2.stage_smem = static_cast<unsigned>(gemm_stage_smem(false));
   g2.acc_stride = bn_max;
   g2.num_acc = 2;
   g2.tmem_cols = next_pow2(2 * bn_max);
@@ -503,7 +510,7 @@ moe_status_t fused_forward_impl(const moe_fused_args* a, void* workspace, size_t
   g2.trace = (a->debug_flags & MOE_DEBUG_TRACE) ? trace + MOE_TRACE_MAX_CTAS * 4 : nullptr;
   const long long work2 = max_tiles * g2.nb_count * g2.k_steps;
   const int grid2 = static_cast<int>(std::max<long long>(1, std::min<long long>(ctas, work2)));
-  if (launch_gemm(bf16, false, g2, tm_w2, tm_h, tm_h64, grid2, s) != cudaSuccess)
+  if (launch_gemm(bf16, false, tok_m2, g2, tm_w2, tm_h, tm_h64, grid2, s) != cudaSuccess)
     return MOE_ERR_CUDA;
 
   // 7. fp32 combine buffer -> bf16 output, or the sum of each token's k rows

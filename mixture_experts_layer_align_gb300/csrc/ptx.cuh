@@ -288,6 +288,13 @@ __device__ __forceinline__ void bulk_reduce_add_f32(float* dst, const float* src
                : "memory");
 }
 
+// Four consecutive fp32 adds at a 16-byte aligned global address.
+__device__ __forceinline__ void red_add_v4_f32(float* dst, float a, float b, float c, float d) {
+  asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(dst), "f"(a), "f"(b), "f"(c),
+               "f"(d)
+               : "memory");
+}
+
 __device__ __forceinline__ void bulk_commit() {
   asm volatile("cp.async.bulk.commit_group;" ::: "memory");
 }

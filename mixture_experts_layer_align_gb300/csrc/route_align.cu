@@ -198,6 +198,9 @@ __global__ void __launch_bounds__(kRouteWarps * 32)
 }
 
 // ------------------------------------------------------------------ align
+__device__ int2 write_mtiles(int tid, int E, int padded, int seg_off, int bm, int bn_max,
+                             int4* __restrict__ mtiles, int* s_tmp);
+
 // Stable counting sort of the T*k (token, slot) pairs by expert, padded per
 // expert to a multiple of bm.  Each CTA owns one chunk of pair ids; it counts
 // all pairs (to get the global offsets) and the pairs before its chunk (to
@@ -341,20 +344,9 @@ __global__ void __launch_bounds__(kAlignThreads) align_kernel(AlignParams p) {
   }
 
   if (p.mtiles != nullptr) {
-    // GEMM row tiles: each expert's padded segment split into
-    // ceil(padded / bn_max) tiles of equal size (multiples of bm); each entry
-    // also carries the expert's tile count and first tile index
-    const int nt = padded > 0 ? (padded + p.bn_max - 1) / p.bn_max : 0;
-    int n_tiles = 0;
-    const int first = block_exclusive_scan_1024(nt, s_tmp, &n_tiles);
-    if (nt > 0) {
-      const int per = ((padded + nt - 1) / nt + p.bm - 1) / p.bm * p.bm;
-      const int o = seg_off[tid];
-      for (int j = 0; j < nt; ++j) {
-        const int rows = min(per, padded - j * per);
-        p.mtiles[first + j] = make_int4(tid, o + j * per, rows | (nt << 12), first);
-      }
-    }
+    // GEMM row tiles
+    const int2 tl = write_mtiles(tid, p.E, padded, tid < p.E ? seg_off[tid] : 0, p.bm, p.bn_max,
+                                 p.mtiles, s_tmp);
     // activation scale of x from the router's per-CTA amax values
     float m = 0.f;
     for (int i = tid; i < p.n_partials; i += kAlignThreads) m = fmaxf(m, p.amax_partials[i]);
@@ -365,7 +357,8 @@ __global__ void __launch_bounds__(kAlignThreads) align_kernel(AlignParams p) {
       float a = 0.f;
       for (int w = 0; w < 32; ++w) a = fmaxf(a, s_red[w]);
       p.ctrl->s_x = p.amax_partials ? scale_from_amax(a) : 1.f;
-      p.ctrl->num_mtiles = n_tiles;
+      p.ctrl->num_mtiles = tl.x;
+      p.ctrl->max_tile_rows = tl.y;
     }
   }
 }
@@ -374,20 +367,25 @@ __global__ void __launch_bounds__(kAlignThreads) align_kernel(AlignParams p) {
 // expert per thread, tid < E; all 1024 threads of the block must call).
 // Each expert's segment is split into ceil(padded / bn_max) equal tiles
 // (multiples of bm); every entry also carries the expert's tile count and the
-// index of its first tile.  Returns the number of tiles.
-__device__ int write_mtiles(int tid, int E, int padded, int seg_off, int bm, int bn_max,
-                            int4* __restrict__ mtiles, int* s_tmp) {
+// index of its first tile.  Returns {number of tiles, rows of the largest}.
+__device__ int2 write_mtiles(int tid, int E, int padded, int seg_off, int bm, int bn_max,
+                             int4* __restrict__ mtiles, int* s_tmp) {
   const int nt = (tid < E && padded > 0) ? (padded + bn_max - 1) / bn_max : 0;
+  const int per = nt > 0 ? ((padded + nt - 1) / nt + bm - 1) / bm * bm : 0;
   int n_tiles = 0;
   const int first = block_exclusive_scan_1024(nt, s_tmp, &n_tiles);
-  if (nt > 0) {
-    const int per = ((padded + nt - 1) / nt + bm - 1) / bm * bm;
-    for (int j = 0; j < nt; ++j) {
-      const int rows = min(per, padded - j * per);
-      mtiles[first + j] = make_int4(tid, seg_off + j * per, rows | (nt << 12), first);
-    }
+  for (int j = 0; j < nt; ++j) {
+    const int rows = min(per, padded - j * per);
+    mtiles[first + j] = make_int4(tid, seg_off + j * per, rows | (nt << 12), first);
   }
-  return n_tiles;
+  // the largest tile is some expert's first one
+  const int wmax = static_cast<int>(__reduce_max_sync(kFull, static_cast<unsigned>(per)));
+  if ((threadIdx.x & 31) == 0) s_tmp[threadIdx.x >> 5] = wmax;
+  __syncthreads();
+  int mx = 0;
+  for (int w = 0; w < 32; ++w) mx = max(mx, s_tmp[w]);
+  __syncthreads();
+  return make_int2(n_tiles, mx);
 }
 
 // Small batches (decode): one CTA routes every token, takes amax |x|, aligns
@@ -482,13 +480,14 @@ __global__ void __launch_bounds__(kAlignThreads, 1) route_align_small_kernel(Sma
     p.ids[q] = s_ids[q];
     p.wts[q] = s_w[q];
   }
-  const int n_tiles = write_mtiles(tid, E, padded, off, kAlignBlock, p.bn_max, p.mtiles, s_tmp);
+  const int2 tl = write_mtiles(tid, E, padded, off, kAlignBlock, p.bn_max, p.mtiles, s_tmp);
   if (tid == 0) {
     float a = 0.f;
     for (int w = 0; w < 32; ++w) a = fmaxf(a, s_red[w]);
     p.offsets[E] = total;
     ctrl->num_padded = total;
-    ctrl->num_mtiles = n_tiles;
+    ctrl->num_mtiles = tl.x;
+    ctrl->max_tile_rows = tl.y;
     ctrl->s_x = p.x != nullptr ? scale_from_amax(a) : 1.f;
   }
 }
@@ -543,9 +542,12 @@ __global__ void __launch_bounds__(256)
 }
 
 // ------------------------------------------------------------------ gather
-// One thread per 16 elements of an aligned row: the pair's token row of x,
-// quantised to E4M3 with s_x (or copied as bf16); padding rows are zero.  The
-// same grid zeroes the fp32 combine buffer.
+// The pair's token row of x for every aligned row -- E4M3 codes made per
+// token (large batches: copied), quantised here with s_x (small batches), or
+// bf16 -- and zero for padding rows.  Copies go one warp per row, with the
+// next row's pair id fetched while the current row moves; quantisation goes
+// one thread per 16 elements, so a few long rows still spread over the whole
+// grid.  The same grid zeroes the fp32 combine buffer.
 __global__ void __launch_bounds__(256)
     gather_x_kernel(const __nv_bfloat16* __restrict__ x, const uint8_t* __restrict__ xq_tok, int H,
                     const int32_t* __restrict__ sorted_ids, const Ctrl* __restrict__ ctrl, int P,
@@ -554,50 +556,51 @@ __global__ void __launch_bounds__(256)
   pdl_wait();
   pdl_trigger();
   const long long rows = ctrl->num_padded;
-  const int per_row = H / 16;
-  const long long n = rows * per_row;
-  const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
   const long long tid = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
+  const uint4 zero = make_uint4(0, 0, 0, 0);
   if (fp8 && xq_tok != nullptr) {
-    // codes already made per token: copy 16 bytes
-    uint4* dst = static_cast<uint4*>(xs);
-    const uint4* codes = reinterpret_cast<const uint4*>(xq_tok);
-    for (long long i = tid; i < n; i += stride) {
-      const long long r = i / per_row;
-      const int c = static_cast<int>(i - r * per_row);
-      const int q = sorted_ids[r];
-      dst[i] = q < P ? codes[static_cast<size_t>(q / k) * per_row + c] : make_uint4(0, 0, 0, 0);
+    const int lane = threadIdx.x & 31;
+    const long long nwarps = stride >> 5;
+    const long long w0 = tid >> 5;
+    const int n16 = H / 16;  // 16 codes per uint4
+    int q_next = w0 < rows ? sorted_ids[w0] : P;
+    for (long long r = w0; r < rows; r += nwarps) {
+      const int q = q_next;
+      q_next = r + nwarps < rows ? sorted_ids[r + nwarps] : P;
+      uint4* dst = static_cast<uint4*>(xs) + r * n16;
+      const uint4* src = reinterpret_cast<const uint4*>(xq_tok) + static_cast<size_t>(q / k) * n16;
+#pragma unroll 4
+      for (int c = lane; c < n16; c += 32) dst[c] = q < P ? src[c] : zero;
     }
   } else if (fp8) {
-    const float s = ctrl->s_x;
+    const float sx = ctrl->s_x;
+    const int per_row = H / 16;
+    const long long n = rows * per_row;
     uint4* dst = static_cast<uint4*>(xs);
     for (long long i = tid; i < n; i += stride) {
       const long long r = i / per_row;
       const int c = static_cast<int>(i - r * per_row);
       const int q = sorted_ids[r];
-      uint4 v = make_uint4(0, 0, 0, 0);
+      uint4 v = zero;
       if (q < P) {
         const uint4* src = reinterpret_cast<const uint4*>(x + static_cast<size_t>(q / k) * H);
-        const uint2 a = quant8(__ldg(src + 2 * c), s);
-        const uint2 b = quant8(__ldg(src + 2 * c + 1), s);
-        v = make_uint4(a.x, a.y, b.x, b.y);
+        const uint2 lo = quant8(__ldg(src + 2 * c), sx);
+        const uint2 hi = quant8(__ldg(src + 2 * c + 1), sx);
+        v = make_uint4(lo.x, lo.y, hi.x, hi.y);
       }
       dst[i] = v;
     }
   } else {
+    const int per_row = H / 8;  // 8 bf16 per uint4
+    const long long n = rows * per_row;
     uint4* dst = static_cast<uint4*>(xs);
     for (long long i = tid; i < n; i += stride) {
       const long long r = i / per_row;
       const int c = static_cast<int>(i - r * per_row);
       const int q = sorted_ids[r];
-      uint4 v0 = make_uint4(0, 0, 0, 0), v1 = v0;
-      if (q < P) {
-        const uint4* src = reinterpret_cast<const uint4*>(x + static_cast<size_t>(q / k) * H);
-        v0 = __ldg(src + 2 * c);
-        v1 = __ldg(src + 2 * c + 1);
-      }
-      dst[2 * i] = v0;
-      dst[2 * i + 1] = v1;
+      dst[i] = q < P ? __ldg(reinterpret_cast<const uint4*>(x + static_cast<size_t>(q / k) * H) + c)
+                     : zero;
     }
   }
   float4* a4 = reinterpret_cast<float4*>(acc);
@@ -784,7 +787,9 @@ cudaError_t launch_gather_x(const __nv_bfloat16* x, const uint8_t* xq_tok, int H
                             const int32_t* sorted_ids, const Ctrl* ctrl, int P, int k, void* xs,
                             bool fp8, float* acc, long long acc_elems, int max_rows, int num_sms,
                             cudaStream_t st) {
-  const long long work = std::max(static_cast<long long>(max_rows) * (H / 16), acc_elems / 4);
+  // copies: a warp per row; quantisation: a thread per 16 elements
+  const long long per_row = xq_tok != nullptr ? 32 : (fp8 ? H / 16 : H / 8);
+  const long long work = std::max(static_cast<long long>(max_rows) * per_row, acc_elems / 4);
   const int grid = capped_grid(work, 256, num_sms, 8);
   return launch_pdl(gather_x_kernel, dim3(grid), dim3(256), 0, st, x, xq_tok, H, sorted_ids, ctrl,
                     P, k, xs, fp8 ? 1 : 0, acc, acc_elems);

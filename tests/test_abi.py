@@ -80,7 +80,7 @@ def _args(**kw):
     (dict(top_k=9), 1), (dict(top_k=0), 1), (dict(E=0), 1), (dict(E=1025, top_k=2), 1),
     (dict(T=-1), 1), (dict(H=100), 2), (dict(I=200), 2), (dict(w13_scale=None), 1),
     (dict(weight_dtype=0), 1), (dict(weight_dtype=7), 1), (dict(x=None), 1),
-    (dict(x=17), 1), (dict(out=24), 1),
+    (dict(x=17), 1), (dict(out=24), 1), (dict(debug_flags=0x4 | 0x8), 1),
 ])
 def test_fused_forward_rejects_bad_arguments(lib, kw, code):
     a = _args(**kw)

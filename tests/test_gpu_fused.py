@@ -17,7 +17,7 @@ from mixture_experts_layer_align_gb300 import inputs
 pytestmark = pytest.mark.gpu
 
 
-def run_case(moe, w, a, top_k, renorm, rows=None, repeat=1):
+def run_case(moe, w, a, top_k, renorm, rows=None, repeat=1, flags=0):
     dev = "cuda"
     T, E = a.T, w.E
     x, lg = a.x.to(dev), a.logits.to(dev)
@@ -31,7 +31,8 @@ def run_case(moe, w, a, top_k, renorm, rows=None, repeat=1):
     ws.fill_(0xAB)  # the call must not rely on a zeroed workspace
     for _ in range(repeat):
         out = moe.moe_fused_forward(x, lg, w13, w2, s13, s2, top_k, renorm, workspace=ws,
-                                    topk_ids_out=ids, topk_w_out=wts, counts_out=counts)
+                                    topk_ids_out=ids, topk_w_out=wts, counts_out=counts,
+                                    debug_flags=flags)
     assert moe.moe_check_status(ws) == 0
     ref = oracle.moe_forward(a.x, a.logits, w.w13.cpu(), w.w2.cpu(),
                              None if w.w13_scale is None else w.w13_scale.cpu(),
@@ -56,20 +57,48 @@ def run_case(moe, w, a, top_k, renorm, rows=None, repeat=1):
     (600, 256, 128, 4, 2, True, "fp8"),     # >256 rows per expert: split tiles
     (130, 1024, 512, 64, 8, True, "fp8"),
 ])
-def test_fused_small(gpu_lib, T, H, I, E, k, renorm, dtype):
+@pytest.mark.parametrize("placement", ["auto", "weights_in_m"])
+def test_fused_small(gpu_lib, T, H, I, E, k, renorm, dtype, placement):
     w = inputs.make_weights(H, I, E, dtype, seed=T)
     a = inputs.make_activations(T, H, E, "uniform", seed=T)
-    run_case(gpu_lib, w, a, k, renorm, repeat=2)
+    flags = gpu_lib.MOE_FLAG_WEIGHTS_IN_M if placement == "weights_in_m" else 0
+    run_case(gpu_lib, w, a, k, renorm, repeat=2, flags=flags)
 
 
 @pytest.mark.parametrize("T,H,I,E,k", [
     (2600, 256, 128, 16, 2),    # > 4096 pairs: two-pass alignment, tokens quantised once
     (2048, 1024, 128, 32, 8),   # pairs x H > 8M: combine through per-pair rows
 ])
-def test_fused_large_batch_paths(gpu_lib, T, H, I, E, k):
+@pytest.mark.parametrize("placement", ["auto", "weights_in_m"])
+def test_fused_large_batch_paths(gpu_lib, T, H, I, E, k, placement):
     w = inputs.make_weights(H, I, E, "fp8", seed=T)
     a = inputs.make_activations(T, H, E, "zipf", seed=T)
-    run_case(gpu_lib, w, a, k, True, rows=sample_rows(T, 64, seed=3))
+    flags = gpu_lib.MOE_FLAG_WEIGHTS_IN_M if placement == "weights_in_m" else 0
+    run_case(gpu_lib, w, a, k, True, rows=sample_rows(T, 64, seed=3), flags=flags)
+
+
+# The unswapped placement (tokens in the MMA M slot, weight rows in N): the
+# ablation of the operand swap must compute the same layer.
+@pytest.mark.parametrize("T,H,I,E,k,renorm,dtype", [
+    (4, 128, 256, 8, 2, True, "bf16"),
+    (37, 256, 384, 8, 2, True, "fp8"),
+    (200, 512, 256, 16, 4, False, "fp8"),
+    (600, 256, 128, 4, 2, True, "fp8"),     # several 128-row tiles per expert
+    (130, 1024, 512, 64, 8, True, "fp8"),
+    (9, 128, 128, 1, 1, False, "bf16"),
+])
+def test_fused_tokens_in_m(gpu_lib, T, H, I, E, k, renorm, dtype):
+    w = inputs.make_weights(H, I, E, dtype, seed=T)
+    a = inputs.make_activations(T, H, E, "uniform", seed=T)
+    run_case(gpu_lib, w, a, k, renorm, repeat=2, flags=gpu_lib.MOE_FLAG_TOKENS_IN_M)
+
+
+@pytest.mark.parametrize("T,H,I,E,k", [(2600, 256, 128, 16, 2), (2048, 1024, 128, 32, 8)])
+def test_fused_tokens_in_m_large_batch_paths(gpu_lib, T, H, I, E, k):
+    w = inputs.make_weights(H, I, E, "fp8", seed=T)
+    a = inputs.make_activations(T, H, E, "zipf", seed=T)
+    run_case(gpu_lib, w, a, k, True, rows=sample_rows(T, 64, seed=3),
+             flags=gpu_lib.MOE_FLAG_TOKENS_IN_M)
 
 
 def test_fused_zipf_skew(gpu_lib):
@@ -126,6 +155,16 @@ def test_fused_full_size(gpu_lib, name, T):
     a = inputs.make_activations(T, c["H"], c["E"], c["routing"], seed=0, device="cuda")
     rows = sample_rows(T, 24, seed=T)
     run_case(gpu_lib, w, a, c["top_k"], True, rows=rows)
+
+
+@pytest.mark.parametrize("name,T", [("decode_e8_top2", 1), ("decode_e8_top2", 64),
+                                    ("finegrained_e128", 16), ("prefill_e128_uniform", 2048)])
+def test_fused_full_size_tokens_in_m(gpu_lib, name, T):
+    c = inputs.workload(name)
+    w = _weights(name)
+    a = inputs.make_activations(T, c["H"], c["E"], c["routing"], seed=0, device="cuda")
+    run_case(gpu_lib, w, a, c["top_k"], True, rows=sample_rows(T, 24, seed=T),
+             flags=gpu_lib.MOE_FLAG_TOKENS_IN_M)
 
 
 @pytest.mark.slow
