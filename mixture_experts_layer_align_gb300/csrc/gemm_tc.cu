@@ -50,6 +50,10 @@ namespace {
 constexpr int kSmemLimit = 232448;  // 227 KB opt-in per CTA
 constexpr int kSmemSlack = 1024 + 256;
 constexpr int kMaxStages = 12;  // 2 * 12 + 5 barriers + 3 words fit the 256-byte area
+// Gate/up stages (32 KB of weights each) beyond 4 were measured to slow the
+// decode weight stream: more requests in flight per SM than HBM rewards.
+constexpr int kMaxStagesGateUp = 4;
+constexpr int kMaxStagesDown = 12;
 constexpr uint32_t kEpiBarrier = 1;  // named barrier of the 4 epilogue warps
 constexpr uint32_t kEpiThreads = 32 * kGemmEpiWarps;
 
@@ -210,7 +214,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   constexpr uint32_t kABytes = kSwiGLU ? 32768u : 16384u;
   const int rows_b = kTokM ? 128 : min(p.bn_max, max(16, p.ctrl->max_tile_rows));
   const uint32_t stage_bytes = kABytes + static_cast<uint32_t>(rows_b) * 128u;
-  const int S = min(kMaxStages, static_cast<int>(p.stage_smem / stage_bytes));
+  const int S = min(kSwiGLU ? kMaxStagesGateUp : kMaxStagesDown,
+                    static_cast<int>(p.stage_smem / stage_bytes));
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + static_cast<size_t>(S) * stage_bytes);
   uint64_t* empty = full + S;
   uint64_t* tfull = empty + S;
