@@ -61,24 +61,43 @@ struct Tile {
   int e, row0, n, nb;
 };
 
-// Tile u -> (expert, first row, rows, weight block).  Tiles of one expert with
-// m row tiles occupy [first * nb_count, (first + m) * nb_count) and are ordered
-// (weight block, row tile), so u / nb_count always lands on a row tile of the
-// same expert.
+// Tile u -> (expert, first row, rows, weight block): row tile u / nb_count
+// (one load of the tile list), weight block u % nb_count.  A row tile's
+// weight blocks are consecutive tiles, and an expert's row tiles follow one
+// another, so the G tiles in flight share token rows and weight blocks.
 __device__ __forceinline__ Tile decode_tile(const GemmParams& p, int u) {
-  const int4 a = p.mtiles[u / p.nb_count];
-  const int m = a.z >> 12;
-  const int first = a.w;
-  const int local = u - first * p.nb_count;
-  const int nb = local / m;
-  const int j = local - nb * m;
-  const int4 t = p.mtiles[first + j];
+  const int m = u / p.nb_count;
+  const int4 t = p.mtiles[m];
   Tile r;
   r.e = t.x;
   r.row0 = t.y;
   r.n = t.z & 0xfff;
-  r.nb = nb;
+  r.nb = u - m * p.nb_count;
   return r;
+}
+
+// Epilogue metadata of a tile.  Swap: lane l holds the pair ids and router
+// weights of columns l, l+32, l+64, l+96 (row tiles have at most 128
+// columns).  Unswapped: the thread's lane is token row row_l of the tile and
+// entry 0 holds it.  wsc: the expert's weight scale.
+struct Meta {
+  int pid[4];
+  float w[4];
+  float wsc;
+};
+
+template <bool kBF16, bool kSwiGLU, bool kTokM>
+__device__ __forceinline__ Meta load_meta(const GemmParams& p, const Tile& t, int lane, int row_l) {
+  Meta m;
+#pragma unroll
+  for (int s4 = 0; s4 < 4; ++s4) {
+    const int c = kTokM ? row_l : s4 * 32 + lane;
+    const bool in = (kTokM ? s4 == 0 : true) && c < t.n;
+    m.pid[s4] = in ? p.sorted_ids[t.row0 + c] : p.P;
+    m.w[s4] = (!kSwiGLU && in) ? p.sorted_w[t.row0 + c] : 0.f;
+  }
+  m.wsc = kBF16 ? 1.f : p.w_scale[t.e];
+  return m;
 }
 
 // Order in which the flat index space visits tiles: the tiles are laid out
@@ -198,8 +217,10 @@ __device__ __forceinline__ V pick4(const V (&v)[4], int s) {
 // kTokM selects the unswapped placement (the ablation of the operand swap):
 // the 128-row token tile is the A operand in the M slot and the weight block
 // is B with N = 128 weight rows; lanes then hold tokens and TMEM columns hold
-// weight rows.
-template <bool kBF16, bool kSwiGLU, bool kTokM>
+// weight rows.  kPair (down projection, unswapped): a tile covers two
+// consecutive 128-row weight blocks against one token tile, two MMAs into two
+// accumulators like gate and up, so the token bytes serve twice the FLOPs.
+template <bool kBF16, bool kSwiGLU, bool kTokM, bool kPair>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     moe_gemm_kernel(const __grid_constant__ GemmParams p, const __grid_constant__ CUtensorMap tm_a,
                     const __grid_constant__ CUtensorMap tm_b,
@@ -211,7 +232,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   // alignment kernel two or more launches back, see below): a stage holds the
   // weight block(s) and that many token rows, and as many stages as fit are
   // used, so decode (tiles of a few rows) keeps more weight bytes in flight.
-  constexpr uint32_t kABytes = kSwiGLU ? 32768u : 16384u;
+  constexpr bool kTwoB = kSwiGLU || kPair;  // two weight blocks per stage
+  constexpr uint32_t kABytes = kTwoB ? 32768u : 16384u;
   const int rows_b = kTokM ? 128 : min(p.bn_max, max(16, p.ctrl->max_tile_rows));
   const uint32_t stage_bytes = kABytes + static_cast<uint32_t>(rows_b) * 128u;
   const int S = min(kSwiGLU ? kMaxStagesGateUp : kMaxStagesDown,
@@ -297,13 +319,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         Seg gj;
         while (pre < static_cast<uint32_t>(S) && seg_next(sch, sj, gj)) {
           const Tile t = decode_tile(p, gj.tile);
-          const int wrow = t.e * p.rows_per_expert + t.nb * 128;
+          const int wrow = t.e * p.rows_per_expert + t.nb * p.wblock_rows;
           for (int kk = gj.k0; kk < gj.k1 && pre < static_cast<uint32_t>(S); ++kk, ++pre) {
             uint8_t* sa = smem + static_cast<size_t>(pre) * stage_bytes;
             mbar_arrive_expect_tx(full + pre, kABytes + static_cast<uint32_t>(kTokM ? 128 : t.n) * 128u);
             const int kc = kk * p.k_elems;
             tma_load_2d_hint(sa, &tm_a, full + pre, kc, wrow, pol_w);
-            if (kSwiGLU)
+            if (kTwoB)
               tma_load_2d_hint(sa + 16384, &tm_a, full + pre, kc, wrow + p.up_offset, pol_w);
           }
         }
@@ -311,9 +333,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       // token rows are the previous kernels' output
       pdl_wait();
       pdl_trigger();
-      while (ok && seg_next(sch, si, g)) {
-        const Tile t = decode_tile(p, g.tile);
-        const int wrow = t.e * p.rows_per_expert + t.nb * 128;
+      // the next segment's tile is fetched while this one's stages are issued
+      bool have = seg_next(sch, si, g);
+      Tile t = have ? decode_tile(p, g.tile) : Tile{};
+      while (ok && have) {
+        Seg gn;
+        const bool have_n = seg_next(sch, si, gn);
+        const Tile tn = have_n ? decode_tile(p, gn.tile) : Tile{};
+        const int wrow = t.e * p.rows_per_expert + t.nb * p.wblock_rows;
         for (int kk = g.k0; kk < g.k1; ++kk, ++it) {
           const uint32_t s = it % S;
           const uint32_t ph = (it / S) & 1u;
@@ -327,7 +354,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             }
             mbar_arrive_expect_tx(full + s, kABytes + static_cast<uint32_t>(kTokM ? 128 : t.n) * 128u);
             tma_load_2d_hint(sa, &tm_a, full + s, kc, wrow, pol_w);
-            if (kSwiGLU) tma_load_2d_hint(sa + 16384, &tm_a, full + s, kc, wrow + p.up_offset, pol_w);
+            if (kTwoB) tma_load_2d_hint(sa + 16384, &tm_a, full + s, kc, wrow + p.up_offset, pol_w);
           }
           if (kTokM) {
             // tokens fill the M = 128 slot: 128 rows from the tile's first row
@@ -342,6 +369,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             for (; j < t.n; j += 16) tma_load_2d(sb + j * 128, &tm_b, full + s, kc, t.row0 + j);
           }
         }
+        g = gn;
+        t = tn;
+        have = have_n;
       }
       if (!ok) {
         *abort_flag = 1;
@@ -363,9 +393,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       if (p.debug & MOE_DEBUG_FORCE_TIMEOUT) ok = mbar_wait(never, 0, abort_flag, limit);
       SegIt si = seg_begin(sch);
       Seg g;
-      while (ok && seg_next(sch, si, g)) {
+      bool have = seg_next(sch, si, g);
+      int n_cur = have ? (kTokM ? 128 : decode_tile(p, g.tile).n) : 0;
+      while (ok && have) {
         const int k0 = g.k0, k1 = g.k1;
-        const Tile t = decode_tile(p, g.tile);
+        Seg gn;
+        const bool have_n = seg_next(sch, si, gn);
+        // the next tile's width (only the swap needs it) is fetched meanwhile
+        const int n_next = (have_n && !kTokM) ? decode_tile(p, gn.tile).n : 128;
         const uint32_t a = tt % static_cast<uint32_t>(p.num_acc);
         const uint32_t aph = (tt / static_cast<uint32_t>(p.num_acc)) & 1u;
         if (!mbar_wait(tempty + a, aph ^ 1u, abort_flag, limit)) {
@@ -373,7 +408,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           break;
         }
         tc_fence_after_sync();
-        const uint32_t idesc = umma_idesc(kBF16, 128, kTokM ? 128 : t.n);
+        const uint32_t idesc = umma_idesc(kBF16, 128, n_cur);
         const uint32_t d0 = tmem + a * static_cast<uint32_t>(p.acc_stride);
         const uint32_t d1 = d0 + static_cast<uint32_t>(p.bn_max);
         for (int kk = k0; kk < k1; ++kk, ++it) {
@@ -398,10 +433,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             const uint64_t a1 = kTokM ? db : da1, b1 = kTokM ? da1 : db;
             if (kBF16) {
               umma_bf16(d0, a0 + 2 * k4, b0 + 2 * k4, idesc, acc);
-              if (kSwiGLU) umma_bf16(d1, a1 + 2 * k4, b1 + 2 * k4, idesc, acc);
+              if (kTwoB) umma_bf16(d1, a1 + 2 * k4, b1 + 2 * k4, idesc, acc);
             } else {
               umma_f8(d0, a0 + 2 * k4, b0 + 2 * k4, idesc, acc);
-              if (kSwiGLU) umma_f8(d1, a1 + 2 * k4, b1 + 2 * k4, idesc, acc);
+              if (kTwoB) umma_f8(d1, a1 + 2 * k4, b1 + 2 * k4, idesc, acc);
             }
           }
           umma_commit(empty + s);
@@ -409,6 +444,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         if (!ok) break;
         umma_commit(tfull + a);
         ++tt;
+        g = gn;
+        have = have_n;
+        n_cur = n_next;
       }
       if (!ok) {
         *abort_flag = 1;
@@ -429,36 +467,27 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     uint32_t n_chunks = 0;  // combine staging chunks issued by this warp
     uint32_t tt = 0;
     bool ok = true;
+    // Metadata runs ahead: the tile list entry two segments ahead and the
+    // pair ids / weights one segment ahead are in flight while a tile is
+    // processed, so no tile starts on a chain of dependent global loads.
     SegIt si = seg_begin(sch);
-    Seg g;
-    while (seg_next(sch, si, g)) {
+    Seg g, g1;
+    bool have = seg_next(sch, si, g);
+    Tile t = have ? decode_tile(p, g.tile) : Tile{};
+    Meta mt = have ? load_meta<kBF16, kSwiGLU, kTokM>(p, t, lane, row_l) : Meta{};
+    bool have1 = have && seg_next(sch, si, g1);
+    Tile t1 = have1 ? decode_tile(p, g1.tile) : Tile{};
+    while (have) {
       const int k0 = g.k0, k1 = g.k1;
-      const Tile t = decode_tile(p, g.tile);
+      const Meta mt1 = have1 ? load_meta<kBF16, kSwiGLU, kTokM>(p, t1, lane, row_l) : Meta{};
+      Seg g2;
+      const bool have2 = have1 && seg_next(sch, si, g2);
+      const Tile t2 = have2 ? decode_tile(p, g2.tile) : Tile{};
       const uint32_t a = tt % static_cast<uint32_t>(p.num_acc);
       const uint32_t aph = (tt / static_cast<uint32_t>(p.num_acc)) & 1u;
-      // Tile metadata, fetched while the MMAs run.  Swap: lane l holds the
-      // pair ids / router weights of columns l, l+32, l+64, l+96 (row tiles
-      // have at most 128 columns).  Unswapped: the thread's lane is token row
-      // row_l of the tile; entry 0 holds its pair.
-      int cpid[4];
-      float cw[4];
-      if (kTokM) {
-        cpid[0] = row_l < t.n ? p.sorted_ids[t.row0 + row_l] : p.P;
-        cw[0] = (!kSwiGLU && cpid[0] < p.P) ? p.topk_w[cpid[0]] : 0.f;
-#pragma unroll
-        for (int s4 = 1; s4 < 4; ++s4) {
-          cpid[s4] = p.P;
-          cw[s4] = 0.f;
-        }
-      } else {
-#pragma unroll
-        for (int s4 = 0; s4 < 4; ++s4) {
-          const int c = s4 * 32 + lane;
-          cpid[s4] = c < t.n ? p.sorted_ids[t.row0 + c] : p.P;
-          cw[s4] = (!kSwiGLU && cpid[s4] < p.P) ? p.topk_w[cpid[s4]] : 0.f;
-        }
-      }
-      const float wsc = kBF16 ? 1.f : p.w_scale[t.e];
+      const int(&cpid)[4] = mt.pid;
+      const float(&cw)[4] = mt.w;
+      const float wsc = mt.wsc;
       int got = 0;
       if (lane == 0) got = mbar_wait(tfull + a, aph, abort_flag, limit) ? 1 : 0;
       got = __shfl_sync(0xffffffffu, got, 0);
@@ -584,20 +613,27 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           float y[16];
           tmem_ld16(tbase + c0, y);
           if (kTokM) {
-            // 16 consecutive output columns of this thread's pair
+            // 16 consecutive output columns of this thread's pair (and, for a
+            // pair of weight blocks, the same 16 of the second block)
+            float y1[16];
+            if (kPair) tmem_ld16(tbase + p.bn_max + c0, y1);
             if (row_ok && cpid[0] < p.P) {
               const float w_r = sc * cw[0];
-              uint4 o[2];
-              uint32_t* ow = reinterpret_cast<uint32_t*>(o);
 #pragma unroll
-              for (int j = 0; j < 8; ++j) {
-                __nv_bfloat162 b2 = __floats2bfloat162_rn(y[2 * j] * w_r, y[2 * j + 1] * w_r);
-                ow[j] = *reinterpret_cast<uint32_t*>(&b2);
+              for (int b2i = 0; b2i < (kPair ? 2 : 1); ++b2i) {
+                const float* yy = b2i == 0 ? y : y1;
+                uint4 o[2];
+                uint32_t* ow = reinterpret_cast<uint32_t*>(o);
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                  __nv_bfloat162 b2 = __floats2bfloat162_rn(yy[2 * j] * w_r, yy[2 * j + 1] * w_r);
+                  ow[j] = *reinterpret_cast<uint32_t*>(&b2);
+                }
+                uint4* dst = reinterpret_cast<uint4*>(p.pair_out + static_cast<size_t>(cpid[0]) * p.ldo +
+                                                      t.nb * p.wblock_rows + b2i * 128 + c0);
+                dst[0] = o[0];
+                dst[1] = o[1];
               }
-              uint4* dst = reinterpret_cast<uint4*>(
-                  p.pair_out + static_cast<size_t>(cpid[0]) * p.ldo + t.nb * 128 + c0);
-              dst[0] = o[0];
-              dst[1] = o[1];
             }
           } else {
             const int pid_c = pick4(cpid, c0 >> 5);
@@ -613,17 +649,24 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         }
       } else if (kTokM) {
         // combine, unswapped: 16 consecutive columns of this thread's token
-        // row, added with four 16-byte vector reductions
+        // row (of each weight block of a pair), added with 16-byte vector
+        // reductions
         for (int c0 = c_begin; c0 < ncols; c0 += 32) {
-          float y[16];
+          float y[16], y1[16];
           tmem_ld16(tbase + c0, y);
+          if (kPair) tmem_ld16(tbase + p.bn_max + c0, y1);
           if (row_ok && cpid[0] < p.P) {
             const float w_r = sc * cw[0];
-            float* dst = p.acc_out + static_cast<size_t>(cpid[0] / p.top_k) * p.ldo + t.nb * 128 + c0;
 #pragma unroll
-            for (int j = 0; j < 4; ++j)
-              red_add_v4_f32(dst + 4 * j, y[4 * j] * w_r, y[4 * j + 1] * w_r, y[4 * j + 2] * w_r,
-                             y[4 * j + 3] * w_r);
+            for (int b2i = 0; b2i < (kPair ? 2 : 1); ++b2i) {
+              const float* yy = b2i == 0 ? y : y1;
+              float* dst = p.acc_out + static_cast<size_t>(cpid[0] / p.top_k) * p.ldo +
+                           t.nb * p.wblock_rows + b2i * 128 + c0;
+#pragma unroll
+              for (int j = 0; j < 4; ++j)
+                red_add_v4_f32(dst + 4 * j, yy[4 * j] * w_r, yy[4 * j + 1] * w_r,
+                               yy[4 * j + 2] * w_r, yy[4 * j + 3] * w_r);
+            }
           }
         }
       } else {
@@ -659,6 +702,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(tempty + a);
       ++tt;
+      g = g1;
+      t = t1;
+      mt = mt1;
+      have = have1;
+      g1 = g2;
+      t1 = t2;
+      have1 = have2;
     }
     if (kSwiGLU && !kBF16) {
 #pragma unroll
@@ -684,20 +734,20 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   }
 }
 
-template <bool kBF16, bool kSwiGLU, bool kTokM>
+template <bool kBF16, bool kSwiGLU, bool kTokM, bool kPair = false>
 cudaError_t launch_one(const GemmParams& p, const CUtensorMap& ta, const CUtensorMap& tb,
                        const CUtensorMap& tb64, int grid, cudaStream_t st) {
   static thread_local int configured_device = -1;
   int dev = 0;
   cudaGetDevice(&dev);
   if (configured_device != dev) {
-    cudaError_t e = checked(cudaFuncSetAttribute(moe_gemm_kernel<kBF16, kSwiGLU, kTokM>,
+    cudaError_t e = checked(cudaFuncSetAttribute(moe_gemm_kernel<kBF16, kSwiGLU, kTokM, kPair>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit), "smem attribute");
     if (e != cudaSuccess) return e;
     configured_device = dev;
   }
   const size_t smem = kSmemLimit;
-  return launch_pdl(moe_gemm_kernel<kBF16, kSwiGLU, kTokM>, dim3(grid), dim3(kGemmThreads), smem, st, p,
+  return launch_pdl(moe_gemm_kernel<kBF16, kSwiGLU, kTokM, kPair>, dim3(grid), dim3(kGemmThreads), smem, st, p,
                     ta, tb, tb64);
 }
 
@@ -710,9 +760,13 @@ size_t gemm_stage_smem(bool swiglu) {
   return kSmemLimit - kSmemSlack - (swiglu ? 0 : kCombineStaging);
 }
 
-cudaError_t launch_gemm(bool bf16, bool swiglu, bool tok_m, const GemmParams& p,
+cudaError_t launch_gemm(bool bf16, bool swiglu, bool tok_m, bool pair, const GemmParams& p,
                         const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tb64,
                         int grid, cudaStream_t st) {
+  if (pair && tok_m && !swiglu)
+    return bf16 ? launch_one<true, false, true, true>(p, ta, tb, tb64, grid, st)
+                : launch_one<false, false, true, true>(p, ta, tb, tb64, grid, st);
+  if (pair) return cudaErrorInvalidValue;  // pairs exist for the unswapped down GEMM only
   if (tok_m) {
     if (bf16)
       return swiglu ? launch_one<true, true, true>(p, ta, tb, tb64, grid, st)

@@ -82,6 +82,8 @@ struct AlignParams {
   // null: every CTA counts all pairs itself
   const int32_t* chunk_hist;
   // fused-path extras (null when unused)
+  const float* wts;      // [P] router weights (read when sorted_w is set)
+  float* sorted_w;       // router weight of each aligned row, 0 for padding
   int4* mtiles;          // GEMM row tiles {expert, first row, rows, 0}
   int bn_max;            // max rows of one row tile
   Ctrl* ctrl;
@@ -108,6 +110,7 @@ struct SmallFrontParams {
   int32_t* counts;
   int32_t* offsets;
   int32_t* sorted_ids;
+  float* sorted_w;  // router weight of each aligned row, 0 for padding
   int4* mtiles;
   int bn_max;
 };
@@ -153,12 +156,13 @@ struct GemmParams {
   int num_acc;          // accumulator buffers (1 or 2)
   int tmem_cols;        // allocated TMEM columns (power of two >= 32)
   int rows_per_expert;  // 2I (gate/up) or H (down)
-  int up_offset;        // I: first up row inside an expert's w13 block
+  int wblock_rows;      // weight rows between consecutive tile blocks: 128, or 256 for pairs
+  int up_offset;        // second weight block of a stage: I (gate/up) or 128 (pairs)
   const int32_t* sorted_ids;
   int P, top_k;
   const float* w_scale;  // [E] per-expert weight scale (FP8) or null
   int act_scale_sel;     // 1: s_x, 2: s_h (FP8); 0: none
-  const float* topk_w;   // [P]
+  const float* sorted_w;  // router weight of each aligned row (0 for padding)
   void* h_out;           // gate/up: [rows, I], fp32 (FP8 path) or bf16 (bf16 path)
   int ldh;
   float* acc_out;        // down, combine by reduction: [T, H] fp32
@@ -194,10 +198,10 @@ constexpr int kGemmThreads = 64 + 32 * kGemmEpiWarps;
 size_t gemm_stage_smem(bool swiglu);
 // tmb / tmb64: the token operand with 16-row and 64-row boxes.  tok_m: tokens
 // in the MMA M slot (the unswapped placement; row tiles of up to 128 rows).
-cudaError_t launch_gemm(bool bf16, bool swiglu, bool tok_m, const GemmParams& p,
+// pair: the unswapped down GEMM with two weight blocks per tile (H % 256 == 0).
+cudaError_t launch_gemm(bool bf16, bool swiglu, bool tok_m, bool pair, const GemmParams& p,
                         const CUtensorMap& tma, const CUtensorMap& tmb, const CUtensorMap& tmb64,
                         int grid, cudaStream_t st);
 // Row-tile width of the unswapped placement (the token tile fills M = 128).
 constexpr int kTokMRows = 128;
-
 }  // namespace moe

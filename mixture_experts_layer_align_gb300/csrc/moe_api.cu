@@ -115,7 +115,7 @@ struct Layout {
   bool large = false;
   size_t chunk_hist = 0, xq_tok = 0;
   size_t ctrl = 0, trace = 0, partials = 0, ids = 0, wts = 0, counts = 0, offsets = 0,
-         sorted = 0, mtiles = 0, tile_cnt = 0, part = 0, xs = 0, h = 0, hq = 0, acc = 0,
+         sorted = 0, sorted_w = 0, mtiles = 0, tile_cnt = 0, part = 0, xs = 0, h = 0, hq = 0, acc = 0,
          total = 0;
 };
 
@@ -142,6 +142,7 @@ Layout make_layout(int T, int H, int I, int E, int k, bool fp8) {
   L.counts = take(sizeof(int32_t) * E);
   L.offsets = take(sizeof(int32_t) * (E + 1));
   L.sorted = take(sizeof(int32_t) * L.pad_max);
+  L.sorted_w = take(sizeof(float) * L.pad_max);
   L.mtiles = take(sizeof(int4) * L.max_mtiles);
   L.tile_cnt = take(sizeof(int) * static_cast<size_t>(L.n_tile_cnt));
   // sized for the widest row tile (the unswapped placement uses 128 rows)
@@ -335,6 +336,7 @@ moe_status_t fused_forward_impl(const moe_fused_args* a, void* workspace, size_t
   int32_t* counts = a->counts_out ? a->counts_out : reinterpret_cast<int32_t*>(ws + L.counts);
   int32_t* offsets = reinterpret_cast<int32_t*>(ws + L.offsets);
   int32_t* sorted = reinterpret_cast<int32_t*>(ws + L.sorted);
+  float* sorted_w = reinterpret_cast<float*>(ws + L.sorted_w);
   int4* mtiles = reinterpret_cast<int4*>(ws + L.mtiles);
   void* xs = ws + L.xs;
   void* h = ws + L.h;
@@ -377,6 +379,7 @@ moe_status_t fused_forward_impl(const moe_fused_args* a, void* workspace, size_t
     sp.counts = counts;
     sp.offsets = offsets;
     sp.sorted_ids = sorted;
+    sp.sorted_w = sorted_w;
     sp.mtiles = mtiles;
     sp.bn_max = bn_max;
     if (launch_route_align_small(sp, s) != cudaSuccess) return MOE_ERR_CUDA;
@@ -400,6 +403,8 @@ moe_status_t fused_forward_impl(const moe_fused_args* a, void* workspace, size_t
   ap.counts = counts;
   ap.offsets = offsets;
   ap.sorted_ids = sorted;
+  ap.wts = wts;
+  ap.sorted_w = sorted_w;
   ap.tile_expert = nullptr;
   ap.num_padded = nullptr;
   ap.mtiles = mtiles;
@@ -456,13 +461,14 @@ moe_status_t fused_forward_impl(const moe_fused_args* a, void* workspace, size_t
   g1.num_acc = (4 * bn_max <= 512) ? 2 : 1;
   g1.tmem_cols = next_pow2(g1.acc_stride * g1.num_acc);
   g1.rows_per_expert = 2 * I;
+  g1.wblock_rows = 128;
   g1.up_offset = I;
   g1.sorted_ids = sorted;
   g1.P = static_cast<int>(P);
   g1.top_k = k;
   g1.w_scale = fp8 ? a->w13_scale : nullptr;
   g1.act_scale_sel = fp8 ? 1 : 0;
-  g1.topk_w = wts;
+  g1.sorted_w = sorted_w;
   g1.h_out = h;
   g1.ldh = I;
   g1.tile_cnt = tile_cnt;
@@ -478,7 +484,7 @@ moe_status_t fused_forward_impl(const moe_fused_args* a, void* workspace, size_t
   const long long work1 = max_tiles * g1.nb_count * g1.k_steps;
   const int grid1 = static_cast<int>(std::max<long long>(1, std::min<long long>(ctas, work1)));
   if (events && cudaEventRecord(events[3], stream) != cudaSuccess) return MOE_ERR_CUDA;
-  if (launch_gemm(bf16, true, tok_m1, g1, tm_w13, tm_xs, tm_xs64, grid1, s) != cudaSuccess)
+  if (launch_gemm(bf16, true, tok_m1, false, g1, tm_w13, tm_xs, tm_xs64, grid1, s) != cudaSuccess)
     return MOE_ERR_CUDA;
 
   // 5. dynamic scale of h and its E4M3 codes
@@ -491,14 +497,17 @@ moe_status_t fused_forward_impl(const moe_fused_args* a, void* workspace, size_t
   //    the combine buffer like any other partial sum)
   if (events && cudaEventRecord(events[5], stream) != cudaSuccess) return MOE_ERR_CUDA;
   GemmParams g2 = g1;
-  g2.nb_count = H / 128;
+  // unswapped: two 128-row weight blocks per tile against one token tile
+  const bool pair2 = tok_m2 && H % 256 == 0;
+  g2.nb_count = H / (pair2 ? 256 : 128);
   g2.k_steps = I / k_elems;
   g2.stage_smem = static_cast<unsigned>(gemm_stage_smem(false));
-  g2.acc_stride = bn_max;
+  g2.acc_stride = pair2 ? 2 * bn_max : bn_max;
   g2.num_acc = 2;
-  g2.tmem_cols = next_pow2(2 * bn_max);
+  g2.tmem_cols = next_pow2(2 * g2.acc_stride);
   g2.rows_per_expert = H;
-  g2.up_offset = 0;
+  g2.wblock_rows = pair2 ? 256 : 128;
+  g2.up_offset = pair2 ? 128 : 0;
   g2.w_scale = fp8 ? a->w2_scale : nullptr;
   g2.act_scale_sel = fp8 ? 2 : 0;
   g2.h_out = nullptr;
@@ -510,7 +519,7 @@ moe_status_t fused_forward_impl(const moe_fused_args* a, void* workspace, size_t
   g2.trace = (a->debug_flags & MOE_DEBUG_TRACE) ? trace + MOE_TRACE_MAX_CTAS * 4 : nullptr;
   const long long work2 = max_tiles * g2.nb_count * g2.k_steps;
   const int grid2 = static_cast<int>(std::max<long long>(1, std::min<long long>(ctas, work2)));
-  if (launch_gemm(bf16, false, tok_m2, g2, tm_w2, tm_h, tm_h64, grid2, s) != cudaSuccess)
+  if (launch_gemm(bf16, false, tok_m2, pair2, g2, tm_w2, tm_h, tm_h64, grid2, s) != cudaSuccess)
     return MOE_ERR_CUDA;
 
   // 7. fp32 combine buffer -> bf16 output, or the sum of each token's k rows

@@ -329,7 +329,11 @@ __global__ void __launch_bounds__(kAlignThreads) align_kernel(AlignParams p) {
       seg[warp * E + e] = static_cast<uint16_t>(seg[warp * E + e] + __popc(mask));
     }
     slot = __shfl_sync(kFull, slot, leader);
-    if (valid) p.sorted_ids[slot + __popc(mask & ((1u << lane) - 1u))] = q;
+    if (valid) {
+      const int at = slot + __popc(mask & ((1u << lane) - 1u));
+      p.sorted_ids[at] = q;
+      if (p.sorted_w) p.sorted_w[at] = p.wts[q];
+    }
     __syncwarp();
   }
 
@@ -338,7 +342,10 @@ __global__ void __launch_bounds__(kAlignThreads) align_kernel(AlignParams p) {
   // padding sentinels and the per-block expert map
   if (tid < E) {
     const int o = seg_off[tid];
-    for (int i = c; i < padded; ++i) p.sorted_ids[o + i] = P;
+    for (int i = c; i < padded; ++i) {
+      p.sorted_ids[o + i] = P;
+      if (p.sorted_w) p.sorted_w[o + i] = 0.f;
+    }
     if (p.tile_expert)
       for (int b = o / p.bm; b < (o + padded) / p.bm; ++b) p.tile_expert[b] = tid;
   }
@@ -467,12 +474,19 @@ __global__ void __launch_bounds__(kAlignThreads, 1) route_align_small_kernel(Sma
         s_run[e] = slot + __popc(mask);
       }
       slot = __shfl_sync(kFull, slot, leader);
-      if (valid) p.sorted_ids[slot + __popc(mask & ((1u << lane) - 1u))] = q;
+      if (valid) {
+        const int at = slot + __popc(mask & ((1u << lane) - 1u));
+        p.sorted_ids[at] = q;
+        p.sorted_w[at] = s_w[q];
+      }
       __syncwarp();
     }
   }
   if (tid < E) {
-    for (int i = c; i < padded; ++i) p.sorted_ids[off + i] = P;
+    for (int i = c; i < padded; ++i) {
+      p.sorted_ids[off + i] = P;
+      p.sorted_w[off + i] = 0.f;
+    }
     p.counts[tid] = c;
     p.offsets[tid] = off;
   }

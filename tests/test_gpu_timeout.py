@@ -12,8 +12,10 @@ from mixture_experts_layer_align_gb300 import inputs
 pytestmark = pytest.mark.gpu
 
 
-def test_forced_timeout_reports_status_and_context_survives(gpu_lib):
-    T, H, I, E, k = 8, 256, 256, 8, 2
+# (8, ...) decode-style tiles; (600, ...) large batch with short K: the down
+# GEMM runs with the token tile held in shared memory
+@pytest.mark.parametrize("T,H,I,E,k", [(8, 256, 256, 8, 2), (600, 256, 128, 4, 2)])
+def test_forced_timeout_reports_status_and_context_survives(gpu_lib, T, H, I, E, k):
     w = inputs.make_weights(H, I, E, "fp8", seed=11)
     a = inputs.make_activations(T, H, E, "uniform", seed=11)
     d = dict(x=a.x.cuda(), lg=a.logits.cuda(), w13=w.w13.cuda(), w2=w.w2.cuda(),
