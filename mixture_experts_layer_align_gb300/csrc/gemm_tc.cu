@@ -77,20 +77,22 @@ __device__ __forceinline__ Tile decode_tile(const GemmParams& p, int u) {
 }
 
 // Epilogue metadata of a tile.  Swap: lane l holds the pair ids and router
-// weights of columns l, l+32, l+64, l+96 (row tiles have at most 128
-// columns).  Unswapped: the thread's lane is token row row_l of the tile and
+// weights of columns l + 32 i, i < N (N = 8 covers the 256-column wide
+// tiles).  Unswapped: the thread's lane is token row row_l of the tile and
 // entry 0 holds it.  wsc: the expert's weight scale.
+template <int N>
 struct Meta {
-  int pid[4];
-  float w[4];
+  int pid[N];
+  float w[N];
   float wsc;
 };
 
-template <bool kBF16, bool kSwiGLU, bool kTokM>
-__device__ __forceinline__ Meta load_meta(const GemmParams& p, const Tile& t, int lane, int row_l) {
-  Meta m;
+template <bool kBF16, bool kSwiGLU, bool kTokM, int N>
+__device__ __forceinline__ Meta<N> load_meta(const GemmParams& p, const Tile& t, int lane,
+                                             int row_l) {
+  Meta<N> m;
 #pragma unroll
-  for (int s4 = 0; s4 < 4; ++s4) {
+  for (int s4 = 0; s4 < N; ++s4) {
     const int c = kTokM ? row_l : s4 * 32 + lane;
     const bool in = (kTokM ? s4 == 0 : true) && c < t.n;
     m.pid[s4] = in ? p.sorted_ids[t.row0 + c] : p.P;
@@ -208,10 +210,13 @@ __device__ __forceinline__ float* part_slot(const GemmParams& p, int c, long lon
   return p.part + (static_cast<size_t>(c) * 2 + s) * gemm_part_slot_floats(p.bn_max);
 }
 
-// v[s] for a warp-uniform runtime s in [0, 4) without local-memory indexing.
-template <typename V>
-__device__ __forceinline__ V pick4(const V (&v)[4], int s) {
-  return s == 0 ? v[0] : (s == 1 ? v[1] : (s == 2 ? v[2] : v[3]));
+// v[s] for a warp-uniform runtime s in [0, N) without local-memory indexing.
+template <int N, typename V>
+__device__ __forceinline__ V pickn(const V (&v)[N], int s) {
+  V r = v[0];
+#pragma unroll
+  for (int i = 1; i < N; ++i) r = (s == i) ? v[i] : r;
+  return r;
 }
 
 // kTokM selects the unswapped placement (the ablation of the operand swap):
@@ -234,7 +239,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   // used, so decode (tiles of a few rows) keeps more weight bytes in flight.
   constexpr bool kTwoB = kSwiGLU || kPair;  // two weight blocks per stage
   constexpr uint32_t kABytes = kTwoB ? 32768u : 16384u;
-  const int rows_b = kTokM ? 128 : min(p.bn_max, max(16, p.ctrl->max_tile_rows));
+  const int max_rows = p.wide ? p.ctrl->max_tile_rows_w : p.ctrl->max_tile_rows;
+  const int rows_b = kTokM ? 128 : min(p.bn_max, max(16, max_rows));
   const uint32_t stage_bytes = kABytes + static_cast<uint32_t>(rows_b) * 128u;
   const int S = min(kSwiGLU ? kMaxStagesGateUp : kMaxStagesDown,
                     static_cast<int>(p.stage_smem / stage_bytes));
@@ -297,7 +303,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   if (trace && threadIdx.x == 0) trace[1] = global_timer_ns();
 
   const int K = p.k_steps;
-  const int tiles = p.ctrl->num_mtiles * p.nb_count;
+  const int tiles = (p.wide ? p.ctrl->num_mtiles_w : p.ctrl->num_mtiles) * p.nb_count;
   const Sched sch = make_sched(tiles, K, p.weights_evict_first == 0,
                                !kSwiGLU && p.pair_out != nullptr);
   const uint64_t limit = p.timeout_ns;
@@ -474,19 +480,23 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     Seg g, g1;
     bool have = seg_next(sch, si, g);
     Tile t = have ? decode_tile(p, g.tile) : Tile{};
-    Meta mt = have ? load_meta<kBF16, kSwiGLU, kTokM>(p, t, lane, row_l) : Meta{};
+    // swap: up to 32 x kMetaN columns per tile (wide gate/up tiles have 256)
+    constexpr int kMetaN = (kSwiGLU && !kTokM) ? 8 : 4;
+    Meta<kMetaN> mt = have ? load_meta<kBF16, kSwiGLU, kTokM, kMetaN>(p, t, lane, row_l)
+                           : Meta<kMetaN>{};
     bool have1 = have && seg_next(sch, si, g1);
     Tile t1 = have1 ? decode_tile(p, g1.tile) : Tile{};
     while (have) {
       const int k0 = g.k0, k1 = g.k1;
-      const Meta mt1 = have1 ? load_meta<kBF16, kSwiGLU, kTokM>(p, t1, lane, row_l) : Meta{};
+      const Meta<kMetaN> mt1 =
+          have1 ? load_meta<kBF16, kSwiGLU, kTokM, kMetaN>(p, t1, lane, row_l) : Meta<kMetaN>{};
       Seg g2;
       const bool have2 = have1 && seg_next(sch, si, g2);
       const Tile t2 = have2 ? decode_tile(p, g2.tile) : Tile{};
       const uint32_t a = tt % static_cast<uint32_t>(p.num_acc);
       const uint32_t aph = (tt / static_cast<uint32_t>(p.num_acc)) & 1u;
-      const int(&cpid)[4] = mt.pid;
-      const float(&cw)[4] = mt.w;
+      const int(&cpid)[kMetaN] = mt.pid;
+      const float(&cw)[kMetaN] = mt.w;
       const float wsc = mt.wsc;
       int got = 0;
       if (lane == 0) got = mbar_wait(tfull + a, aph, abort_flag, limit) ? 1 : 0;
@@ -538,7 +548,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         }
         if (finish) {
           for (int c0 = c_begin; c0 < ncols; c0 += 32) {
-            const int pid_c = pick4(cpid, c0 >> 5);  // swap: column (c0 & 31) + lane of this block
+            const int pid_c = pickn<kMetaN>(cpid, c0 >> 5);  // swap: column (c0 & 31) + lane of this block
             float gg[16], v[16];
             tmem_ld16x2(tbase + c0, tbase + p.bn_max + c0, gg, v);
             if (!whole) {
@@ -636,8 +646,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
               }
             }
           } else {
-            const int pid_c = pick4(cpid, c0 >> 5);
-            const float w_c = sc * pick4(cw, c0 >> 5);
+            const int pid_c = pickn<kMetaN>(cpid, c0 >> 5);
+            const float w_c = sc * pickn<kMetaN>(cw, c0 >> 5);
 #pragma unroll
             for (int j = 0; j < 16; ++j) {
               const int pj = __shfl_sync(0xffffffffu, pid_c, (c0 & 31) + j);
@@ -679,9 +689,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           tmem_ld16(tbase + c0, y);
           float* buf = wstage + (n_chunks & 1u) * 16 * 32;
           // lane j < 16 handles column c0 + j
-          const int pid = __shfl_sync(0xffffffffu, pick4(cpid, c0 >> 5), (c0 & 31) + (lane & 15));
+          const int pid = __shfl_sync(0xffffffffu, pickn<kMetaN>(cpid, c0 >> 5), (c0 & 31) + (lane & 15));
           const float wscale =
-              sc * __shfl_sync(0xffffffffu, pick4(cw, c0 >> 5), (c0 & 31) + (lane & 15));
+              sc * __shfl_sync(0xffffffffu, pickn<kMetaN>(cw, c0 >> 5), (c0 & 31) + (lane & 15));
           if (lane < 16) bulk_wait_read<1>();  // this buffer's reductions from two chunks ago have read it
           __syncwarp();
 #pragma unroll

@@ -58,7 +58,9 @@ struct Ctrl {
   int num_padded;   // rows of the aligned (sorted, padded) pair list
   int num_mtiles;   // entries of the GEMM row-tile list
   int max_tile_rows;  // rows of the largest row tile
-  int pad[9];
+  int num_mtiles_w;     // the same for the list of wide (256-row) tiles, when written
+  int max_tile_rows_w;
+  int pad[7];
 };
 static_assert(sizeof(Ctrl) == 64, "Ctrl layout");
 
@@ -86,6 +88,7 @@ struct AlignParams {
   float* sorted_w;       // router weight of each aligned row, 0 for padding
   int4* mtiles;          // GEMM row tiles {expert, first row, rows, 0}
   int bn_max;            // max rows of one row tile
+  int4* mtiles_w;        // second list of tiles of up to 256 rows, or null
   Ctrl* ctrl;
   const float* amax_partials;
   int n_partials;
@@ -113,6 +116,7 @@ struct SmallFrontParams {
   float* sorted_w;  // router weight of each aligned row, 0 for padding
   int4* mtiles;
   int bn_max;
+  int4* mtiles_w;   // second list of tiles of up to 256 rows, or null
 };
 cudaError_t launch_route_align_small(const SmallFrontParams& p, cudaStream_t st);
 
@@ -147,6 +151,7 @@ struct GemmParams {
   // the expert's first tile}, written by the alignment kernel.
   const int4* mtiles;
   Ctrl* ctrl;
+  int wide;             // 1: the wide tile list (counts num_mtiles_w / max_tile_rows_w)
   int nb_count;         // 128-row weight blocks per expert (I/128 or H/128)
   int k_steps;          // K / (128 bytes of K)
   int k_elems;          // elements of K per step: 128 (E4M3) or 64 (bf16)
@@ -185,6 +190,9 @@ struct GemmParams {
 // (fp32 accumulation, bf16 result).
 cudaError_t launch_combine_rows(const __nv_bfloat16* rows, int T, int k, int H,
                                 __nv_bfloat16* out, int num_sms, cudaStream_t st);
+
+// Widest row tile of any GEMM (wide gate/up tiles).
+constexpr int kWideRows = 256;
 
 // Partial-accumulator slot (gate and up, bn_max columns x 128 rows, fp32).
 __host__ __device__ inline size_t gemm_part_slot_floats(int bn_max) { return static_cast<size_t>(2) * bn_max * 128; }

@@ -115,7 +115,7 @@ struct Layout {
   bool large = false;
   size_t chunk_hist = 0, xq_tok = 0;
   size_t ctrl = 0, trace = 0, partials = 0, ids = 0, wts = 0, counts = 0, offsets = 0,
-         sorted = 0, sorted_w = 0, mtiles = 0, tile_cnt = 0, part = 0, xs = 0, h = 0, hq = 0, acc = 0,
+         sorted = 0, sorted_w = 0, mtiles = 0, mtiles_w = 0, tile_cnt = 0, part = 0, xs = 0, h = 0, hq = 0, acc = 0,
          total = 0;
 };
 
@@ -144,9 +144,10 @@ Layout make_layout(int T, int H, int I, int E, int k, bool fp8) {
   L.sorted = take(sizeof(int32_t) * L.pad_max);
   L.sorted_w = take(sizeof(float) * L.pad_max);
   L.mtiles = take(sizeof(int4) * L.max_mtiles);
+  L.mtiles_w = take(sizeof(int4) * L.max_mtiles);
   L.tile_cnt = take(sizeof(int) * static_cast<size_t>(L.n_tile_cnt));
-  // sized for the widest row tile (the unswapped placement uses 128 rows)
-  L.part = take(sizeof(float) * 2 * static_cast<size_t>(L.ctas) * gemm_part_slot_floats(kTokMRows));
+  // sized for the widest row tile (wide gate/up tiles have 256 rows)
+  L.part = take(sizeof(float) * 2 * static_cast<size_t>(L.ctas) * gemm_part_slot_floats(kWideRows));
   L.xs = take(static_cast<size_t>(L.pad_max) * H * (fp8 ? 1 : 2));
   L.h = take(static_cast<size_t>(L.pad_max) * I * (fp8 ? 4 : 2));
   L.hq = take(fp8 ? static_cast<size_t>(L.pad_max) * I : 0);
@@ -356,6 +357,12 @@ moe_status_t fused_forward_impl(const moe_fused_args* a, void* workspace, size_t
   const bool tok_m1 = force_tok;
   const bool tok_m2 = force_tok || (!force_w && I / 128 <= 16);
   const int bn_max = L.bn_max;
+  // Gate/up with the weights in M and experts of more than 256 rows on
+  // average (prefill): 256-token tiles read each weight block half as often
+  // (at the cost of a single TMEM accumulator buffer), from a second tile list.
+  const long long touched_ub = std::min<long long>(E, P);
+  const bool wide1 = !tok_m1 && (P + touched_ub - 1) / touched_ub > kWideRows;
+  int4* mtiles_w = reinterpret_cast<int4*>(ws + L.mtiles_w);
   int* tile_cnt = reinterpret_cast<int*>(ws + L.tile_cnt);
   float* part = reinterpret_cast<float*>(ws + L.part);
 
@@ -382,6 +389,7 @@ moe_status_t fused_forward_impl(const moe_fused_args* a, void* workspace, size_t
     sp.sorted_w = sorted_w;
     sp.mtiles = mtiles;
     sp.bn_max = bn_max;
+    sp.mtiles_w = wide1 ? mtiles_w : nullptr;
     if (launch_route_align_small(sp, s) != cudaSuccess) return MOE_ERR_CUDA;
     if (events && (cudaEventRecord(events[1], stream) != cudaSuccess ||
                    cudaEventRecord(events[2], stream) != cudaSuccess))
@@ -409,6 +417,7 @@ moe_status_t fused_forward_impl(const moe_fused_args* a, void* workspace, size_t
   ap.num_padded = nullptr;
   ap.mtiles = mtiles;
   ap.bn_max = bn_max;
+  ap.mtiles_w = wide1 ? mtiles_w : nullptr;
   ap.ctrl = ctrl;
   ap.amax_partials = fp8 ? partials : nullptr;
   ap.n_partials = fp8 ? L.n_partials : 0;
@@ -450,15 +459,17 @@ moe_status_t fused_forward_impl(const moe_fused_args* a, void* workspace, size_t
 
   // 4. gate/up GEMM + SiLU*up epilogue
   GemmParams g1{};
-  g1.mtiles = mtiles;
+  const int bn1 = wide1 ? kWideRows : bn_max;
+  g1.mtiles = wide1 ? mtiles_w : mtiles;
+  g1.wide = wide1 ? 1 : 0;
   g1.ctrl = ctrl;
   g1.nb_count = I / 128;
   g1.k_steps = H / k_elems;
   g1.k_elems = k_elems;
-  g1.bn_max = bn_max;
+  g1.bn_max = bn1;
   g1.stage_smem = static_cast<unsigned>(gemm_stage_smem(true));
-  g1.acc_stride = 2 * bn_max;
-  g1.num_acc = (4 * bn_max <= 512) ? 2 : 1;
+  g1.acc_stride = 2 * bn1;
+  g1.num_acc = (4 * bn1 <= 512) ? 2 : 1;
   g1.tmem_cols = next_pow2(g1.acc_stride * g1.num_acc);
   g1.rows_per_expert = 2 * I;
   g1.wblock_rows = 128;
@@ -474,14 +485,16 @@ moe_status_t fused_forward_impl(const moe_fused_args* a, void* workspace, size_t
   g1.tile_cnt = tile_cnt;
   g1.part = part;
   // a weight block serves one row tile when an expert's rows fit one tile
-  g1.weights_evict_first = (P + touched - 1) / touched <= bn_max ? 1 : 0;
+  g1.weights_evict_first = (P + touched - 1) / touched <= bn1 ? 1 : 0;
   g1.pair_out = nullptr;
   g1.timeout_ns = (a->debug_flags & MOE_DEBUG_FORCE_TIMEOUT) ? MOE_DEBUG_TIMEOUT_MS * 1000000ull
                                                              : kWaitLimitNs;
   g1.debug = a->debug_flags;
   unsigned long long* trace = reinterpret_cast<unsigned long long*>(ws + L.trace);
   g1.trace = (a->debug_flags & MOE_DEBUG_TRACE) ? trace : nullptr;
-  const long long work1 = max_tiles * g1.nb_count * g1.k_steps;
+  const long long max_tiles1 =
+      wide1 ? std::min<long long>(L.max_mtiles, (L.pad_max + bn1 - 1) / bn1 + touched) : max_tiles;
+  const long long work1 = max_tiles1 * g1.nb_count * g1.k_steps;
   const int grid1 = static_cast<int>(std::max<long long>(1, std::min<long long>(ctas, work1)));
   if (events && cudaEventRecord(events[3], stream) != cudaSuccess) return MOE_ERR_CUDA;
   if (launch_gemm(bf16, true, tok_m1, false, g1, tm_w13, tm_xs, tm_xs64, grid1, s) != cudaSuccess)
@@ -497,6 +510,9 @@ moe_status_t fused_forward_impl(const moe_fused_args* a, void* workspace, size_t
   //    the combine buffer like any other partial sum)
   if (events && cudaEventRecord(events[5], stream) != cudaSuccess) return MOE_ERR_CUDA;
   GemmParams g2 = g1;
+  g2.mtiles = mtiles;  // 128-row tiles
+  g2.wide = 0;
+  g2.bn_max = bn_max;
   // unswapped: two 128-row weight blocks per tile against one token tile
   const bool pair2 = tok_m2 && H % 256 == 0;
   g2.nb_count = H / (pair2 ? 256 : 128);

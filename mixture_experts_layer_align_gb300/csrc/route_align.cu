@@ -354,6 +354,9 @@ __global__ void __launch_bounds__(kAlignThreads) align_kernel(AlignParams p) {
     // GEMM row tiles
     const int2 tl = write_mtiles(tid, p.E, padded, tid < p.E ? seg_off[tid] : 0, p.bm, p.bn_max,
                                  p.mtiles, s_tmp);
+    const int2 tw = p.mtiles_w ? write_mtiles(tid, p.E, padded, tid < p.E ? seg_off[tid] : 0, p.bm,
+                                              kWideRows, p.mtiles_w, s_tmp)
+                               : make_int2(0, 0);
     // activation scale of x from the router's per-CTA amax values
     float m = 0.f;
     for (int i = tid; i < p.n_partials; i += kAlignThreads) m = fmaxf(m, p.amax_partials[i]);
@@ -366,6 +369,8 @@ __global__ void __launch_bounds__(kAlignThreads) align_kernel(AlignParams p) {
       p.ctrl->s_x = p.amax_partials ? scale_from_amax(a) : 1.f;
       p.ctrl->num_mtiles = tl.x;
       p.ctrl->max_tile_rows = tl.y;
+      p.ctrl->num_mtiles_w = tw.x;
+      p.ctrl->max_tile_rows_w = tw.y;
     }
   }
 }
@@ -495,6 +500,9 @@ __global__ void __launch_bounds__(kAlignThreads, 1) route_align_small_kernel(Sma
     p.wts[q] = s_w[q];
   }
   const int2 tl = write_mtiles(tid, E, padded, off, kAlignBlock, p.bn_max, p.mtiles, s_tmp);
+  const int2 tw = p.mtiles_w ? write_mtiles(tid, E, padded, off, kAlignBlock, kWideRows, p.mtiles_w,
+                                            s_tmp)
+                             : make_int2(0, 0);
   if (tid == 0) {
     float a = 0.f;
     for (int w = 0; w < 32; ++w) a = fmaxf(a, s_red[w]);
@@ -502,6 +510,8 @@ __global__ void __launch_bounds__(kAlignThreads, 1) route_align_small_kernel(Sma
     ctrl->num_padded = total;
     ctrl->num_mtiles = tl.x;
     ctrl->max_tile_rows = tl.y;
+    ctrl->num_mtiles_w = tw.x;
+    ctrl->max_tile_rows_w = tw.y;
     ctrl->s_x = p.x != nullptr ? scale_from_amax(a) : 1.f;
   }
 }
