@@ -192,7 +192,7 @@ def tokens_list(args, cfg):
 
 
 # --------------------------------------------------------------------------- CPU oracle
-def time_oracle(cfg, Ts, weights_cpu, acts_cpu, min_seconds=10.0, max_passes=3):
+def time_oracle(cfg, Ts, weights_cpu, acts_cpu, min_seconds=10.0, max_passes=8):
     """Wall time of the CPU oracle over the T sweep; repeats whole passes
     until `min_seconds` elapsed (at most `max_passes`)."""
     import oracle
