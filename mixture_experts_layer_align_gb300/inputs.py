@@ -17,6 +17,11 @@ Workloads (the sizes of the five measured configurations):
 All renormalise the top-k weights.  Draw order per case: logits, x (one
 generator seeded with (seed, T)), then w13, w2 (a generator seeded with seed
 alone, so that one set of weights serves every T of a sweep).
+
+The inverse-rotary / per-head FP8 kernel takes head vectors x ~ N(0,1) bf16
+[T, NH, D], positions uniform in [0, max_pos) and the rotary cache a model
+would hold: cos and sin of pos * base^(-2i/D), computed in fp64 and stored as
+fp32 [max_pos, D/2] (base 10000).
 """
 from __future__ import annotations
 
@@ -122,6 +127,25 @@ def make_activations(T: int, H: int, E: int, routing: str = "uniform", seed: int
     return Activations(x, logits.contiguous(), T)
 
 
+@dataclasses.dataclass
+class RopeInputs:
+    x: torch.Tensor          # bf16 [T, NH, D]
+    positions: torch.Tensor  # int32 [T]
+    cos: torch.Tensor        # fp32 [max_pos, D/2]
+    sin: torch.Tensor        # fp32 [max_pos, D/2]
+
+
+def make_rope_inputs(T: int, NH: int, D: int, max_pos: int = 8192, seed: int = 0,
+                     device="cpu", base: float = 10000.0) -> RopeInputs:
+    g = torch.Generator(device="cpu").manual_seed(seed * 7919 + T)
+    x = torch.randn(T, NH, D, generator=g, dtype=torch.float32).to(torch.bfloat16)
+    positions = torch.randint(0, max_pos, (T,), generator=g, dtype=torch.int64).to(torch.int32)
+    inv_freq = base ** (-torch.arange(0, D // 2, dtype=torch.float64) * 2.0 / D)
+    ang = torch.arange(max_pos, dtype=torch.float64)[:, None] * inv_freq[None, :]
+    return RopeInputs(x.to(device), positions.to(device), torch.cos(ang).float().to(device),
+                      torch.sin(ang).float().to(device))
+
+
 def workload(name: str) -> dict:
     return dict(WORKLOADS[name])
 
@@ -136,4 +160,5 @@ def ceil_div(a: int, b: int) -> int:
 
 
 __all__ = ["WORKLOADS", "Weights", "Activations", "make_weights", "make_activations",
-           "zipf_bias", "workload", "weight_bytes_per_expert", "ceil_div"]
+           "zipf_bias", "workload", "weight_bytes_per_expert", "ceil_div", "RopeInputs",
+           "make_rope_inputs"]

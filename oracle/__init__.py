@@ -63,6 +63,8 @@ def lib():
             L.oracle_moe_forward.argtypes = [P, P, P, P, P, P, i, i, i, i, i, i, i, P, i, P, P, P,
                                              P, P, P, i]
             L.oracle_moe_forward.restype = ctypes.c_int
+            L.oracle_inv_rope_quant.argtypes = [P, P, P, P, i, i, i, i, P, P, P]
+            L.oracle_inv_rope_quant.restype = i
             L.oracle_max_threads.argtypes = []
             L.oracle_max_threads.restype = ctypes.c_int
             _lib = L
@@ -196,6 +198,26 @@ def moe_forward(x, logits, w13, w2, w13_scale, w2_scale, top_k: int, renormalize
         raise RuntimeError(f"oracle_moe_forward failed ({rc})")
     return dict(out=out[:n_rows], ids=ids[:P].reshape(T, top_k), weights=w[:P].reshape(T, top_k),
                 counts=counts, s_x=float(sx[0]), s_h=float(sh[0]))
+
+
+def inv_rope_quant(x, positions, cos_tab, sin_tab):
+    """Inverse rotary embedding + per-head E4M3 quantisation (the oracle's
+    reading of the pages' fused inverse-RoPE / per-head FP8 kernel).
+    x: bf16 [T, NH, D]; positions: int [T]; cos_tab, sin_tab: fp32 [max_pos, D/2].
+    -> dict(codes uint8 [T, NH, D], scales fp32 [NH], y fp32 [T, NH, D])."""
+    xb = _np(x, np.uint16)
+    T, NH, D = xb.shape
+    pos = np.ascontiguousarray(np.asarray(positions, dtype=np.int32))
+    c = np.ascontiguousarray(np.asarray(cos_tab, dtype=np.float32))
+    sn = np.ascontiguousarray(np.asarray(sin_tab, dtype=np.float32))
+    codes = np.zeros((T, NH, D), np.uint8)
+    scales = np.zeros(NH, np.float32)
+    y = np.zeros((T, NH, D), np.float32)
+    rc = lib().oracle_inv_rope_quant(_ptr(xb), _ptr(pos), _ptr(c), _ptr(sn), T, NH, D, c.shape[0],
+                                     _ptr(codes), _ptr(scales), _ptr(y))
+    if rc != 0:
+        raise ValueError("odd head size or position outside the tables")
+    return dict(codes=codes, scales=scales, y=y)
 
 
 def max_threads() -> int:

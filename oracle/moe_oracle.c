@@ -356,6 +356,68 @@ int oracle_moe_forward(const uint16_t* x, const float* logits, const void* w13, 
   return 0;
 }
 
+/* ------------------------------------------------------------------ */
+/* Inverse rotary position embedding + per-head FP8 quantisation       */
+/* ------------------------------------------------------------------ */
+/* The pages name one more kernel, _fused_inv_rope_fp8_quant_per_head
+ * (section "Triton JIT recompilation elimination": it fuses rotary position
+ * embedding with FP8 quantisation and was recompiled for every new number of
+ * tokens), and give none of its arithmetic.  Reading taken here:
+ *   rotary embedding: the RoFormer rotation of the consecutive pairs
+ *     (2i, 2i+1) of each head vector by the angle pos * theta_i; the caller
+ *     supplies cos and sin of those angles per position ([max_pos][D/2]
+ *     each, fp32), so every implementation rotates with the same values;
+ *   inverse: rotation by the negated angle,
+ *     y[2i]   = x[2i] c + x[2i+1] s,   y[2i+1] = x[2i+1] c - x[2i] s,
+ *     each product rounded to fp32, then the sum or difference;
+ *   per-head FP8: one dynamic scale per head over all tokens,
+ *     s_h = amax over tokens and dims of |y[., h, .]| / 448 (1 if 0),
+ *     code = E4M3(fp32(y) / s_h), the division in IEEE fp32.
+ * x: bf16 [T][NH][D]; pos: int32 [T] in [0, max_pos); codes: [T][NH][D];
+ * scales: [NH]; y (optional): the rotated values, fp32 [T][NH][D].
+ * Returns 0, or -1 for an odd D or a position outside the tables. */
+int oracle_inv_rope_quant(const uint16_t* x, const int32_t* pos, const float* cos_tab,
+                          const float* sin_tab, int T, int NH, int D, int max_pos,
+                          uint8_t* codes, float* scales, float* y) {
+  if (D % 2 != 0) return -1;
+  for (int t = 0; t < T; ++t)
+    if (pos[t] < 0 || pos[t] >= max_pos) return -1;
+  const int half = D / 2;
+  const long n = (long)T * NH * D;
+  float* yy = y ? y : (float*)malloc(sizeof(float) * (size_t)(n > 0 ? n : 1));
+  if (!yy) return -1;
+  for (int t = 0; t < T; ++t)
+    for (int h = 0; h < NH; ++h)
+      for (int i = 0; i < half; ++i) {
+        const long at = ((long)t * NH + h) * D + 2 * i;
+        const float x0 = (float)bf16_bits_to_double(x[at]);
+        const float x1 = (float)bf16_bits_to_double(x[at + 1]);
+        const float c = cos_tab[(long)pos[t] * half + i];
+        const float sn = sin_tab[(long)pos[t] * half + i];
+        const float a = x0 * c, b = x1 * sn;  /* each product rounded to fp32 */
+        const float d = x1 * c, e = x0 * sn;
+        yy[at] = a + b;
+        yy[at + 1] = d - e;
+      }
+  for (int h = 0; h < NH; ++h) {
+    float amax = 0.0f;
+    for (int t = 0; t < T; ++t)
+      for (int j = 0; j < D; ++j) {
+        const float v = fabsf(yy[((long)t * NH + h) * D + j]);
+        if (v > amax) amax = v;
+      }
+    scales[h] = act_scale_from_amax(amax);
+  }
+  for (int t = 0; t < T; ++t)
+    for (int h = 0; h < NH; ++h)
+      for (int j = 0; j < D; ++j) {
+        const long at = ((long)t * NH + h) * D + j;
+        codes[at] = quantize(yy[at], scales[h]);
+      }
+  if (!y) free(yy);
+  return 0;
+}
+
 int oracle_max_threads(void) {
 #ifdef _OPENMP
   return omp_get_max_threads();
