@@ -58,6 +58,9 @@ def parse():
                     help="first-call vs steady-state time for every T in 1..--max-tokens "
                          "in one process, plus CUDA-graph capture per T bucket")
     ap.add_argument("--max-tokens", type=int, default=8192)
+    ap.add_argument("--rope", action="store_true",
+                    help="time the inverse rotary embedding + per-head FP8 quantisation "
+                         "kernel (32 heads of 128, T in 1..8192) instead of the layer")
     ap.add_argument("--placement", default="auto", choices=["auto", "weights", "tokens"],
                     help="MMA operand placement of both expert GEMMs: weight rows in M (the "
                          "swap), tokens in M (ablation), or the library's default choice")
@@ -645,9 +648,76 @@ def run_shape_sweep(args, rank, local_rank):
     print(json.dumps(line), flush=True)
 
 
+# --------------------------------------------------------------------------- inverse RoPE
+def run_rope(args, rank, local_rank):
+    """Inverse rotary embedding + per-head E4M3 quantisation of [T, 32, 128]
+    head vectors (max position 8192).  Four copies of the inputs rotate call
+    to call, so the 64 MB inputs of T=8192 do not stay in L2."""
+    import torch
+    import mixture_experts_layer_align_gb300 as moe
+    from mixture_experts_layer_align_gb300 import inputs
+
+    if rank != 0:
+        return
+    moe.load()
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    NH, D, max_pos = 32, 128, 8192
+    hbm_peak, _, peak_kind = measured_peaks()
+    K = max(args.steps // 10, 20)
+    sweep = []
+    for T in (1, 64, 1024, 8192):
+        cps = [inputs.make_rope_inputs(T, NH, D, max_pos, seed=c, device=dev) for c in range(4)]
+        codes = torch.empty(T, NH, D, dtype=torch.uint8, device=dev)
+        scales = torch.empty(NH, dtype=torch.float32, device=dev)
+        scratch = torch.empty(moe.moe_inv_rope_scratch_size(T, NH, D), dtype=torch.uint8,
+                              device=dev)
+
+        def call(i):
+            r = cps[i % 4]
+            moe.moe_inv_rope_quant_per_head(r.x, r.positions, r.cos, r.sin, codes, scales,
+                                            scratch)
+
+        for i in range(max(args.warmup, 3)):
+            call(i)
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for i in range(K):
+            call(i)
+        e1.record()
+        torch.cuda.synchronize()
+        if moe.moe_check_status(scratch) != 0:
+            raise RuntimeError("device status")
+        us = e0.elapsed_time(e1) * 1e3 / K
+        # algorithmic bytes: x once, codes, positions, the cos/sin rows used, scales
+        nbytes = T * NH * D * 2 + T * NH * D + T * 4 + T * D * 4 + NH * 4
+        sweep.append({"T": T, "us_per_call": round(us, 2), "tokens_per_s": round(T / (us * 1e-6), 1),
+                      "algorithmic_bytes": nbytes,
+                      "hbm_frac": round(nbytes / (us * 1e-6) / 1e9 / hbm_peak, 4)})
+    big = sweep[-1]
+    line = {"metric": "inverse-RoPE + per-head FP8 quant tokens/s (32 heads x 128)",
+            "value": big["tokens_per_s"], "unit": "tokens/s", "steps": K, "warmup": args.warmup,
+            "config": {"workload": "x bf16 [T, 32, 128], positions < 8192, fp32 cos/sin tables; "
+                                   "two kernels (per-head amax, quantise)",
+                       "l2": "four input copies rotate call to call"},
+            "sweep": sweep,
+            "roofline": {"bound": "hbm", "achieved": round(big["algorithmic_bytes"] /
+                                                           (big["us_per_call"] * 1e-6) / 1e9, 1),
+                         "peak": hbm_peak, "peak_kind": f"{peak_kind} hbm_gbs", "unit": "GB/s",
+                         "frac": big["hbm_frac"],
+                         "note": "x is read twice (amax pass, quantise pass); the algorithmic "
+                                 "bytes count it once"}}
+    print(json.dumps(line), flush=True)
+
+
 def main():
     args = parse()
     rank, local_rank, world = dist_env()
+    if args.rope:
+        run_rope(args, rank, local_rank)
+        return
     if args.shape_sweep:
         run_shape_sweep(args, rank, local_rank)
         return

@@ -127,6 +127,35 @@ moe_status_t moe_quantize_e4m3(const void* x, int T, int H, uint8_t* x_q, float*
 moe_status_t moe_quantize_e4m3_noalloc(const void* x, int T, int H, uint8_t* x_q, float* scale,
                                        moe_stream_t stream);
 
+/*
+ * Inverse rotary position embedding + per-head FP8 quantisation (the fused
+ * kernel named in section "Triton JIT recompilation elimination", whose
+ * arithmetic the pages leave open; read here as):
+ *   y[2i]   = x[2i] c + x[2i+1] s,   y[2i+1] = x[2i+1] c - x[2i] s
+ *     (RoFormer's pair rotation by the negated angle; c, s = cos_tab/sin_tab
+ *     [positions[t]][i]; each product rounded to fp32, then the sum),
+ *   scales[h] = amax over tokens and dims of |y[., h, .]| / 448 (1 if 0),
+ *   codes = E4M3_rne_satfinite(y / scales[h]) (IEEE fp32 division).
+ *   x          bf16 [T, NH, D]
+ *   positions  int32 [T], each in [0, max_pos)
+ *   cos_tab    fp32 [max_pos, D/2]; sin_tab fp32 [max_pos, D/2]
+ *   codes      uint8 [T, NH, D]  out
+ *   scales     fp32 [NH]         out
+ *   scratch    moe_inv_rope_scratch_size(T, NH, D) bytes, 256-byte aligned; its
+ *              first word is the status word moe_check_status() reads
+ *              (MOE_ERR_DEVICE_RANGE: a position outside the tables, treated
+ *              as 0)
+ * Requires T >= 0 (0 enqueues nothing), 1 <= NH <= 4096, D in {8, 16, 32, 64,
+ * 128, 256}, max_pos >= 1, 16-byte aligned x / cos_tab / sin_tab, 8-byte
+ * aligned codes.  Two kernels on `stream`; all sizes are runtime values.
+ */
+size_t moe_inv_rope_scratch_size(int T, int NH, int D);
+moe_status_t moe_inv_rope_quant_per_head(const void* x, const int32_t* positions,
+                                         const float* cos_tab, const float* sin_tab, int T,
+                                         int NH, int D, int max_pos, uint8_t* codes,
+                                         float* scales, void* scratch, size_t scratch_bytes,
+                                         moe_stream_t stream);
+
 /* Arguments of the fused layer forward. */
 typedef struct {
   const void* x;             /* bf16 [T, H] */

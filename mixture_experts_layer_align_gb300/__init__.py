@@ -81,6 +81,9 @@ def load():
         L.moe_quantize_scratch_size.restype = sz
         L.moe_quantize_e4m3.argtypes = [P, i, i, P, P, P, sz, P]
         L.moe_quantize_e4m3_noalloc.argtypes = [P, i, i, P, P, P]
+        L.moe_inv_rope_scratch_size.argtypes = [i, i, i]
+        L.moe_inv_rope_scratch_size.restype = sz
+        L.moe_inv_rope_quant_per_head.argtypes = [P, P, P, P, i, i, i, i, P, P, P, sz, P]
         L.moe_quantize_e4m3_noalloc.restype = ctypes.c_int
         L.moe_fused_trace_offset.argtypes = [i, i, i, i, i, i]
         L.moe_fused_trace_offset.restype = sz
@@ -207,6 +210,42 @@ def moe_quantize_e4m3_noalloc(x, x_q=None, scale=None, stream=None):
     return x_q, scale
 
 
+def moe_inv_rope_scratch_size(T: int, NH: int, D: int) -> int:
+    return int(load().moe_inv_rope_scratch_size(T, NH, D))
+
+
+def moe_inv_rope_quant_per_head(x, positions, cos_tab, sin_tab, codes=None, scales=None,
+                                scratch=None, stream=None):
+    """Inverse rotary embedding of each head vector, then one dynamic E4M3
+    scale per head.  x: bf16 [T, NH, D]; positions: int32 [T]; cos_tab,
+    sin_tab: fp32 [max_pos, D/2].  Returns (codes uint8 [T, NH, D], scales fp32
+    [NH]); `scratch` (uint8, moe_inv_rope_scratch_size bytes) may be passed in."""
+    import torch
+    _require(x, torch.bfloat16, "x")
+    T, NH, D = x.shape
+    _require(positions, torch.int32, "positions", (T,))
+    _require(cos_tab, torch.float32, "cos_tab")
+    max_pos = cos_tab.shape[0]
+    _require(cos_tab, torch.float32, "cos_tab", (max_pos, D // 2))
+    _require(sin_tab, torch.float32, "sin_tab", (max_pos, D // 2))
+    if codes is None:
+        codes = torch.empty(T, NH, D, dtype=torch.uint8, device=x.device)
+    if scales is None:
+        scales = torch.empty(NH, dtype=torch.float32, device=x.device)
+    _require(codes, torch.uint8, "codes", (T, NH, D))
+    _require(scales, torch.float32, "scales", (NH,))
+    n = moe_inv_rope_scratch_size(T, NH, D)
+    if n == 0:
+        raise MoeError(1, "moe_inv_rope_scratch_size")
+    if scratch is None:
+        scratch = torch.empty(n, dtype=torch.uint8, device=x.device)
+    _check(load().moe_inv_rope_quant_per_head(_ptr(x), _ptr(positions), _ptr(cos_tab),
+                                              _ptr(sin_tab), T, NH, D, max_pos, _ptr(codes),
+                                              _ptr(scales), _ptr(scratch), scratch.numel(),
+                                              _stream(stream)), "moe_inv_rope_quant_per_head")
+    return codes, scales, scratch
+
+
 def moe_fused_workspace_size(T: int, H: int, I: int, E: int, top_k: int, dtype: int) -> int:
     return int(load().moe_fused_workspace_size(T, H, I, E, top_k, dtype))
 
@@ -318,7 +357,8 @@ def moe_check_status(workspace, stream=None) -> int:
 
 
 __all__ = ["load", "moe_route_topk", "moe_align_by_expert", "moe_quantize_e4m3",
-           "moe_fused_workspace_size", "moe_fused_launch_count", "moe_fused_forward", "moe_check_status", "alloc_workspace",
+           "moe_fused_workspace_size", "moe_fused_launch_count", "moe_inv_rope_scratch_size",
+           "moe_inv_rope_quant_per_head", "moe_fused_forward", "moe_check_status", "alloc_workspace",
            "status_string", "MoeError", "make_step_events", "MoeFusedArgs", "MOE_DT_BF16", "MOE_DT_FP8_E4M3",
            "MOE_DEBUG_FORCE_TIMEOUT", "MOE_FLAG_TOKENS_IN_M",
            "MOE_FLAG_WEIGHTS_IN_M", "LIB_PATH"]

@@ -145,6 +145,15 @@ cudaError_t launch_finalize(const float* acc, __nv_bfloat16* out, long long n, i
 cudaError_t launch_quantize_e4m3(const __nv_bfloat16* x, long long n, uint8_t* xq, float* scale,
                                  float* partials, int n_partials, cudaStream_t st);
 
+// ------------------------------------------------------------ inverse RoPE + FP8
+constexpr int kRopeMaxCtas = 1024;
+int rope_grid(long long T, int NH, int D, int num_sms);
+// partials: (grid * (NH + 1)) floats of scratch; ctrl->err gets the status.
+cudaError_t launch_inv_rope_quant(const __nv_bfloat16* x, const int32_t* pos, const float* cos_t,
+                                  const float* sin_t, int T, int NH, int D, int max_pos,
+                                  uint8_t* codes, float* scales, Ctrl* ctrl, float* partials,
+                                  int num_sms, cudaStream_t st);
+
 // ------------------------------------------------------------ grouped GEMM
 struct GemmParams {
   // Row tiles {expert, first row, rows | (tiles of this expert << 12), index of

@@ -279,6 +279,36 @@ moe_status_t moe_quantize_e4m3(const void* x, int T, int H, uint8_t* x_q, float*
              : MOE_ERR_CUDA;
 }
 
+size_t moe_inv_rope_scratch_size(int T, int NH, int D) {
+  if (T < 0 || NH < 1 || NH > 4096 || D < 8 || D > 256 || (D & (D - 1)) != 0) return 0;
+  return 256 + sizeof(float) * static_cast<size_t>(kRopeMaxCtas) * (NH + 1);
+}
+
+moe_status_t moe_inv_rope_quant_per_head(const void* x, const int32_t* positions,
+                                         const float* cos_tab, const float* sin_tab, int T,
+                                         int NH, int D, int max_pos, uint8_t* codes,
+                                         float* scales, void* scratch, size_t scratch_bytes,
+                                         moe_stream_t stream) {
+  const size_t need = moe_inv_rope_scratch_size(T, NH, D);
+  if (need == 0 || max_pos < 1) return MOE_ERR_INVALID_ARG;
+  if (T == 0) return MOE_OK;
+  if (!x || !positions || !cos_tab || !sin_tab || !codes || !scales) return MOE_ERR_INVALID_ARG;
+  if (!aligned(x, 16) || !aligned(cos_tab, 16) || !aligned(sin_tab, 16) || !aligned(codes, 8) ||
+      !aligned(positions, 4) || !aligned(scales, 4))
+    return MOE_ERR_INVALID_ARG;
+  if (!scratch || !aligned(scratch, 256) || scratch_bytes < need) return MOE_ERR_WORKSPACE;
+  DeviceInfo dev;
+  moe_status_t st = check_device(&dev);
+  if (st != MOE_OK) return st;
+  uint8_t* ws = static_cast<uint8_t*>(scratch);
+  return launch_inv_rope_quant(static_cast<const __nv_bfloat16*>(x), positions, cos_tab, sin_tab,
+                               T, NH, D, max_pos, codes, scales, reinterpret_cast<Ctrl*>(ws),
+                               reinterpret_cast<float*>(ws + 256), dev.num_sms,
+                               stream) == cudaSuccess
+             ? MOE_OK
+             : MOE_ERR_CUDA;
+}
+
 size_t moe_fused_workspace_size(int T, int H, int I, int E, int top_k, moe_dtype_t dtype) {
   if (T < 0 || H <= 0 || I <= 0 || E < 1 || E > kMaxExperts || top_k < 1 || top_k > E) return 0;
   if (dtype != MOE_DT_BF16 && dtype != MOE_DT_FP8_E4M3) return 0;

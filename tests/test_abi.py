@@ -68,6 +68,19 @@ def test_launch_count(lib):
     assert moe.moe_fused_launch_count(4, 128, 256, 8, 9, fp8) == -1
 
 
+def test_inv_rope_argument_checks(lib):
+    assert moe.moe_inv_rope_scratch_size(8, 4, 128) > 0
+    assert moe.moe_inv_rope_scratch_size(8, 4, 96) == 0     # head size not a power of two
+    assert moe.moe_inv_rope_scratch_size(8, 0, 128) == 0
+    f = lib.moe_inv_rope_quant_per_head
+    assert f(None, None, None, None, 0, 4, 64, 16, None, None, None, 0, None) == 0  # T = 0
+    assert f(None, None, None, None, 4, 4, 64, 16, None, None, None, 0, None) == 1
+    assert f(ctypes.c_void_p(16), ctypes.c_void_p(16), ctypes.c_void_p(16), ctypes.c_void_p(16),
+             4, 4, 64, 0, ctypes.c_void_p(16), ctypes.c_void_p(16), None, 0, None) == 1  # max_pos
+    assert f(ctypes.c_void_p(16), ctypes.c_void_p(16), ctypes.c_void_p(16), ctypes.c_void_p(16),
+             4, 4, 64, 16, ctypes.c_void_p(16), ctypes.c_void_p(16), None, 0, None) == 3  # scratch
+
+
 def _args(**kw):
     base = dict(x=16, router_logits=16, w13=16, w2=16, w13_scale=16, w2_scale=16,
                 weight_dtype=1, T=4, H=128, I=256, E=8, top_k=2, renormalize=1, out=16,

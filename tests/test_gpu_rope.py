@@ -1,0 +1,54 @@
+"""GPU parity of the inverse rotary embedding + per-head FP8 quantisation
+against the CPU oracle: codes and scales bit-exact (both sides round the same
+fp32 products and sums and divide in IEEE fp32), at shapes with ragged token
+counts, every supported head size, and a position outside the tables."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from mixture_experts_layer_align_gb300 import inputs
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.mark.parametrize("T,NH,D,max_pos", [
+    (1, 1, 8, 4), (37, 6, 64, 512), (257, 8, 128, 4096), (1000, 3, 256, 2048),
+    (129, 5, 16, 64), (4096, 32, 128, 8192), (8192, 8, 32, 8192),
+])
+def test_inv_rope_quant_matches_oracle(gpu_lib, T, NH, D, max_pos):
+    r = inputs.make_rope_inputs(T, NH, D, max_pos, seed=T)
+    ref = oracle.inv_rope_quant(r.x, r.positions, r.cos, r.sin)
+    codes, scales, scratch = gpu_lib.moe_inv_rope_quant_per_head(
+        r.x.cuda(), r.positions.cuda(), r.cos.cuda(), r.sin.cuda())
+    assert gpu_lib.moe_check_status(scratch) == 0
+    assert np.array_equal(scales.cpu().numpy(), ref["scales"])
+    assert np.array_equal(codes.cpu().numpy(), ref["codes"])
+
+
+def test_zero_head_and_repeat_calls(gpu_lib):
+    r = inputs.make_rope_inputs(64, 4, 64, 128, seed=9)
+    x = r.x.clone()
+    x[:, 2, :] = 0
+    ref = oracle.inv_rope_quant(x, r.positions, r.cos, r.sin)
+    args = (x.cuda(), r.positions.cuda(), r.cos.cuda(), r.sin.cuda())
+    for _ in range(2):  # the scratch and outputs of a previous call do not leak in
+        codes, scales, scratch = gpu_lib.moe_inv_rope_quant_per_head(*args)
+        assert np.array_equal(scales.cpu().numpy(), ref["scales"])
+        assert np.array_equal(codes.cpu().numpy(), ref["codes"])
+
+
+def test_position_outside_tables_is_reported(gpu_lib):
+    r = inputs.make_rope_inputs(16, 2, 32, 64, seed=10)
+    pos = r.positions.clone()
+    pos[3] = 64  # one past the tables: read as position 0, status word set
+    codes, scales, scratch = gpu_lib.moe_inv_rope_quant_per_head(
+        r.x.cuda(), pos.cuda(), r.cos.cuda(), r.sin.cuda())
+    assert gpu_lib.moe_check_status(scratch) == 6  # MOE_ERR_DEVICE_RANGE
+    pos[3] = 0
+    ref = oracle.inv_rope_quant(r.x, pos, r.cos, r.sin)
+    assert np.array_equal(codes.cpu().numpy(), ref["codes"])
+    # the next good call clears the status
+    _, _, scratch = gpu_lib.moe_inv_rope_quant_per_head(
+        r.x.cuda(), pos.cuda(), r.cos.cuda(), r.sin.cuda(), scratch=scratch)
+    assert gpu_lib.moe_check_status(scratch) == 0
