@@ -112,6 +112,21 @@ def recorded_traffic(workload, Ts):
         return None
 
 
+def max_over_ranks(ms: float, dist=None, device="cpu") -> float:
+    """The slowest rank's time (each rank runs one independent replica)."""
+    if dist is None:
+        return ms
+    import torch
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tokens_per_s(world: int, tokens_per_step: int, steps: int, ms: float) -> float:
+    """Whole-job throughput: every replica processed steps x tokens_per_step."""
+    return world * tokens_per_step * steps / (ms * 1e-3)
+
+
 class ClockSampler:
     """nvidia-smi clock/throttle samples while the timed region runs."""
 
@@ -354,12 +369,8 @@ def run_ours(args, rank, local_rank, world):
         clk.mark(False)
     if dist is not None:
         dist.barrier()
-    elapsed_ms = start.elapsed_time(stop)
+    elapsed_ms = max_over_ranks(start.elapsed_time(stop), dist, dev)
     instrumented_ms = mid.elapsed_time(end2)
-    if dist is not None:
-        t = torch.tensor([elapsed_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        elapsed_ms = float(t.item())
     clocks = clk.summary()
 
     # per-step (kernel) durations from the events inside the timed region
@@ -407,7 +418,7 @@ def run_ours(args, rank, local_rank, world):
                     "tensor_frac": round(achieved_tfs / tc_peak, 4)}
 
     tokens_per_step = sum(Ts)
-    value = world * tokens_per_step * K / (elapsed_ms * 1e-3)
+    value = job_tokens_per_s(world, tokens_per_step, K, elapsed_ms)
     sweep = []
     for T in Ts:
         us = statistics.median(per_T_call_us[T])
@@ -453,12 +464,8 @@ def run_ours(args, rank, local_rank, world):
             e2e_step(s)
         s1.record()
         torch.cuda.synchronize()
-        e_ms = s0.elapsed_time(s1)
-        if dist is not None:
-            t = torch.tensor([e_ms], device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            e_ms = float(t.item())
-        e2e = {"value": world * tokens_per_step * K / (e_ms * 1e-3), "unit": "tokens/s",
+        e_ms = max_over_ranks(s0.elapsed_time(s1), dist, dev)
+        e2e = {"value": job_tokens_per_s(world, tokens_per_step, K, e_ms), "unit": "tokens/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
 
     cpu = None
