@@ -292,6 +292,7 @@ moe_status_t moe_inv_rope_quant_per_head(const void* x, const int32_t* positions
   const size_t need = moe_inv_rope_scratch_size(T, NH, D);
   if (need == 0 || max_pos < 1) return MOE_ERR_INVALID_ARG;
   if (T == 0) return MOE_OK;
+  if (static_cast<long long>(T) * NH * D >= (1ll << 31)) return MOE_ERR_UNSUPPORTED;
   if (!x || !positions || !cos_tab || !sin_tab || !codes || !scales) return MOE_ERR_INVALID_ARG;
   if (!aligned(x, 16) || !aligned(cos_tab, 16) || !aligned(sin_tab, 16) || !aligned(codes, 8) ||
       !aligned(positions, 4) || !aligned(scales, 4))

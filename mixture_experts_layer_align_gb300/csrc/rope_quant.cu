@@ -15,16 +15,17 @@
 // Shapes are runtime values: one binary for every T, head count and (power of
 // two) head size.
 //
-// Two passes over x (bf16 [T][NH][D]):
-//   1. rope_amax_kernel: rotate, per-head maxima of |y| per CTA -> partials;
-//   2. rope_quant_kernel: every CTA folds the partials into the NH scales,
-//      rotates again and writes the codes (CTA 0 also writes the scales and
-//      the status word).
-// A thread takes 8 elements (4 pairs) of one head vector: one 16-byte load
-// of x, 16-byte loads of the 4 cosines and 4 sines, one 8-byte store of codes.
-// A group of D/8 lanes covers one head vector, so a warp covers 32/(D/8)
-// consecutive (token, head) rows and the per-head maxima reduce inside each
-// group before one shared-memory atomic per group.
+// Two passes over x (bf16 [T][NH][D]), three launches:
+//   1. rope_pass_kernel<false>: per-head maxima of |y| per CTA -> partials;
+//   2. rope_fold_kernel (one CTA): the NH scales and the status word;
+//   3. rope_pass_kernel<true>: rotate again, divide by the head's scale,
+//      write the codes.
+// A warp takes one token at a time: one load of its position and of the
+// cos/sin entries of its lane's 4 pairs, then the token's heads, 32/(D/8) per
+// iteration (a group of D/8 lanes per head vector, 8 elements per lane: one
+// 16-byte load of x, one 8-byte store of codes), several iterations' loads in
+// flight.  Per-head maxima reduce inside each group, then one shared-memory
+// atomic per group.
 #include <cuda_bf16.h>
 #include <stdint.h>
 
@@ -34,29 +35,14 @@
 namespace moe {
 namespace {
 
-constexpr int kRopeThreads = 256;
+constexpr int kRopeThreads = 256;  // 8 warps: 8 tokens at a time per CTA
+constexpr int kRopeBatch = 4;      // head iterations whose x loads are in flight together
 
 __device__ __forceinline__ float lo16(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float hi16(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
 
-// The 8 rotated values of one thread item.  Positions outside the tables are
-// clamped to 0 and reported through *bad.
-__device__ __forceinline__ void rotate8(const __nv_bfloat16* __restrict__ x,
-                                        const int32_t* __restrict__ pos,
-                                        const float* __restrict__ cos_t,
-                                        const float* __restrict__ sin_t, int NH, int D,
-                                        int max_pos, long long row, int c8, float (&y)[8],
-                                        int* bad) {
-  const int t = static_cast<int>(row / NH);
-  int p = pos[t];
-  if (p < 0 || p >= max_pos) {
-    *bad = 1;
-    p = 0;
-  }
-  const uint4 v = *reinterpret_cast<const uint4*>(x + row * D + c8 * 8);
-  const size_t tab = static_cast<size_t>(p) * (D / 2) + c8 * 4;
-  const float4 c = *reinterpret_cast<const float4*>(cos_t + tab);
-  const float4 s = *reinterpret_cast<const float4*>(sin_t + tab);
+// 4 pairs of one head vector rotated by the negated angles (cos c, sin s).
+__device__ __forceinline__ void rotate8(uint4 v, float4 c, float4 s, float (&y)[8]) {
   const float xs[8] = {lo16(v.x), hi16(v.x), lo16(v.y), hi16(v.y),
                        lo16(v.z), hi16(v.z), lo16(v.w), hi16(v.w)};
   const float cs[4] = {c.x, c.y, c.z, c.w};
@@ -69,92 +55,126 @@ __device__ __forceinline__ void rotate8(const __nv_bfloat16* __restrict__ x,
   }
 }
 
+// kQuant = false: per-CTA per-head maxima of |y| into partials [NH][grid]
+// (head-major, so the fold reads each head's maxima contiguously), then one
+// flag per CTA (a position outside the tables, treated as 0) after them.
+// kQuant = true: codes with the per-head scales.
+template <bool kQuant>
 __global__ void __launch_bounds__(kRopeThreads)
-    rope_amax_kernel(const __nv_bfloat16* __restrict__ x, const int32_t* __restrict__ pos,
+    rope_pass_kernel(const __nv_bfloat16* __restrict__ x, const int32_t* __restrict__ pos,
                      const float* __restrict__ cos_t, const float* __restrict__ sin_t, int T,
-                     int NH, int D, int max_pos, float* __restrict__ partials) {
-  extern __shared__ unsigned s_amax[];  // [NH] bits of max|y| (non-negative floats order like uints)
+                     int NH, int D, int max_pos, float* __restrict__ partials,
+                     const float* __restrict__ scales, uint8_t* __restrict__ codes) {
+  extern __shared__ unsigned s_head[];  // [NH]: max|y| bits, or the scales
   __shared__ int s_bad;
   pdl_wait();
   pdl_trigger();
-  for (int h = threadIdx.x; h < NH; h += blockDim.x) s_amax[h] = 0u;
+  for (int h = threadIdx.x; h < NH; h += blockDim.x)
+    s_head[h] = kQuant ? __float_as_uint(scales[h]) : 0u;
   if (threadIdx.x == 0) s_bad = 0;
   __syncthreads();
-  const int n8 = D / 8;                 // lanes per head vector (a power of two <= 32)
-  const long long items = static_cast<long long>(T) * NH * n8;
-  const long long step = static_cast<long long>(gridDim.x) * blockDim.x;
+  const int lane = threadIdx.x & 31;
+  const int n8 = D >> 3;              // lanes per head vector (a power of two <= 32)
+  const int lg8 = __ffs(n8) - 1;
+  const int hp = 32 >> lg8;           // head vectors per warp iteration
+  const int c8 = lane & (n8 - 1);
+  const int hoff = lane >> lg8;
+  const int nwarps = gridDim.x * (blockDim.x >> 5);
   int bad = 0;
-  // every lane of a warp runs the same number of iterations (the warp shuffle
-  // below needs all of them); out-of-range items contribute 0
-  const long long base0 = static_cast<long long>(blockIdx.x) * blockDim.x + (threadIdx.x & ~31);
-  for (long long b = base0; b < items; b += step) {
-    const long long i = b + (threadIdx.x & 31);
-    float m = 0.f;
-    long long row = 0;
-    if (i < items) {
-      row = i / n8;
-      float y[8];
-      rotate8(x, pos, cos_t, sin_t, NH, D, max_pos, row, static_cast<int>(i - row * n8), y, &bad);
-#pragma unroll
-      for (int j = 0; j < 8; ++j) m = fmaxf(m, fabsf(y[j]));
+  for (int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); t < T; t += nwarps) {
+    int p = pos[t];
+    if (p < 0 || p >= max_pos) {
+      bad = 1;
+      p = 0;
     }
-    // maximum over the n8 lanes of one head vector
-    for (int o = n8 >> 1; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-    if (i < items && ((threadIdx.x & 31) & (n8 - 1)) == 0 && m > 0.f)
-      atomicMax(&s_amax[static_cast<int>(row % NH)], __float_as_uint(m));
+    const size_t tab = static_cast<size_t>(p) * (D / 2) + c8 * 4;
+    const float4 c = *reinterpret_cast<const float4*>(cos_t + tab);
+    const float4 s = *reinterpret_cast<const float4*>(sin_t + tab);
+    const size_t row0 = static_cast<size_t>(t) * NH;
+    // kRopeBatch iterations' loads of x are issued before any is used
+    for (int hb = 0; hb < NH; hb += hp * kRopeBatch) {
+      uint4 v[kRopeBatch];
+#pragma unroll
+      for (int u = 0; u < kRopeBatch; ++u) {
+        const int h = hb + u * hp + hoff;
+        v[u] = h < NH ? *reinterpret_cast<const uint4*>(x + (row0 + h) * D + c8 * 8)
+                      : make_uint4(0, 0, 0, 0);
+      }
+#pragma unroll
+      for (int u = 0; u < kRopeBatch; ++u) {
+        const int h = hb + u * hp + hoff;
+        float y[8];
+        rotate8(v[u], c, s, y);
+        float m = 0.f;
+        if (kQuant) {
+          if (h < NH) {
+            const float sc = __uint_as_float(s_head[h]);
+            uint2 q;
+            q.x = static_cast<uint32_t>(cvt_e4m3x2(__fdiv_rn(y[0], sc), __fdiv_rn(y[1], sc))) |
+                  (static_cast<uint32_t>(cvt_e4m3x2(__fdiv_rn(y[2], sc), __fdiv_rn(y[3], sc))) << 16);
+            q.y = static_cast<uint32_t>(cvt_e4m3x2(__fdiv_rn(y[4], sc), __fdiv_rn(y[5], sc))) |
+                  (static_cast<uint32_t>(cvt_e4m3x2(__fdiv_rn(y[6], sc), __fdiv_rn(y[7], sc))) << 16);
+            *reinterpret_cast<uint2*>(codes + (row0 + h) * D + c8 * 8) = q;
+          }
+        } else {
+#pragma unroll
+          for (int j = 0; j < 8; ++j) m = fmaxf(m, fabsf(y[j]));
+          // maximum over the group of lanes of one head vector
+          for (int o = n8 >> 1; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+          if (c8 == 0 && h < NH && m > 0.f) atomicMax(&s_head[h], __float_as_uint(m));
+        }
+      }
+    }
   }
-  if (bad) s_bad = 1;
-  __syncthreads();
-  for (int h = threadIdx.x; h < NH; h += blockDim.x)
-    partials[static_cast<size_t>(blockIdx.x) * NH + h] = __uint_as_float(s_amax[h]);
-  if (threadIdx.x == 0) partials[static_cast<size_t>(gridDim.x) * NH + blockIdx.x] = s_bad ? 1.f : 0.f;
+  if (!kQuant) {
+    if (bad) s_bad = 1;
+    __syncthreads();
+    for (int h = threadIdx.x; h < NH; h += blockDim.x)
+      partials[static_cast<size_t>(h) * gridDim.x + blockIdx.x] = __uint_as_float(s_head[h]);
+    if (threadIdx.x == 0)
+      partials[static_cast<size_t>(gridDim.x) * NH + blockIdx.x] = s_bad ? 1.f : 0.f;
+  }
 }
 
-__global__ void __launch_bounds__(kRopeThreads)
-    rope_quant_kernel(const __nv_bfloat16* __restrict__ x, const int32_t* __restrict__ pos,
-                      const float* __restrict__ cos_t, const float* __restrict__ sin_t, int T,
-                      int NH, int D, int max_pos, const float* __restrict__ partials, int n_part,
-                      uint8_t* __restrict__ codes, float* __restrict__ scales, Ctrl* ctrl) {
-  extern __shared__ float s_scale[];  // [NH]
+// One CTA: a warp per head folds the per-CTA maxima into the head's scale;
+// the status word records a position outside the tables.
+__global__ void __launch_bounds__(1024)
+    rope_fold_kernel(const float* __restrict__ partials, int n_part, int NH,
+                     float* __restrict__ scales, Ctrl* ctrl) {
   pdl_wait();
   pdl_trigger();
-  for (int h = threadIdx.x; h < NH; h += blockDim.x) {
-    float a = 0.f;
-    for (int b = 0; b < n_part; ++b) a = fmaxf(a, partials[static_cast<size_t>(b) * NH + h]);
-    const float s = a > 0.f ? __fdiv_rn(a, 448.f) : 1.f;
-    s_scale[h] = s;
-    if (blockIdx.x == 0) scales[h] = s;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
+  for (int h = warp; h < NH; h += nwarps) {
+    const float* ph = partials + static_cast<size_t>(h) * n_part;
+    float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;  // independent chains: loads in flight
+    int b = lane;
+    for (; b + 96 < n_part; b += 128) {
+      a0 = fmaxf(a0, ph[b]);
+      a1 = fmaxf(a1, ph[b + 32]);
+      a2 = fmaxf(a2, ph[b + 64]);
+      a3 = fmaxf(a3, ph[b + 96]);
+    }
+    for (; b < n_part; b += 32) a0 = fmaxf(a0, ph[b]);
+    float a = fmaxf(fmaxf(a0, a1), fmaxf(a2, a3));
+    for (int o = 16; o > 0; o >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
+    if (lane == 0) scales[h] = a > 0.f ? __fdiv_rn(a, 448.f) : 1.f;
   }
-  if (blockIdx.x == 0 && threadIdx.x == 0) {
+  if (warp == 0) {
     int bad = 0;
-    for (int b = 0; b < n_part; ++b) bad |= partials[static_cast<size_t>(n_part) * NH + b] != 0.f;
-    ctrl->err = bad ? kDevErrRange : 0;
-  }
-  __syncthreads();
-  const int n8 = D / 8;
-  const long long items = static_cast<long long>(T) * NH * n8;
-  int bad = 0;
-  for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < items;
-       i += static_cast<long long>(gridDim.x) * blockDim.x) {
-    const long long row = i / n8;
-    float y[8];
-    rotate8(x, pos, cos_t, sin_t, NH, D, max_pos, row, static_cast<int>(i - row * n8), y, &bad);
-    const float s = s_scale[static_cast<int>(row % NH)];
-    uint2 q;
-    q.x = static_cast<uint32_t>(cvt_e4m3x2(__fdiv_rn(y[0], s), __fdiv_rn(y[1], s))) |
-          (static_cast<uint32_t>(cvt_e4m3x2(__fdiv_rn(y[2], s), __fdiv_rn(y[3], s))) << 16);
-    q.y = static_cast<uint32_t>(cvt_e4m3x2(__fdiv_rn(y[4], s), __fdiv_rn(y[5], s))) |
-          (static_cast<uint32_t>(cvt_e4m3x2(__fdiv_rn(y[6], s), __fdiv_rn(y[7], s))) << 16);
-    *reinterpret_cast<uint2*>(codes + i * 8) = q;
+    for (int b = lane; b < n_part; b += 32)
+      bad |= partials[static_cast<size_t>(n_part) * NH + b] != 0.f;
+    bad = __any_sync(0xffffffffu, bad);
+    if (lane == 0) ctrl->err = bad ? kDevErrRange : 0;
   }
 }
 
 }  // namespace
 
 int rope_grid(long long T, int NH, int D, int num_sms) {
-  const long long items = T * NH * (D / 8);
-  long long g = (items + kRopeThreads - 1) / kRopeThreads;
-  const long long cap = static_cast<long long>(num_sms) * 4;
+  (void)NH;
+  (void)D;
+  long long g = (T + (kRopeThreads / 32) - 1) / (kRopeThreads / 32);  // a warp per token
+  const long long cap = static_cast<long long>(num_sms) * 8;
   if (g > cap) g = cap;
   if (g > kRopeMaxCtas) g = kRopeMaxCtas;
   return static_cast<int>(g < 1 ? 1 : g);
@@ -166,12 +186,16 @@ cudaError_t launch_inv_rope_quant(const __nv_bfloat16* x, const int32_t* pos, co
                                   int num_sms, cudaStream_t st) {
   const int grid = rope_grid(T, NH, D, num_sms);
   const size_t smem = static_cast<size_t>(NH) * sizeof(float);
-  cudaError_t e = launch_pdl(rope_amax_kernel, dim3(grid), dim3(kRopeThreads), smem, st, x, pos,
-                             cos_t, sin_t, T, NH, D, max_pos, partials);
+  cudaError_t e = launch_pdl(rope_pass_kernel<false>, dim3(grid), dim3(kRopeThreads), smem, st, x,
+                             pos, cos_t, sin_t, T, NH, D, max_pos, partials,
+                             static_cast<const float*>(nullptr), static_cast<uint8_t*>(nullptr));
   if (e != cudaSuccess) return e;
-  return launch_pdl(rope_quant_kernel, dim3(grid), dim3(kRopeThreads), smem, st, x, pos, cos_t,
-                    sin_t, T, NH, D, max_pos, static_cast<const float*>(partials), grid, codes,
-                    scales, ctrl);
+  e = launch_pdl(rope_fold_kernel, dim3(1), dim3(1024), 0, st,
+                 static_cast<const float*>(partials), grid, NH, scales, ctrl);
+  if (e != cudaSuccess) return e;
+  return launch_pdl(rope_pass_kernel<true>, dim3(grid), dim3(kRopeThreads), smem, st, x, pos,
+                    cos_t, sin_t, T, NH, D, max_pos, static_cast<float*>(nullptr),
+                    static_cast<const float*>(scales), codes);
 }
 
 }  // namespace moe
