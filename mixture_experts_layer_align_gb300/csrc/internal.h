@@ -86,6 +86,7 @@ struct AlignParams {
   // fused-path extras (null when unused)
   const float* wts;      // [P] router weights (read when sorted_w is set)
   float* sorted_w;       // router weight of each aligned row, 0 for padding
+  int32_t* inv_slot;     // [P] aligned row of each pair, or null
   int4* mtiles;          // GEMM row tiles {expert, first row, rows, 0}
   int bn_max;            // max rows of one row tile
   int4* mtiles_w;        // second list of tiles of up to 256 rows, or null
@@ -98,6 +99,9 @@ int align_chunk();
 // Router + alignment in one CTA for small batches (decode).  Used when
 // T*k <= kSmallMaxPairs, E <= kSmallMaxExperts and T*H <= kSmallMaxXElems.
 constexpr int kSmallMaxPairs = 2048;
+// Above this many pairs: two-pass alignment (per-chunk histograms) and x
+// quantised once per token before a byte-copy gather.
+constexpr long long kLargePairs = 4096;
 constexpr int kSmallMaxExperts = 256;
 constexpr long long kSmallMaxXElems = 1ll << 19;
 struct SmallFrontParams {
@@ -123,18 +127,20 @@ cudaError_t launch_route_align_small(const SmallFrontParams& p, cudaStream_t st)
 // First pass of the two-pass alignment: expert histogram of each chunk of
 // align_chunk() pairs into hist[chunk][E].
 cudaError_t launch_align_hist(const int32_t* ids, int P, int E, int32_t* hist, cudaStream_t st);
-// x (bf16) -> E4M3 codes in token order with ctrl->s_x (large batches quantise
-// each token once, the gather then copies bytes).
-cudaError_t launch_quant_tokens(const __nv_bfloat16* x, long long n, const Ctrl* ctrl,
-                                uint8_t* xq, int num_sms, cudaStream_t st);
+// Large FP8 batches: each token row of x quantised once with ctrl->s_x and
+// written to its k aligned rows of xs (inv_slot[pair] = aligned row); padding
+// rows of every segment zeroed; the fp32 combine buffer zeroed (acc_elems may
+// be 0).
+cudaError_t launch_quant_scatter(const __nv_bfloat16* x, int T, int H, int k,
+                                 const int32_t* inv_slot, const int32_t* counts,
+                                 const int32_t* offsets, int E, const Ctrl* ctrl, uint8_t* xs,
+                                 float* acc, long long acc_elems, int num_sms, cudaStream_t st);
 
 // Gather the routed rows of x into aligned order (E4M3 with s_x, or bf16), zero
 // the fp32 combine buffer.
-// xq_tok: E4M3 codes of x in token order (FP8 path, large batches) or null.
-cudaError_t launch_gather_x(const __nv_bfloat16* x, const uint8_t* xq_tok, int H,
-                            const int32_t* sorted_ids, const Ctrl* ctrl, int P, int k, void* xs,
-                            bool fp8, float* acc, long long acc_elems, int max_rows, int num_sms,
-                            cudaStream_t st);
+cudaError_t launch_gather_x(const __nv_bfloat16* x, int H, const int32_t* sorted_ids,
+                            const Ctrl* ctrl, int P, int k, void* xs, bool fp8, float* acc,
+                            long long acc_elems, int max_rows, int num_sms, cudaStream_t st);
 // h (fp32) -> E4M3 with s_h = amax_h / 448 (stored into ctrl->s_h).
 cudaError_t launch_quant_h(const float* h, int I, Ctrl* ctrl, uint8_t* hq, int max_rows,
                            int num_sms, cudaStream_t st);

@@ -110,10 +110,10 @@ struct Layout {
   // separate kernel (large batches, where the reductions would saturate L2).
   bool combine_rows = false;
   size_t rows = 0;
-  // Large batches: two-pass alignment (per-chunk histograms) and x quantised
-  // once per token before the gather.
+  // Large batches: two-pass alignment (per-chunk histograms); FP8: x quantised
+  // once per token and scattered to its aligned rows (inv_slot: row of each pair).
   bool large = false;
-  size_t chunk_hist = 0, xq_tok = 0;
+  size_t chunk_hist = 0, inv_slot = 0;
   size_t ctrl = 0, trace = 0, partials = 0, ids = 0, wts = 0, counts = 0, offsets = 0,
          sorted = 0, sorted_w = 0, mtiles = 0, mtiles_w = 0, tile_cnt = 0, part = 0, xs = 0, h = 0, hq = 0, acc = 0,
          total = 0;
@@ -151,9 +151,9 @@ Layout make_layout(int T, int H, int I, int E, int k, bool fp8) {
   L.xs = take(static_cast<size_t>(L.pad_max) * H * (fp8 ? 1 : 2));
   L.h = take(static_cast<size_t>(L.pad_max) * I * (fp8 ? 4 : 2));
   L.hq = take(fp8 ? static_cast<size_t>(L.pad_max) * I : 0);
-  L.large = L.P > align_chunk();
+  L.large = L.P > kLargePairs;
   L.chunk_hist = take(L.large ? sizeof(int32_t) * E * ((L.P + align_chunk() - 1) / align_chunk()) : 0);
-  L.xq_tok = take(L.large && fp8 ? static_cast<size_t>(T) * H : 0);
+  L.inv_slot = take(L.large && fp8 ? sizeof(int32_t) * L.P : 0);
   L.combine_rows = L.P * H > (8ll << 20);
   L.acc = take(L.combine_rows ? 0 : static_cast<size_t>(T) * H * sizeof(float));
   L.rows = take(L.combine_rows ? static_cast<size_t>(L.P) * H * 2 : 0);
@@ -369,6 +369,7 @@ moe_status_t fused_forward_impl(const moe_fused_args* a, void* workspace, size_t
   int32_t* offsets = reinterpret_cast<int32_t*>(ws + L.offsets);
   int32_t* sorted = reinterpret_cast<int32_t*>(ws + L.sorted);
   float* sorted_w = reinterpret_cast<float*>(ws + L.sorted_w);
+  int32_t* inv_slot = reinterpret_cast<int32_t*>(ws + L.inv_slot);
   int4* mtiles = reinterpret_cast<int4*>(ws + L.mtiles);
   void* xs = ws + L.xs;
   void* h = ws + L.h;
@@ -444,6 +445,7 @@ moe_status_t fused_forward_impl(const moe_fused_args* a, void* workspace, size_t
   ap.sorted_ids = sorted;
   ap.wts = wts;
   ap.sorted_w = sorted_w;
+  ap.inv_slot = (L.large && fp8) ? inv_slot : nullptr;
   ap.tile_expert = nullptr;
   ap.num_padded = nullptr;
   ap.mtiles = mtiles;
@@ -461,16 +463,20 @@ moe_status_t fused_forward_impl(const moe_fused_args* a, void* workspace, size_t
   if (launch_align(ap, s) != cudaSuccess) return MOE_ERR_CUDA;
   if (events && cudaEventRecord(events[2], stream) != cudaSuccess) return MOE_ERR_CUDA;
   }
-  // 3. gather (+ quantise) the routed rows of x; zero the combine buffer
-  uint8_t* xq_tok = (L.large && fp8) ? ws + L.xq_tok : nullptr;
-  if (xq_tok && launch_quant_tokens(static_cast<const __nv_bfloat16*>(a->x),
-                                    static_cast<long long>(T) * H, ctrl, xq_tok, dev.num_sms,
-                                    s) != cudaSuccess)
+  // 3. the routed rows of x in aligned order, E4M3 with s_x (or bf16): large
+  //    FP8 batches quantise each token once and scatter it to its k rows,
+  //    smaller ones gather (and quantise) per aligned row; zero the combine
+  //    buffer
+  if (L.large && fp8) {
+    if (launch_quant_scatter(static_cast<const __nv_bfloat16*>(a->x), T, H, k, inv_slot, counts,
+                             offsets, E, ctrl, static_cast<uint8_t*>(xs), acc, acc_elems,
+                             dev.num_sms, s) != cudaSuccess)
+      return MOE_ERR_CUDA;
+  } else if (launch_gather_x(static_cast<const __nv_bfloat16*>(a->x), H, sorted, ctrl,
+                             static_cast<int>(P), k, xs, fp8, acc, acc_elems, L.pad_max,
+                             dev.num_sms, s) != cudaSuccess) {
     return MOE_ERR_CUDA;
-  if (launch_gather_x(static_cast<const __nv_bfloat16*>(a->x), xq_tok, H, sorted, ctrl,
-                      static_cast<int>(P), k, xs, fp8, acc, acc_elems, L.pad_max, dev.num_sms,
-                      s) != cudaSuccess)
-    return MOE_ERR_CUDA;
+  }
 
   // TMA descriptors
   CUtensorMap tm_w13, tm_xs, tm_xs64, tm_w2, tm_h, tm_h64;
@@ -608,9 +614,8 @@ int moe_fused_launch_count(int T, int H, int I, int E, int top_k, moe_dtype_t dt
     n += 1;                          // router + alignment
   } else {
     n += 2 + (L.large ? 1 : 0);      // router, (chunk histograms), alignment
-    n += (L.large && fp8) ? 1 : 0;   // per-token quantisation of x
   }
-  n += 1;                            // gather of x
+  n += 1;                            // gather of x, or per-token quantise + scatter
   n += 1;                            // gate/up GEMM
   n += fp8 ? 1 : 0;                  // quantisation of h
   n += 1;                            // down GEMM

@@ -176,12 +176,32 @@ __global__ void __launch_bounds__(kRouteWarps * 32)
   const int t = blockIdx.x * kRouteWarps + warp;
   float xmax = 0.f;
   if (t < T) {
+    // the token's first 8 x 16 bytes per lane are requested before the
+    // routing, so their latency hides behind it
+    const uint4* xr = x != nullptr ? reinterpret_cast<const uint4*>(x + static_cast<size_t>(t) * H)
+                                   : nullptr;
+    const int n8 = x != nullptr ? H / 8 : 0;
+    uint4 v[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int i = lane + 32 * u;
+      v[u] = i < n8 ? __ldg(xr + i) : make_uint4(0, 0, 0, 0);
+    }
     route_token(logits + static_cast<size_t>(t) * E, E, k, renorm,
                 s_logits + static_cast<size_t>(warp) * E, ids + static_cast<size_t>(t) * k,
                 wts + static_cast<size_t>(t) * k, lane);
     if (x != nullptr) {
-      const uint4* xr = reinterpret_cast<const uint4*>(x + static_cast<size_t>(t) * H);
-      for (int i = lane; i < H / 8; i += 32) xmax = absmax8(__ldg(xr + i), xmax);
+#pragma unroll
+      for (int u = 0; u < 8; ++u) xmax = absmax8(v[u], xmax);
+      for (int i0 = 256 + lane; i0 < n8; i0 += 256) {
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const int i = i0 + 32 * u;
+          v[u] = i < n8 ? __ldg(xr + i) : make_uint4(0, 0, 0, 0);
+        }
+#pragma unroll
+        for (int u = 0; u < 8; ++u) xmax = absmax8(v[u], xmax);
+      }
       xmax = warp_max(xmax);
     }
   }
@@ -210,7 +230,7 @@ __device__ int2 write_mtiles(int tid, int E, int padded, int seg_off, int bm, in
 // order with __match_any_sync ranks.  The resulting order is exactly the
 // ascending pair id order within each expert.
 constexpr int kAlignThreads = 1024;
-constexpr int kAlignChunk = 4096;  // pairs per CTA (<= 65535: per-warp counts are uint16)
+constexpr int kAlignChunk = 1024;  // pairs per CTA (<= 65535: per-warp counts are uint16)
 constexpr int kAlignUnroll = 8;    // id loads in flight per thread in the histogram pass
 
 __global__ void __launch_bounds__(kAlignThreads) align_kernel(AlignParams p) {
@@ -333,6 +353,7 @@ __global__ void __launch_bounds__(kAlignThreads) align_kernel(AlignParams p) {
       const int at = slot + __popc(mask & ((1u << lane) - 1u));
       p.sorted_ids[at] = q;
       if (p.sorted_w) p.sorted_w[at] = p.wts[q];
+      if (p.inv_slot) p.inv_slot[q] = at;
     }
     __syncwarp();
   }
@@ -548,32 +569,62 @@ __global__ void __launch_bounds__(kAlignThreads)
   for (int e = tid; e < E; e += kAlignThreads) hist[static_cast<size_t>(blockIdx.x) * E + e] = s_hist[e];
 }
 
-// x -> E4M3 codes in token order, 16 elements per thread.
+// Large FP8 batches: every token row of x is quantised once with s_x (a warp
+// per token, 16 elements per lane item) and its 16-byte code chunks are
+// written to each of the token's k aligned rows (the slots the alignment
+// recorded per pair); the padding rows of every expert segment are zeroed,
+// and so is the fp32 combine buffer when there is one.
 __global__ void __launch_bounds__(256)
-    quant_tokens_kernel(const __nv_bfloat16* __restrict__ x, long long n16, const Ctrl* ctrl,
-                        uint8_t* __restrict__ xq) {
+    quant_scatter_kernel(const __nv_bfloat16* __restrict__ x, int T, int H, int k,
+                         const int32_t* __restrict__ inv_slot, const int32_t* __restrict__ counts,
+                         const int32_t* __restrict__ offsets, int E, const Ctrl* __restrict__ ctrl,
+                         uint8_t* __restrict__ xs, float* __restrict__ acc, long long acc_elems) {
   pdl_wait();
   pdl_trigger();
+  const int lane = threadIdx.x & 31;
+  const int nwarps = gridDim.x * (blockDim.x >> 5);
+  const int w0 = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   const float s = ctrl->s_x;
-  const uint4* src = reinterpret_cast<const uint4*>(x);
-  uint4* dst = reinterpret_cast<uint4*>(xq);
-  for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < n16;
-       i += static_cast<long long>(gridDim.x) * blockDim.x) {
-    const uint2 a = quant8(__ldg(src + 2 * i), s);
-    const uint2 b = quant8(__ldg(src + 2 * i + 1), s);
-    dst[i] = make_uint4(a.x, a.y, b.x, b.y);
+  const int n16 = H / 16;
+  const uint4 zero = make_uint4(0, 0, 0, 0);
+  const unsigned rows = static_cast<unsigned>(ctrl->num_padded);
+  for (int t = w0; t < T; t += nwarps) {
+    // lane j < k holds the aligned row of pair (t, j) (k > 32: read per use)
+    const int32_t* tslots = inv_slot + static_cast<size_t>(t) * k;
+    const int my_slot = lane < k ? tslots[lane] : 0;
+    const uint4* src = reinterpret_cast<const uint4*>(x + static_cast<size_t>(t) * H);
+    for (int c = lane; c < n16; c += 32) {
+      const uint2 lo = quant8(__ldg(src + 2 * c), s);
+      const uint2 hi = quant8(__ldg(src + 2 * c + 1), s);
+      const uint4 v = make_uint4(lo.x, lo.y, hi.x, hi.y);
+      for (int j = 0; j < k; ++j) {
+        const int slot = k <= 32 ? __shfl_sync(0xffffffffu, my_slot, j) : tslots[j];
+        if (static_cast<unsigned>(slot) < rows)  // every routed pair has a row below num_padded
+          reinterpret_cast<uint4*>(xs + static_cast<size_t>(slot) * H)[c] = v;
+      }
+    }
   }
+  // padding rows: a warp per expert segment
+  for (int e = w0; e < E; e += nwarps) {
+    const int r0 = offsets[e] + counts[e], r1 = offsets[e + 1];
+    for (int r = r0; r < r1; ++r) {
+      uint4* dst = reinterpret_cast<uint4*>(xs + static_cast<size_t>(r) * H);
+      for (int c = lane; c < n16; c += 32) dst[c] = zero;
+    }
+  }
+  const long long tid = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
+  float4* a4 = reinterpret_cast<float4*>(acc);
+  for (long long i = tid; i < acc_elems / 4; i += stride) a4[i] = make_float4(0.f, 0.f, 0.f, 0.f);
 }
 
 // ------------------------------------------------------------------ gather
-// The pair's token row of x for every aligned row -- E4M3 codes made per
-// token (large batches: copied), quantised here with s_x (small batches), or
-// bf16 -- and zero for padding rows.  Copies go one warp per row, with the
-// next row's pair id fetched while the current row moves; quantisation goes
-// one thread per 16 elements, so a few long rows still spread over the whole
-// grid.  The same grid zeroes the fp32 combine buffer.
+// The pair's token row of x for every aligned row, quantised to E4M3 with s_x
+// (FP8) or copied (bf16), zero for padding rows: one thread per 16 (8 for
+// bf16) elements, so a few long rows still spread over the whole grid.  The
+// same grid zeroes the fp32 combine buffer.
 __global__ void __launch_bounds__(256)
-    gather_x_kernel(const __nv_bfloat16* __restrict__ x, const uint8_t* __restrict__ xq_tok, int H,
+    gather_x_kernel(const __nv_bfloat16* __restrict__ x, int H,
                     const int32_t* __restrict__ sorted_ids, const Ctrl* __restrict__ ctrl, int P,
                     int k, void* __restrict__ xs, int fp8, float* __restrict__ acc,
                     long long acc_elems) {
@@ -583,21 +634,7 @@ __global__ void __launch_bounds__(256)
   const long long tid = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
   const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
   const uint4 zero = make_uint4(0, 0, 0, 0);
-  if (fp8 && xq_tok != nullptr) {
-    const int lane = threadIdx.x & 31;
-    const long long nwarps = stride >> 5;
-    const long long w0 = tid >> 5;
-    const int n16 = H / 16;  // 16 codes per uint4
-    int q_next = w0 < rows ? sorted_ids[w0] : P;
-    for (long long r = w0; r < rows; r += nwarps) {
-      const int q = q_next;
-      q_next = r + nwarps < rows ? sorted_ids[r + nwarps] : P;
-      uint4* dst = static_cast<uint4*>(xs) + r * n16;
-      const uint4* src = reinterpret_cast<const uint4*>(xq_tok) + static_cast<size_t>(q / k) * n16;
-#pragma unroll 4
-      for (int c = lane; c < n16; c += 32) dst[c] = q < P ? src[c] : zero;
-    }
-  } else if (fp8) {
+  if (fp8) {
     const float sx = ctrl->s_x;
     const int per_row = H / 16;
     const long long n = rows * per_row;
@@ -807,16 +844,14 @@ cudaError_t launch_align(const AlignParams& p, cudaStream_t st) {
   return launch_pdl(align_kernel, dim3(grid), dim3(kAlignThreads), smem, st, p);
 }
 
-cudaError_t launch_gather_x(const __nv_bfloat16* x, const uint8_t* xq_tok, int H,
-                            const int32_t* sorted_ids, const Ctrl* ctrl, int P, int k, void* xs,
-                            bool fp8, float* acc, long long acc_elems, int max_rows, int num_sms,
-                            cudaStream_t st) {
-  // copies: a warp per row; quantisation: a thread per 16 elements
-  const long long per_row = xq_tok != nullptr ? 32 : (fp8 ? H / 16 : H / 8);
+cudaError_t launch_gather_x(const __nv_bfloat16* x, int H, const int32_t* sorted_ids,
+                            const Ctrl* ctrl, int P, int k, void* xs, bool fp8, float* acc,
+                            long long acc_elems, int max_rows, int num_sms, cudaStream_t st) {
+  const long long per_row = fp8 ? H / 16 : H / 8;
   const long long work = std::max(static_cast<long long>(max_rows) * per_row, acc_elems / 4);
   const int grid = capped_grid(work, 256, num_sms, 8);
-  return launch_pdl(gather_x_kernel, dim3(grid), dim3(256), 0, st, x, xq_tok, H, sorted_ids, ctrl,
-                    P, k, xs, fp8 ? 1 : 0, acc, acc_elems);
+  return launch_pdl(gather_x_kernel, dim3(grid), dim3(256), 0, st, x, H, sorted_ids, ctrl, P, k,
+                    xs, fp8 ? 1 : 0, acc, acc_elems);
 }
 
 cudaError_t launch_route_align_small(const SmallFrontParams& p, cudaStream_t st) {
@@ -844,10 +879,14 @@ cudaError_t launch_align_hist(const int32_t* ids, int P, int E, int32_t* hist, c
                     P, E, kAlignChunk, hist);
 }
 
-cudaError_t launch_quant_tokens(const __nv_bfloat16* x, long long n, const Ctrl* ctrl,
-                                uint8_t* xq, int num_sms, cudaStream_t st) {
-  const int grid = capped_grid(n / 16, 256, num_sms, 8);
-  return launch_pdl(quant_tokens_kernel, dim3(grid), dim3(256), 0, st, x, n / 16, ctrl, xq);
+cudaError_t launch_quant_scatter(const __nv_bfloat16* x, int T, int H, int k,
+                                 const int32_t* inv_slot, const int32_t* counts,
+                                 const int32_t* offsets, int E, const Ctrl* ctrl, uint8_t* xs,
+                                 float* acc, long long acc_elems, int num_sms, cudaStream_t st) {
+  const long long warps = std::max<long long>(T, E);
+  const int grid = capped_grid(std::max(warps * 32, acc_elems / 4), 256, num_sms, 8);
+  return launch_pdl(quant_scatter_kernel, dim3(grid), dim3(256), 0, st, x, T, H, k, inv_slot,
+                    counts, offsets, E, ctrl, xs, acc, acc_elems);
 }
 
 cudaError_t launch_quant_h(const float* h, int I, Ctrl* ctrl, uint8_t* hq, int max_rows,

@@ -61,8 +61,9 @@ def test_launch_count(lib):
     assert moe.moe_fused_launch_count(4, 128, 256, 8, 2, bf16) == 5   # no quant of h
     # 512 x 8 pairs: separate router and alignment kernels
     assert moe.moe_fused_launch_count(512, 2048, 768, 128, 8, fp8) == 7
-    # > 4096 pairs: chunk histograms and per-token quantisation of x as well
-    assert moe.moe_fused_launch_count(8192, 2048, 768, 128, 8, fp8) == 9
+    # > 4096 pairs: chunk histograms as well; x quantised per token and
+    # scattered to its aligned rows in one kernel
+    assert moe.moe_fused_launch_count(8192, 2048, 768, 128, 8, fp8) == 8
     assert moe.moe_fused_launch_count(0, 2048, 768, 128, 8, fp8) == 0
     assert moe.moe_fused_launch_count(4, 100, 256, 8, 2, fp8) == -1
     assert moe.moe_fused_launch_count(4, 128, 256, 8, 9, fp8) == -1
