@@ -342,7 +342,15 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       // the next segment's tile is fetched while this one's stages are issued
       bool have = seg_next(sch, si, g);
       Tile t = have ? decode_tile(p, g.tile) : Tile{};
+      bool bad_rows = false;
       while (ok && have) {
+        if (!kTokM && t.n > rows_b) {
+          // a tile wider than the stage (the alignment kernels write none):
+          // stop and report instead of writing past the stage
+          bad_rows = true;
+          ok = false;
+          break;
+        }
         Seg gn;
         const bool have_n = seg_next(sch, si, gn);
         const Tile tn = have_n ? decode_tile(p, gn.tile) : Tile{};
@@ -381,7 +389,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       }
       if (!ok) {
         *abort_flag = 1;
-        atomicOr(&p.ctrl->err, kDevErrTimeout);
+        atomicOr(&p.ctrl->err, bad_rows ? kDevErrRange : kDevErrTimeout);
         // let the copies already issued land before the CTA leaves
         const uint32_t n_back = it < static_cast<uint32_t>(S) ? it : static_cast<uint32_t>(S);
         for (uint32_t b = 1; b <= n_back; ++b) {

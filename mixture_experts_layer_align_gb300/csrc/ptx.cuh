@@ -274,6 +274,49 @@ __device__ __forceinline__ uint16_t cvt_e4m3x2(float lo, float hi) {
   return r;
 }
 
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+// amax -> per-tensor scale: amax / 448 (IEEE fp32 division), 1 when amax is 0.
+__device__ __forceinline__ float scale_from_amax(float amax) {
+  return amax > 0.f ? __fdiv_rn(amax, 448.f) : 1.f;
+}
+
+// v / s correctly rounded to fp32, as far as its E4M3 code is concerned.
+// With rs = 1/s correctly rounded, q = v * rs (one rounding) lies within 2.5
+// ulp of the rounded quotient.  E4M3 keeps 3 of the 23 mantissa bits, so when
+// the 20 bits below them are more than 8 ulp away from the half-way pattern
+// (and q is zero or in E4M3's normal range, |q| >= 2^-6) the quotient and q
+// round to the same code and the multiply stands in for the division;
+// otherwise (a few percent of typical activations) the IEEE division runs.
+__device__ __forceinline__ float div_for_e4m3(float v, float s, float rs) {
+  const float q = __fmul_rn(v, rs);
+  const uint32_t b = __float_as_uint(q) & 0x7fffffffu;
+  const int d = static_cast<int>(b & 0xfffffu) - 0x80000;
+  if (b == 0u || ((b >> 23) >= 121u && (d > 8 || d < -8))) return q;
+  return __fdiv_rn(v, s);
+}
+
+__device__ __forceinline__ uint16_t quant2(float a, float b, float s, float rs) {
+  return cvt_e4m3x2(div_for_e4m3(a, s, rs), div_for_e4m3(b, s, rs));
+}
+
+// 8 bf16 (one uint4) / s -> 8 E4M3 codes (two uint32); rs = __frcp_rn(s).
+__device__ __forceinline__ uint2 quant8(uint4 v, float s, float rs) {
+  uint2 r;
+  r.x = static_cast<uint32_t>(quant2(bf16_lo(v.x), bf16_hi(v.x), s, rs)) |
+        (static_cast<uint32_t>(quant2(bf16_lo(v.y), bf16_hi(v.y), s, rs)) << 16);
+  r.y = static_cast<uint32_t>(quant2(bf16_lo(v.z), bf16_hi(v.z), s, rs)) |
+        (static_cast<uint32_t>(quant2(bf16_lo(v.w), bf16_hi(v.w), s, rs)) << 16);
+  return r;
+}
+
+// 4 fp32 / s -> 4 E4M3 codes (one uint32); rs = __frcp_rn(s).
+__device__ __forceinline__ uint32_t quant4(float4 v, float s, float rs) {
+  return static_cast<uint32_t>(quant2(v.x, v.y, s, rs)) |
+         (static_cast<uint32_t>(quant2(v.z, v.w, s, rs)) << 16);
+}
+
 __device__ __forceinline__ void red_add_f32(float* p, float v) {
   asm volatile("red.global.add.f32 [%0], %1;" ::"l"(p), "f"(v) : "memory");
 }

@@ -34,32 +34,12 @@ __device__ __forceinline__ float warp_sum(float v) {
   return v;
 }
 
-__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
-__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
-
 __device__ __forceinline__ float absmax8(uint4 v, float m) {
   m = fmaxf(m, fmaxf(fabsf(bf16_lo(v.x)), fabsf(bf16_hi(v.x))));
   m = fmaxf(m, fmaxf(fabsf(bf16_lo(v.y)), fabsf(bf16_hi(v.y))));
   m = fmaxf(m, fmaxf(fabsf(bf16_lo(v.z)), fabsf(bf16_hi(v.z))));
   m = fmaxf(m, fmaxf(fabsf(bf16_lo(v.w)), fabsf(bf16_hi(v.w))));
   return m;
-}
-
-// amax -> per-tensor scale: amax / 448 (IEEE fp32 division), 1 when amax is 0.
-__device__ __forceinline__ float scale_from_amax(float amax) {
-  return amax > 0.f ? __fdiv_rn(amax, 448.f) : 1.f;
-}
-
-// 8 bf16 (one uint4) / s -> 8 E4M3 codes (two uint32).
-__device__ __forceinline__ uint2 quant8(uint4 v, float s) {
-  uint2 r;
-  r.x = static_cast<uint32_t>(cvt_e4m3x2(__fdiv_rn(bf16_lo(v.x), s), __fdiv_rn(bf16_hi(v.x), s))) |
-        (static_cast<uint32_t>(cvt_e4m3x2(__fdiv_rn(bf16_lo(v.y), s), __fdiv_rn(bf16_hi(v.y), s)))
-         << 16);
-  r.y = static_cast<uint32_t>(cvt_e4m3x2(__fdiv_rn(bf16_lo(v.z), s), __fdiv_rn(bf16_hi(v.z), s))) |
-        (static_cast<uint32_t>(cvt_e4m3x2(__fdiv_rn(bf16_lo(v.w), s), __fdiv_rn(bf16_hi(v.w), s)))
-         << 16);
-  return r;
 }
 
 // Block-wide exclusive scan of one int per thread (blockDim.x == 1024).
@@ -585,6 +565,7 @@ __global__ void __launch_bounds__(256)
   const int nwarps = gridDim.x * (blockDim.x >> 5);
   const int w0 = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   const float s = ctrl->s_x;
+  const float rs = __frcp_rn(s);
   const int n16 = H / 16;
   const uint4 zero = make_uint4(0, 0, 0, 0);
   const unsigned rows = static_cast<unsigned>(ctrl->num_padded);
@@ -594,8 +575,8 @@ __global__ void __launch_bounds__(256)
     const int my_slot = lane < k ? tslots[lane] : 0;
     const uint4* src = reinterpret_cast<const uint4*>(x + static_cast<size_t>(t) * H);
     for (int c = lane; c < n16; c += 32) {
-      const uint2 lo = quant8(__ldg(src + 2 * c), s);
-      const uint2 hi = quant8(__ldg(src + 2 * c + 1), s);
+      const uint2 lo = quant8(__ldg(src + 2 * c), s, rs);
+      const uint2 hi = quant8(__ldg(src + 2 * c + 1), s, rs);
       const uint4 v = make_uint4(lo.x, lo.y, hi.x, hi.y);
       for (int j = 0; j < k; ++j) {
         const int slot = k <= 32 ? __shfl_sync(0xffffffffu, my_slot, j) : tslots[j];
@@ -636,6 +617,7 @@ __global__ void __launch_bounds__(256)
   const uint4 zero = make_uint4(0, 0, 0, 0);
   if (fp8) {
     const float sx = ctrl->s_x;
+    const float rsx = __frcp_rn(sx);
     const int per_row = H / 16;
     const long long n = rows * per_row;
     uint4* dst = static_cast<uint4*>(xs);
@@ -646,8 +628,8 @@ __global__ void __launch_bounds__(256)
       uint4 v = zero;
       if (q < P) {
         const uint4* src = reinterpret_cast<const uint4*>(x + static_cast<size_t>(q / k) * H);
-        const uint2 lo = quant8(__ldg(src + 2 * c), sx);
-        const uint2 hi = quant8(__ldg(src + 2 * c + 1), sx);
+        const uint2 lo = quant8(__ldg(src + 2 * c), sx, rsx);
+        const uint2 hi = quant8(__ldg(src + 2 * c + 1), sx, rsx);
         v = make_uint4(lo.x, lo.y, hi.x, hi.y);
       }
       dst[i] = v;
@@ -670,16 +652,12 @@ __global__ void __launch_bounds__(256)
 }
 
 // ------------------------------------------------------------------ h quant
-__device__ __forceinline__ uint32_t quant4(float4 v, float s) {
-  return static_cast<uint32_t>(cvt_e4m3x2(__fdiv_rn(v.x, s), __fdiv_rn(v.y, s))) |
-         (static_cast<uint32_t>(cvt_e4m3x2(__fdiv_rn(v.z, s), __fdiv_rn(v.w, s))) << 16);
-}
-
 __global__ void __launch_bounds__(256)
     quant_h_kernel(const float* __restrict__ h, int I, Ctrl* ctrl, uint8_t* __restrict__ hq) {
   pdl_wait();
   pdl_trigger();
   const float s = scale_from_amax(__uint_as_float(ctrl->amax_h));
+  const float rs = __frcp_rn(s);
   if (blockIdx.x == 0 && threadIdx.x == 0) ctrl->s_h = s;
   const long long n16 = static_cast<long long>(ctrl->num_padded) * I / 16;
   const float4* src = reinterpret_cast<const float4*>(h);
@@ -687,10 +665,10 @@ __global__ void __launch_bounds__(256)
   for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < n16;
        i += static_cast<long long>(gridDim.x) * blockDim.x) {
     uint4 r;
-    r.x = quant4(src[4 * i + 0], s);
-    r.y = quant4(src[4 * i + 1], s);
-    r.z = quant4(src[4 * i + 2], s);
-    r.w = quant4(src[4 * i + 3], s);
+    r.x = quant4(src[4 * i + 0], s, rs);
+    r.y = quant4(src[4 * i + 1], s, rs);
+    r.z = quant4(src[4 * i + 2], s, rs);
+    r.w = quant4(src[4 * i + 3], s, rs);
     dst[i] = r;
   }
 }
@@ -794,13 +772,14 @@ __global__ void __launch_bounds__(256)
   }
   __syncthreads();
   const float s = s_scale;
+  const float rs = __frcp_rn(s);
   if (blockIdx.x == 0 && threadIdx.x == 0) *scale = s;
   const uint4* src = reinterpret_cast<const uint4*>(x);
   uint4* dst = reinterpret_cast<uint4*>(xq);
   for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < n16;
        i += static_cast<long long>(gridDim.x) * blockDim.x) {
-    const uint2 a = quant8(__ldg(src + 2 * i), s);
-    const uint2 b = quant8(__ldg(src + 2 * i + 1), s);
+    const uint2 a = quant8(__ldg(src + 2 * i), s, rs);
+    const uint2 b = quant8(__ldg(src + 2 * i + 1), s, rs);
     dst[i] = make_uint4(a.x, a.y, b.x, b.y);
   }
 }

@@ -56,6 +56,8 @@ def run_case(moe, w, a, top_k, renorm, rows=None, repeat=1, flags=0):
     (33, 384, 256, 12, 3, True, "bf16"),
     (600, 256, 128, 4, 2, True, "fp8"),     # >256 rows per expert: split tiles
     (130, 1024, 512, 64, 8, True, "fp8"),
+    (8, 256, 2176, 4, 2, True, "fp8"),      # I > 2048: down weights in M by default
+    (70, 384, 2304, 16, 3, False, "fp8"),   # ragged rows, I > 2048
 ])
 @pytest.mark.parametrize("placement", ["auto", "weights_in_m"])
 def test_fused_small(gpu_lib, T, H, I, E, k, renorm, dtype, placement):

@@ -91,3 +91,22 @@ def test_quantize_e4m3_bit_exact(gpu_lib, T, H, scale):
     ref_codes, ref_s = oracle.quantize_act(x)
     assert float(s.item()) == ref_s
     assert np.array_equal(codes.cpu().numpy(), ref_codes)
+
+
+@pytest.mark.parametrize("amax_bits", [0x43E0, 0x43E2, 0x3F81, 0x4011, 0x3A83, 0x4C35])
+def test_quantize_e4m3_every_bf16_value(gpu_lib, amax_bits):
+    """Every finite bf16 value of magnitude <= amax, both signs, under the scale
+    amax / 448: the kernels' multiply-by-reciprocal shortcut must give the code
+    of the correctly rounded quotient for each of them, including the values
+    whose quotient falls near an E4M3 rounding midpoint."""
+    amax = np.array([amax_bits], np.uint16).view(np.uint16)[0]
+    pos = np.arange(0, 0x7F80, dtype=np.uint16)          # +0 .. largest finite
+    pos = pos[pos <= amax]
+    vals = np.concatenate([pos, pos | np.uint16(0x8000)])
+    vals = np.concatenate([vals, np.full((-vals.size) % 128, 0, np.uint16)])
+    x = torch.from_numpy(vals.view(np.int16).copy()).view(torch.bfloat16).reshape(-1, 128)
+    codes, s = gpu_lib.moe_quantize_e4m3(x.cuda())
+    torch.cuda.synchronize()
+    ref_codes, ref_s = oracle.quantize_act(x)
+    assert float(s.item()) == ref_s
+    assert np.array_equal(codes.cpu().numpy(), ref_codes)
