@@ -390,10 +390,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       if (!ok) {
         *abort_flag = 1;
         atomicOr(&p.ctrl->err, bad_rows ? kDevErrRange : kDevErrTimeout);
-        // let the copies already issued land before the CTA leaves
-        const uint32_t n_back = it < static_cast<uint32_t>(S) ? it : static_cast<uint32_t>(S);
+        // let the copies already issued land before the CTA leaves (stages
+        // [0, pre) had their weights issued before the loop; a stage whose
+        // token rows never went out ends its wait at the limit)
+        const uint32_t n_iss = it > pre ? it : pre;
+        const uint32_t n_back = n_iss < static_cast<uint32_t>(S) ? n_iss : static_cast<uint32_t>(S);
         for (uint32_t b = 1; b <= n_back; ++b) {
-          const uint32_t i2 = it - b;
+          const uint32_t i2 = n_iss - b;
           volatile int no_abort = 0;
           mbar_wait(full + (i2 % S), (i2 / S) & 1u, &no_abort, 20000000ull);
         }
