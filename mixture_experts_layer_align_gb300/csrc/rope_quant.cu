@@ -109,11 +109,12 @@ __global__ void __launch_bounds__(kRopeThreads)
         if (kQuant) {
           if (h < NH) {
             const float sc = __uint_as_float(s_head[h]);
+            const float rsc = __frcp_rn(sc);  // codes of y / sc (see div_for_e4m3)
             uint2 q;
-            q.x = static_cast<uint32_t>(cvt_e4m3x2(__fdiv_rn(y[0], sc), __fdiv_rn(y[1], sc))) |
-                  (static_cast<uint32_t>(cvt_e4m3x2(__fdiv_rn(y[2], sc), __fdiv_rn(y[3], sc))) << 16);
-            q.y = static_cast<uint32_t>(cvt_e4m3x2(__fdiv_rn(y[4], sc), __fdiv_rn(y[5], sc))) |
-                  (static_cast<uint32_t>(cvt_e4m3x2(__fdiv_rn(y[6], sc), __fdiv_rn(y[7], sc))) << 16);
+            q.x = static_cast<uint32_t>(quant2(y[0], y[1], sc, rsc)) |
+                  (static_cast<uint32_t>(quant2(y[2], y[3], sc, rsc)) << 16);
+            q.y = static_cast<uint32_t>(quant2(y[4], y[5], sc, rsc)) |
+                  (static_cast<uint32_t>(quant2(y[6], y[7], sc, rsc)) << 16);
             *reinterpret_cast<uint2*>(codes + (row0 + h) * D + c8 * 8) = q;
           }
         } else {

@@ -135,6 +135,72 @@ __device__ void route_token(const float* __restrict__ src, int E, int k, int ren
   __syncwarp();
 }
 
+// The same selection with the row's order keys in registers (E <= 32 * R):
+// each lane holds experts lane + 32 i; a taken expert's key is set to 0 (every
+// real key is > 0).  The full softmax sum is only formed when the weights are
+// not renormalised over the k selected.  Same results as route_token.
+template <int R>
+__device__ void route_token_reg(const float* __restrict__ src, int E, int k, int renorm,
+                                int32_t* id_row, float* w_row, int lane) {
+  uint32_t key[R];
+  uint32_t km = 0u;
+#pragma unroll
+  for (int i = 0; i < R; ++i) {
+    const int e = lane + 32 * i;
+    key[i] = e < E ? float_key(src[e]) : 0u;
+    km = max(km, key[i]);
+  }
+  const float m = key_float(__reduce_max_sync(kFull, km));
+  float z = 0.f;
+  if (!renorm) {
+#pragma unroll
+    for (int i = 0; i < R; ++i)
+      if (lane + 32 * i < E) z += expf(key_float(key[i]) - m);
+    z = warp_sum(z);
+  }
+  float sel = 0.f;
+  for (int j = 0; j < k; ++j) {
+    uint32_t bk = 0u;
+    int bi = 0;
+#pragma unroll
+    for (int i = 0; i < R; ++i)
+      if (key[i] > bk) {  // ascending scan: equal keys keep the lower index
+        bk = key[i];
+        bi = lane + 32 * i;
+      }
+    const uint32_t kmax = __reduce_max_sync(kFull, bk);
+    const int win = static_cast<int>(
+        __reduce_min_sync(kFull, bk == kmax ? static_cast<uint32_t>(bi) : 0xffffffffu));
+    if ((win & 31) == lane) {
+#pragma unroll
+      for (int i = 0; i < R; ++i)
+        if (i == (win >> 5)) key[i] = 0u;
+    }
+    const float ex = expf(key_float(kmax) - m);
+    sel += ex;
+    if (lane == 0) {
+      id_row[j] = win;
+      w_row[j] = ex;
+    }
+  }
+  __syncwarp();
+  const float denom = renorm ? sel : z;
+  for (int j = lane; j < k; j += 32) w_row[j] = __fdiv_rn(w_row[j], denom);
+  __syncwarp();
+}
+
+// Dispatch on the number of experts: registers up to 256, else the shared
+// memory row `l`.
+__device__ __forceinline__ void route_token_any(const float* __restrict__ src, int E, int k,
+                                                int renorm, float* l, int32_t* id_row,
+                                                float* w_row, int lane) {
+  if (E <= 32) route_token_reg<1>(src, E, k, renorm, id_row, w_row, lane);
+  else if (E <= 64) route_token_reg<2>(src, E, k, renorm, id_row, w_row, lane);
+  else if (E <= 128) route_token_reg<4>(src, E, k, renorm, id_row, w_row, lane);
+  else if (E <= 256) route_token_reg<8>(src, E, k, renorm, id_row, w_row, lane);
+  else route_token(src, E, k, renorm, l, id_row, w_row, lane);
+}
+
 // Router kernel: one warp per token, plus the per-CTA amax of x (the first
 // half of the dynamic activation scale) and the per-call resets.
 __global__ void __launch_bounds__(kRouteWarps * 32)
@@ -167,7 +233,7 @@ __global__ void __launch_bounds__(kRouteWarps * 32)
       const int i = lane + 32 * u;
       v[u] = i < n8 ? __ldg(xr + i) : make_uint4(0, 0, 0, 0);
     }
-    route_token(logits + static_cast<size_t>(t) * E, E, k, renorm,
+    route_token_any(logits + static_cast<size_t>(t) * E, E, k, renorm,
                 s_logits + static_cast<size_t>(warp) * E, ids + static_cast<size_t>(t) * k,
                 wts + static_cast<size_t>(t) * k, lane);
     if (x != nullptr) {
@@ -242,18 +308,24 @@ __global__ void __launch_bounds__(kAlignThreads) align_kernel(AlignParams p) {
   __syncthreads();
 
   if (p.chunk_hist != nullptr) {
-    // totals and the pairs before this chunk from the per-chunk histograms
-    for (int e = tid; e < E; e += kAlignThreads) {
+    // totals and the pairs before this chunk from the per-chunk histograms:
+    // thread (e, r) sums chunks r, r + R, ... of expert e (R = 1024 / E
+    // threads per expert, so all threads have loads in flight), then shared
+    // atomics fold the R partial sums
+    const int R = E <= kAlignThreads ? kAlignThreads / E : 1;
+    const int e = tid % E, r = tid / E;
+    if (r < R) {
       int tot = 0, bef = 0;
-#pragma unroll 8
-      for (int b = 0; b < static_cast<int>(gridDim.x); ++b) {
+#pragma unroll 4
+      for (int b = r; b < static_cast<int>(gridDim.x); b += R) {
         const int v = p.chunk_hist[static_cast<size_t>(b) * E + e];
         tot += v;
         bef += b < static_cast<int>(blockIdx.x) ? v : 0;
       }
-      hist_all[e] = tot;
-      hist_before[e] = bef;
+      if (tot) atomicAdd(&hist_all[e], tot);
+      if (bef) atomicAdd(&hist_before[e], bef);
     }
+    __syncthreads();
   }
   // histograms of every pair, and of the pairs before this chunk (loads of
   // kAlignUnroll rounds issued together: this pass is latency bound)
@@ -429,7 +501,7 @@ __global__ void __launch_bounds__(kAlignThreads, 1) route_align_small_kernel(Sma
 
   // routing, one warp per token
   for (int t = warp; t < T; t += 32)
-    route_token(p.logits + static_cast<size_t>(t) * E, E, k, p.renorm, s_logits + warp * E,
+    route_token_any(p.logits + static_cast<size_t>(t) * E, E, k, p.renorm, s_logits + warp * E,
                 s_ids + t * k, s_w + t * k, lane);
   // amax |x| (FP8), 8 vector loads in flight per thread
   float xmax = 0.f;
