@@ -64,6 +64,9 @@ def parse():
     ap.add_argument("--placement", default="auto", choices=["auto", "weights", "tokens"],
                     help="MMA operand placement of both expert GEMMs: weight rows in M (the "
                          "swap), tokens in M (ablation), or the library's default choice")
+    ap.add_argument("--no-sm-pairs", action="store_true",
+                    help="ablation: wide FP8 gate/up tiles on one SM each instead of SM pairs "
+                         "(tcgen05 cta_group::2)")
     return ap.parse_args()
 
 
@@ -286,6 +289,8 @@ def run_ours(args, rank, local_rank, world):
     dtype = moe.MOE_DT_FP8_E4M3 if fp8 else moe.MOE_DT_BF16
     flags = {"auto": 0, "weights": moe.MOE_FLAG_WEIGHTS_IN_M,
              "tokens": moe.MOE_FLAG_TOKENS_IN_M}[args.placement]
+    if args.no_sm_pairs:
+        flags |= moe.MOE_FLAG_NO_SM_PAIRS
     w = inputs.make_weights(H, I, E, cfg["dtype"], seed=0, device=dev)
     # second copy of the same weights in other buffers: consecutive calls
     # alternate, so no call finds its weights in L2
@@ -504,7 +509,9 @@ def run_ours(args, rank, local_rank, world):
                                    "if I > 2048 else tokens in M",
                            "weights": "weights in the MMA M slot for both GEMMs (swap-AB)",
                            "tokens": "tokens in the MMA M slot for both GEMMs (no swap)"}[
-                              args.placement]},
+                              args.placement] + (
+                              "; wide gate/up tiles on one SM each" if args.no_sm_pairs
+                              else "")},
         "sweep": sweep,
         "kernel_share": {n: round(step_ms[n] / total_kernel_ms, 4) for n in STEP_NAMES},
         "kernel_timing": "CUDA events between the kernels of every call, second pass of the "

@@ -196,6 +196,12 @@ typedef struct {
  * the same within fp32 summation order. */
 #define MOE_FLAG_TOKENS_IN_M 0x4
 #define MOE_FLAG_WEIGHTS_IN_M 0x8
+/* FP8 gate/up tiles of 256 tokens (experts averaging more than 256 routed
+ * rows: prefill) run on SM pairs by default: a cluster of two CTAs issues
+ * tcgen05 MMAs with M = 256 (cta_group::2), each SM holding its 128 weight rows
+ * and half of the token rows.  This flag runs them on one SM per tile instead
+ * (ablation).  Results are the same within fp32 summation order. */
+#define MOE_FLAG_NO_SM_PAIRS 0x10
 #define MOE_TRACE_MAX_CTAS 256
 size_t moe_fused_trace_offset(int T, int H, int I, int E, int top_k, moe_dtype_t dtype);
 

@@ -225,6 +225,12 @@ size_t gemm_stage_smem(bool swiglu);
 cudaError_t launch_gemm(bool bf16, bool swiglu, bool tok_m, bool pair, const GemmParams& p,
                         const CUtensorMap& tma, const CUtensorMap& tmb, const CUtensorMap& tmb64,
                         int grid, cudaStream_t st);
+// Gate/up GEMM of wide row tiles (256 tokens) on SM pairs (cluster of two,
+// tcgen05 cta_group::2): E4M3, weights in M, I % 256 == 0, whole tiles;
+// p.mtiles is the wide tile list and p.nb_count = I / 256.  At most
+// `max_clusters` clusters (the units of the call).
+cudaError_t launch_gemm_pair(const GemmParams& p, const CUtensorMap& tma, const CUtensorMap& tmb,
+                             const CUtensorMap& tmb64, int max_clusters, cudaStream_t st);
 // Row-tile width of the unswapped placement (the token tile fills M = 128).
 constexpr int kTokMRows = 128;
 }  // namespace moe

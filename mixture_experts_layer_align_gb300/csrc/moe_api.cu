@@ -394,6 +394,9 @@ moe_status_t fused_forward_impl(const moe_fused_args* a, void* workspace, size_t
   // (at the cost of a single TMEM accumulator buffer), from a second tile list.
   const long long touched_ub = std::min<long long>(E, P);
   const bool wide1 = !tok_m1 && (P + touched_ub - 1) / touched_ub > kWideRows;
+  // FP8 wide tiles run on SM pairs (cta_group::2): 256 weight rows x 256
+  // tokens per tile, each SM loading half of the token rows.
+  const bool pair1 = fp8 && wide1 && I % 256 == 0 && (a->debug_flags & MOE_FLAG_NO_SM_PAIRS) == 0;
   int4* mtiles_w = reinterpret_cast<int4*>(ws + L.mtiles_w);
   int* tile_cnt = reinterpret_cast<int*>(ws + L.tile_cnt);
   float* part = reinterpret_cast<float*>(ws + L.part);
@@ -534,8 +537,18 @@ moe_status_t fused_forward_impl(const moe_fused_args* a, void* workspace, size_t
   const long long work1 = max_tiles1 * g1.nb_count * g1.k_steps;
   const int grid1 = static_cast<int>(std::max<long long>(1, std::min<long long>(ctas, work1)));
   if (events && cudaEventRecord(events[3], stream) != cudaSuccess) return MOE_ERR_CUDA;
-  if (launch_gemm(bf16, true, tok_m1, false, g1, tm_w13, tm_xs, tm_xs64, grid1, s) != cudaSuccess)
+  if (pair1) {
+    GemmParams gp = g1;
+    gp.nb_count = I / 256;  // units: (wide row tile, pair of weight blocks)
+    const long long units = max_tiles1 * gp.nb_count;
+    const int max_clusters =
+        static_cast<int>(std::max<long long>(1, std::min<long long>(ctas / 2, units)));
+    if (launch_gemm_pair(gp, tm_w13, tm_xs, tm_xs64, max_clusters, s) != cudaSuccess)
+      return MOE_ERR_CUDA;
+  } else if (launch_gemm(bf16, true, tok_m1, false, g1, tm_w13, tm_xs, tm_xs64, grid1, s) !=
+             cudaSuccess) {
     return MOE_ERR_CUDA;
+  }
 
   // 5. dynamic scale of h and its E4M3 codes
   if (events && cudaEventRecord(events[4], stream) != cudaSuccess) return MOE_ERR_CUDA;

@@ -79,6 +79,22 @@ def test_fused_large_batch_paths(gpu_lib, T, H, I, E, k, placement):
     run_case(gpu_lib, w, a, k, True, rows=sample_rows(T, 64, seed=3), flags=flags)
 
 
+# Wide gate/up tiles (experts averaging more than 256 rows, I % 256 == 0) run on
+# SM pairs (tcgen05 cta_group::2) by default; MOE_FLAG_NO_SM_PAIRS runs the same
+# tiles on one SM each.
+@pytest.mark.parametrize("T,H,I,E,k,routing", [
+    (1200, 256, 512, 4, 2, "uniform"),    # one alignment kernel, gather
+    (1100, 384, 768, 4, 3, "uniform"),    # ragged tiles, three weight-block pairs
+    (3000, 256, 512, 8, 2, "zipf"),       # > 4096 pairs: two-pass alignment, skew
+])
+@pytest.mark.parametrize("pairs", [True, False])
+def test_fused_wide_tiles_sm_pairs(gpu_lib, T, H, I, E, k, routing, pairs):
+    w = inputs.make_weights(H, I, E, "fp8", seed=T)
+    a = inputs.make_activations(T, H, E, routing, seed=T)
+    run_case(gpu_lib, w, a, k, True, repeat=2,
+             flags=0 if pairs else gpu_lib.MOE_FLAG_NO_SM_PAIRS)
+
+
 # The unswapped placement (tokens in the MMA M slot, weight rows in N): the
 # ablation of the operand swap must compute the same layer.
 @pytest.mark.parametrize("T,H,I,E,k,renorm,dtype", [

@@ -13,9 +13,10 @@ pytestmark = pytest.mark.gpu
 
 
 # (8, ...) decode-style tiles (I = 2176 > 2048 keeps the down weights in M);
-# (600, ...) 300 rows per expert: wide gate/up tiles, tokens in M for down
+# (600, ...) 300 rows per expert: wide gate/up tiles on one SM each (I = 128),
+# tokens in M for down; (1200, ...) wide gate/up tiles on SM pairs
 @pytest.mark.parametrize("T,H,I,E,k", [(8, 256, 256, 8, 2), (8, 256, 2176, 4, 2),
-                                       (600, 256, 128, 4, 2)])
+                                       (600, 256, 128, 4, 2), (1200, 256, 512, 4, 2)])
 def test_forced_timeout_reports_status_and_context_survives(gpu_lib, T, H, I, E, k):
     w = inputs.make_weights(H, I, E, "fp8", seed=11)
     a = inputs.make_activations(T, H, E, "uniform", seed=11)
