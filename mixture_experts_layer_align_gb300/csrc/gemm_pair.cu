@@ -112,8 +112,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
   tc_fence_after_sync();
   const uint32_t tmem = *tmem_slot;
 
-  pdl_wait();
-  pdl_trigger();
+  // Everything above overlaps the previous kernel.  The producer also puts the
+  // first stages' weight blocks in flight before that kernel has finished: the
+  // tile list it reads for that was written two or more kernels back, and every
+  // kernel of the library signals its dependents only after its own wait.
+  const bool early_producer = (warp == 0 && lane == 0);
+  if (!early_producer) {
+    pdl_wait();
+    pdl_trigger();
+  }
 
   const int K = p.k_steps;
   const int units = p.ctrl->num_mtiles_w * p.nb_count;
@@ -125,6 +132,24 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
     // ------------------------------------------------ TMA producer (both CTAs)
     if (lane == 0) {
       const uint64_t pol_w = policy_evict_last();  // weight blocks serve several row tiles
+      // weight blocks of the first S stages (fresh stages: no wait on `empty`)
+      uint32_t pre = 0;
+      for (int u = cid; pre < static_cast<uint32_t>(S) && u < units; u += n_cl) {
+        const PairTile t = pair_tile(p, u, rank);
+        const uint32_t half = static_cast<uint32_t>(t.nmma / 2);
+        const int wrow = t.e * p.rows_per_expert + t.nb * 128;
+        for (int kk = 0; kk < K && pre < static_cast<uint32_t>(S); ++kk, ++pre) {
+          const uint32_t fb = mapa_shared(smem_addr(full + pre), 0);
+          if (leader) mbar_arrive_expect_tx(full + pre, 2u * (kPairABytes + half * 128u));
+          uint8_t* sa = smem + static_cast<size_t>(pre) * kPairStageBytes;
+          const int kc = kk * p.k_elems;
+          tma_load_2d_pair(sa, &tm_a, fb, kc, wrow, pol_w);
+          tma_load_2d_pair(sa + 16384, &tm_a, fb, kc, wrow + p.up_offset, pol_w);
+        }
+      }
+      // token rows are the previous kernels' output
+      pdl_wait();
+      pdl_trigger();
       uint32_t it = 0;
       bool ok = true;
       for (int u = cid; ok && u < units; u += n_cl) {
@@ -135,17 +160,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
         for (int kk = 0; kk < K; ++kk, ++it) {
           const uint32_t s = it % S;
           const uint32_t ph = (it / S) & 1u;
-          if (!mbar_wait(empty + s, ph ^ 1u, abort_flag, limit)) {
-            ok = false;
-            break;
-          }
           const uint32_t fb = mapa_shared(smem_addr(full + s), 0);
-          if (leader) mbar_arrive_expect_tx(full + s, 2u * (kPairABytes + static_cast<uint32_t>(half) * 128u));
           uint8_t* sa = smem + static_cast<size_t>(s) * kPairStageBytes;
           uint8_t* sb = sa + kPairABytes;
           const int kc = kk * p.k_elems;
-          tma_load_2d_pair(sa, &tm_a, fb, kc, wrow, pol_w);
-          tma_load_2d_pair(sa + 16384, &tm_a, fb, kc, wrow + p.up_offset, pol_w);
+          if (it >= pre) {
+            if (!mbar_wait(empty + s, ph ^ 1u, abort_flag, limit)) {
+              ok = false;
+              break;
+            }
+            if (leader) mbar_arrive_expect_tx(full + s, 2u * (kPairABytes + static_cast<uint32_t>(half) * 128u));
+            tma_load_2d_pair(sa, &tm_a, fb, kc, wrow, pol_w);
+            tma_load_2d_pair(sa + 16384, &tm_a, fb, kc, wrow + p.up_offset, pol_w);
+          }
           int j = 0;
           for (; j + 64 <= half; j += 64) tma_load_2d_pair(sb + j * 128, &tm_b64, fb, kc, brow + j);
           for (; j < half; j += 16) tma_load_2d_pair(sb + j * 128, &tm_b, fb, kc, brow + j);
