@@ -353,7 +353,7 @@ def read_trace(workspace, T, H, I, E, top_k, dtype):
 
 
 def moe_check_status(workspace, stream=None) -> int:
-    """Synchronise and return the device status word's verdict (0 = MOE_OK)."""
+    """Synchronise and return the status the last call left in the workspace (0 = MOE_OK)."""
     return int(load().moe_check_status(_ptr(workspace), _stream(stream)))
 
 

@@ -58,6 +58,7 @@ def run_case(moe, w, a, top_k, renorm, rows=None, repeat=1, flags=0):
     (130, 1024, 512, 64, 8, True, "fp8"),
     (8, 256, 2176, 4, 2, True, "fp8"),      # I > 2048: down weights in M by default
     (70, 384, 2304, 16, 3, False, "fp8"),   # ragged rows, I > 2048
+    (1000, 256, 512, 4, 2, True, "fp8"),    # 500 rows per expert: gate/up on SM pairs
 ])
 @pytest.mark.parametrize("placement", ["auto", "weights_in_m"])
 def test_fused_small(gpu_lib, T, H, I, E, k, renorm, dtype, placement):
