@@ -58,6 +58,10 @@ def parse():
                     help="first-call vs steady-state time for every T in 1..--max-tokens "
                          "in one process, plus CUDA-graph capture per T bucket")
     ap.add_argument("--max-tokens", type=int, default=8192)
+    ap.add_argument("--cta-trace", action="store_true",
+                    help="per-CTA timeline of the two expert GEMMs (MOE_DEBUG_TRACE stamps: "
+                         "entry, inputs ready, first stage landed, exit) for the workload's T "
+                         "values, weights cold; prints one JSON line")
     ap.add_argument("--rope", action="store_true",
                     help="time the inverse rotary embedding + per-head FP8 quantisation "
                          "kernel (32 heads of 128, T in 1..8192) instead of the layer")
@@ -739,9 +743,60 @@ def run_rope(args, rank, local_rank):
     print(json.dumps(line), flush=True)
 
 
+def run_cta_trace(args, rank, local_rank):
+    """Per-CTA %globaltimer stamps of the two expert GEMMs of one call per T,
+    relative to the kernel's first CTA entry (us): min/median/max of the
+    stamps and the CTAs' exit spread.  Diagnostic only (not a bench line)."""
+    if rank != 0:
+        return
+    import numpy as np
+    import torch
+    import mixture_experts_layer_align_gb300 as moe
+    from mixture_experts_layer_align_gb300 import inputs
+    moe.load()
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    cfg = inputs.workload(args.workload)
+    H, I, E, k = cfg["H"], cfg["I"], cfg["E"], cfg["top_k"]
+    dtype = moe.MOE_DT_FP8_E4M3 if cfg["dtype"] == "fp8" else moe.MOE_DT_BF16
+    w = inputs.make_weights(H, I, E, cfg["dtype"], seed=0, device=dev)
+    w_alt = inputs.Weights(w.w13.clone(), w.w2.clone(), w.w13_scale, w.w2_scale, w.dtype, H, I, E)
+    n_sm = torch.cuda.get_device_properties(dev).multi_processor_count
+    out = {"metric": "per-CTA timeline of the expert GEMMs (us from the kernel's first CTA)",
+           "workload": args.workload, "per_T": []}
+    for T in tokens_list(args, cfg):
+        a = inputs.make_activations(T, H, E, cfg["routing"], seed=0, device=dev)
+        ws = moe.alloc_workspace(T, H, I, E, k, dtype, dev)
+        for it in range(6):  # the two weight copies alternate: the last call is cold
+            ww = w if it % 2 == 0 else w_alt
+            moe.moe_fused_forward(a.x, a.logits, ww.w13, ww.w2, ww.w13_scale, ww.w2_scale, k, True,
+                                  workspace=ws, debug_flags=moe.MOE_DEBUG_TRACE)
+        torch.cuda.synchronize()
+        tr = moe.read_trace(ws, T, H, I, E, k, dtype).numpy()
+        row = {"T": T}
+        for g, name in enumerate(("gate_up", "down")):
+            t = tr[g][:min(n_sm, tr.shape[1])].astype(np.float64)
+            t = t[t[:, 0] > 0]
+            if len(t) == 0:
+                continue
+            rel = (t - t[:, 0].min()) / 1e3
+            row[name] = {"ctas": int(len(t)),
+                         "entry_max": round(float(rel[:, 0].max()), 2),
+                         "ready_max": round(float(rel[:, 1].max()), 2),
+                         "first_median": round(float(np.median(rel[:, 2])), 2),
+                         "exit_min_median_max": [round(float(rel[:, 3].min()), 2),
+                                                 round(float(np.median(rel[:, 3])), 2),
+                                                 round(float(rel[:, 3].max()), 2)]}
+        out["per_T"].append(row)
+    print(json.dumps(out), flush=True)
+
+
 def main():
     args = parse()
     rank, local_rank, world = dist_env()
+    if args.cta_trace:
+        run_cta_trace(args, rank, local_rank)
+        return
     if args.rope:
         run_rope(args, rank, local_rank)
         return
