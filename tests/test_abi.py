@@ -134,3 +134,29 @@ def test_no_device_is_reported_not_faked(lib):
     need = moe.moe_fused_workspace_size(4, 128, 256, 8, 2, 1)
     st = lib.moe_fused_forward(ctypes.byref(a), ctypes.c_void_p(1 << 20), need, None)
     assert st in (2, 4)
+
+
+def test_binding_constants_match_header():
+    """The binding's copies of the header's flag bits, enum values and sizes
+    agree with include/moe_gb300.h (read as text)."""
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    text = open(os.path.join(root, "include", "moe_gb300.h")).read()
+    defines = {m.group(1): int(m.group(2), 0)
+               for m in re.finditer(r"^#define (MOE_\w+) (0x[0-9a-fA-F]+|\d+)\s*$", text, re.M)}
+    enums = {m.group(1): int(m.group(2))
+             for m in re.finditer(r"\b(MOE_(?:OK|ERR_\w+|DT_\w+)) = (\d+)", text)}
+    for name in ("MOE_DEBUG_FORCE_TIMEOUT", "MOE_DEBUG_TRACE", "MOE_FLAG_TOKENS_IN_M",
+                 "MOE_FLAG_WEIGHTS_IN_M", "MOE_FLAG_NO_SM_PAIRS"):
+        assert getattr(moe, name) == defines[name], name
+    assert moe.TRACE_MAX_CTAS == defines["MOE_TRACE_MAX_CTAS"]
+    assert len(moe.make_step_events.__defaults__) == 1
+    assert moe.make_step_events.__defaults__[0] == defines["MOE_TIMED_EVENTS"]
+    assert moe.MOE_OK == enums["MOE_OK"]
+    assert moe.MOE_DT_BF16 == enums["MOE_DT_BF16"]
+    assert moe.MOE_DT_FP8_E4M3 == enums["MOE_DT_FP8_E4M3"]
+    for code, name in moe.STATUS_NAMES.items():
+        assert enums[name] == code, name
+    # the flag bits are distinct single bits
+    flags = [defines[n] for n in defines if n.startswith(("MOE_FLAG_", "MOE_DEBUG_"))
+             and n != "MOE_DEBUG_TIMEOUT_MS"]
+    assert all(f & (f - 1) == 0 for f in flags) and len(set(flags)) == len(flags)
