@@ -96,6 +96,20 @@ def test_fused_wide_tiles_sm_pairs(gpu_lib, T, H, I, E, k, routing, pairs):
              flags=0 if pairs else gpu_lib.MOE_FLAG_NO_SM_PAIRS)
 
 
+# More shapes through the SM-pair kernel, drawn once with random.Random(2026):
+# E in {2..8}, k <= min(E, 4), H = 128..512, I = 256..1024 (multiples of 256),
+# 260..700 routed rows per expert on average, uniform or Zipf routing.
+@pytest.mark.parametrize("T,H,I,E,k,routing", [
+    (567, 128, 512, 2, 2, "zipf"), (522, 512, 512, 8, 4, "uniform"),
+    (265, 128, 1024, 2, 2, "zipf"), (876, 512, 768, 4, 2, "zipf"),
+    (3270, 384, 256, 6, 1, "zipf"), (272, 256, 768, 4, 4, "zipf"),
+])
+def test_fused_sm_pairs_random_shapes(gpu_lib, T, H, I, E, k, routing):
+    w = inputs.make_weights(H, I, E, "fp8", seed=T + I)
+    a = inputs.make_activations(T, H, E, routing, seed=T + I)
+    run_case(gpu_lib, w, a, k, True)
+
+
 # The unswapped placement (tokens in the MMA M slot, weight rows in N): the
 # ablation of the operand swap must compute the same layer.
 @pytest.mark.parametrize("T,H,I,E,k,renorm,dtype", [
