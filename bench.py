@@ -464,15 +464,36 @@ def run_ours(args, rank, local_rank, world):
         h2d = sum(T * H * 2 + T * E * 4 for T in Ts)
         d2h = sum(T * H * 2 for T in Ts)
 
+        # Copies run on a side stream, as a serving loop would issue them: the
+        # step's inputs go up first (each call waits for its own), each result
+        # comes back as soon as its call is done, and a call's input buffers
+        # are refilled only after that call of the previous step has run.
+        compute = torch.cuda.current_stream(dev)
+        copier = torch.cuda.Stream(device=dev)
+        in_ready = {T: torch.cuda.Event() for T in Ts}
+        call_done = {T: torch.cuda.Event() for T in Ts}
+        for T in Ts:
+            call_done[T].record(compute)
+
         def e2e_step(s):
+            with torch.cuda.stream(copier):
+                for T in Ts:
+                    copier.wait_event(call_done[T])
+                    hx, hl, _ = host[T]
+                    dx[T].copy_(hx, non_blocking=True)
+                    dl[T].copy_(hl, non_blocking=True)
+                    in_ready[T].record(copier)
             for j, T in enumerate(Ts):
                 ww = copies[(s * calls_per_step + j) % 2]
-                hx, hl, ho = host[T]
-                dx[T].copy_(hx, non_blocking=True)
-                dl[T].copy_(hl, non_blocking=True)
+                compute.wait_event(in_ready[T])
                 moe.moe_fused_forward(dx[T], dl[T], ww.w13, ww.w2, ww.w13_scale, ww.w2_scale, k,
                                       True, out=outs[T], workspace=wss[T], debug_flags=flags)
-                ho.copy_(outs[T], non_blocking=True)
+                call_done[T].record(compute)
+                with torch.cuda.stream(copier):
+                    copier.wait_event(call_done[T])
+                    host[T][2].copy_(outs[T], non_blocking=True)
+            # the step ends when its last result has reached the host buffer
+            compute.wait_stream(copier)
 
         for i in range(3):
             e2e_step(i)
