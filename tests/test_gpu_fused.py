@@ -96,6 +96,16 @@ def test_fused_wide_tiles_sm_pairs(gpu_lib, T, H, I, E, k, routing, pairs):
              flags=0 if pairs else gpu_lib.MOE_FLAG_NO_SM_PAIRS)
 
 
+# bf16 weights on the large-batch paths: two-pass alignment, bf16 rows of x,
+# 256-token gate/up tiles on one SM (SM pairs are FP8 only), combine through the
+# fp32 buffer or through rows per pair (P x H > 8M).
+@pytest.mark.parametrize("T,H,I,E,k", [(5000, 256, 256, 8, 2), (2048, 1024, 128, 32, 8)])
+def test_fused_bf16_large_batch_paths(gpu_lib, T, H, I, E, k):
+    w = inputs.make_weights(H, I, E, "bf16", seed=T)
+    a = inputs.make_activations(T, H, E, "zipf", seed=T)
+    run_case(gpu_lib, w, a, k, True, rows=sample_rows(T, 64, seed=5))
+
+
 # More shapes through the SM-pair kernel, drawn once with random.Random(2026):
 # E in {2..8}, k <= min(E, 4), H = 128..512, I = 256..1024 (multiples of 256),
 # 260..700 routed rows per expert on average, uniform or Zipf routing.
