@@ -217,3 +217,33 @@ def test_fused_prefill_8192(gpu_lib, name):
     w = _weights(name)
     a = inputs.make_activations(8192, c["H"], c["E"], c["routing"], seed=0, device="cuda")
     run_case(gpu_lib, w, a, c["top_k"], True, rows=sample_rows(8192, 16, seed=1))
+
+
+def test_fused_timed_and_traced_call(gpu_lib):
+    """moe_fused_forward_timed: eight events bracket the steps in order and the
+    output agrees with the untimed call's; MOE_DEBUG_TRACE: every CTA of the two
+    expert GEMMs that ran leaves stamps with entry and "inputs ready" before
+    "first stage landed" and exit."""
+    T, H, I, E, k = 64, 256, 2176, 8, 2
+    w = inputs.make_weights(H, I, E, "fp8", seed=9, device="cuda")
+    a = inputs.make_activations(T, H, E, "uniform", seed=9, device="cuda")
+    ws = gpu_lib.alloc_workspace(T, H, I, E, k, gpu_lib.MOE_DT_FP8_E4M3)
+    ev = gpu_lib.make_step_events()
+    o1 = gpu_lib.moe_fused_forward(a.x, a.logits, w.w13, w.w2, w.w13_scale, w.w2_scale, k, True,
+                                   workspace=ws, events=ev, debug_flags=gpu_lib.MOE_DEBUG_TRACE)
+    torch.cuda.synchronize()
+    assert gpu_lib.moe_check_status(ws) == 0
+    times = [ev[0].elapsed_time(e) for e in ev]
+    assert all(t1 >= t0 for t0, t1 in zip(times, times[1:]))
+    tr = gpu_lib.read_trace(ws, T, H, I, E, k, gpu_lib.MOE_DT_FP8_E4M3).numpy()
+    for g in range(2):
+        stamps = tr[g][np.all(tr[g] > 0, axis=1)]  # CTAs that ran at least one stage
+        assert len(stamps) > 0
+        entry, ready, first, leave = (stamps[:, i] for i in range(4))
+        assert np.all(entry <= ready) and np.all(ready <= leave)
+        assert np.all(entry <= first) and np.all(first <= leave)
+    o2 = gpu_lib.moe_fused_forward(a.x, a.logits, w.w13, w.w2, w.w13_scale, w.w2_scale, k, True,
+                                   workspace=ws)
+    torch.cuda.synchronize()
+    d = (o1.float() - o2.float()).abs().max().item()
+    assert d <= 2e-2 * o2.float().abs().max().item()
