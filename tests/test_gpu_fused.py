@@ -228,6 +228,7 @@ def test_fused_timed_and_traced_call(gpu_lib):
     w = inputs.make_weights(H, I, E, "fp8", seed=9, device="cuda")
     a = inputs.make_activations(T, H, E, "uniform", seed=9, device="cuda")
     ws = gpu_lib.alloc_workspace(T, H, I, E, k, gpu_lib.MOE_DT_FP8_E4M3)
+    ws.zero_()  # trace rows of CTAs that are not launched stay as they were
     ev = gpu_lib.make_step_events()
     o1 = gpu_lib.moe_fused_forward(a.x, a.logits, w.w13, w.w2, w.w13_scale, w.w2_scale, k, True,
                                    workspace=ws, events=ev, debug_flags=gpu_lib.MOE_DEBUG_TRACE)
@@ -236,8 +237,10 @@ def test_fused_timed_and_traced_call(gpu_lib):
     times = [ev[0].elapsed_time(e) for e in ev]
     assert all(t1 >= t0 for t0, t1 in zip(times, times[1:]))
     tr = gpu_lib.read_trace(ws, T, H, I, E, k, gpu_lib.MOE_DT_FP8_E4M3).numpy()
+    n_sm = torch.cuda.get_device_properties(0).multi_processor_count
     for g in range(2):
-        stamps = tr[g][np.all(tr[g] > 0, axis=1)]  # CTAs that ran at least one stage
+        rows = tr[g][:n_sm]  # at most one CTA per SM
+        stamps = rows[np.all(rows > 0, axis=1)]  # CTAs that ran at least one stage
         assert len(stamps) > 0
         entry, ready, first, leave = (stamps[:, i] for i in range(4))
         assert np.all(entry <= ready) and np.all(ready <= leave)
