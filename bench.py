@@ -788,6 +788,7 @@ def run_cta_trace(args, rank, local_rank):
     for T in tokens_list(args, cfg):
         a = inputs.make_activations(T, H, E, cfg["routing"], seed=0, device=dev)
         ws = moe.alloc_workspace(T, H, I, E, k, dtype, dev)
+        ws.zero_()  # trace rows of CTAs that are not launched keep their contents
         for it in range(6):  # the two weight copies alternate: the last call is cold
             ww = w if it % 2 == 0 else w_alt
             moe.moe_fused_forward(a.x, a.logits, ww.w13, ww.w2, ww.w13_scale, ww.w2_scale, k, True,

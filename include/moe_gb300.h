@@ -185,7 +185,9 @@ typedef struct {
 /* Diagnostic: the two expert-GEMM kernels record, per CTA, four %globaltimer
  * stamps (ns): kernel entry, inputs ready, first weight tile landed, exit.
  * They go to uint64 [2][MOE_TRACE_MAX_CTAS][4] at byte offset
- * moe_fused_trace_offset() of the workspace (gate/up kernel first). */
+ * moe_fused_trace_offset() of the workspace (gate/up kernel first); rows of
+ * CTAs that are not launched keep their previous contents (zero the region
+ * first to tell them apart). */
 #define MOE_DEBUG_TRACE 0x2
 /* Operand placement (section "Swap-AB for WGMMA utilization").  By default
  * the gate/up GEMM puts the expert's weight rows in the MMA's M slot (the
