@@ -112,9 +112,11 @@ moe_status_t moe_quantize_e4m3(const void* x, int T, int H, uint8_t* x_q, float*
  * component owns every allocation, or the calling thread must not take
  * cudaMalloc's implicit synchronisation).
  *   - Allocates nothing: no cudaMalloc, cudaFree or allocating library call.
- *   - The first call on a device looks up the array's device address
- *     (cudaGetSymbolAddress) with that device current and caches it; make
- *     that first call before any stream capture on the device.
+ *   - The first call in a CUDA context looks up the array's device address
+ *     (cudaGetSymbolAddress) with that device current and caches it under
+ *     the context's unique id (cuCtxGetId); a call in another context (after
+ *     cudaDeviceReset, or with another driver context current) looks it up
+ *     again.  Make the first call on a device before any stream capture.
  *   - The array is shared by every call on the device and keeps the last
  *     call's contents; calls that overlap on the GPU (other streams, or other
  *     host threads) race on it and must be serialised by the caller.

@@ -131,6 +131,10 @@ def _require(t, dtype, name, shape=None):
     import torch
     if not isinstance(t, torch.Tensor) or not t.is_cuda:
         raise ValueError(f"{name} must be a CUDA tensor")
+    if t.device.index != torch.cuda.current_device():
+        # the library launches on the current device and uses its per-device state
+        raise ValueError(f"{name} is on {t.device}, but the current CUDA device is "
+                         f"cuda:{torch.cuda.current_device()} (use torch.cuda.device(...))")
     if t.dtype != dtype:
         raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
     if not t.is_contiguous():
@@ -309,6 +313,10 @@ def moe_fused_forward(x, router_logits, w13, w2, w13_scale, w2_scale, top_k: int
 
     x bf16 [T,H]; router_logits fp32 [T,E]; w13 [E,2I,H] and w2 [E,H,I] as uint8
     E4M3 codes (with fp32 [E] scales) or bf16 (scales None).  Returns out bf16 [T,H].
+    With a caller `workspace` the call is asynchronous and device-side errors
+    are read with moe_check_status(workspace); without one, a workspace is
+    allocated for this call and its status is checked before returning (the
+    stream is synchronised and a device-side error raises MoeError).
     `events`: optional list of 8 recorded torch.cuda.Event (enable_timing) that
     bracket the seven steps (moe_fused_forward_timed).
     """
@@ -318,7 +326,8 @@ def moe_fused_forward(x, router_logits, w13, w2, w13_scale, w2_scale, top_k: int
     args, (T, H, I, E, dtype) = _fused_args(x, router_logits, w13, w2, w13_scale, w2_scale,
                                             top_k, renormalize, out, topk_ids_out, topk_w_out,
                                             counts_out, debug_flags)
-    if workspace is None:
+    own_ws = workspace is None
+    if own_ws:
         workspace = alloc_workspace(T, H, I, E, top_k, dtype, x.device)
     L = load()
     if events is None:
@@ -330,6 +339,10 @@ def moe_fused_forward(x, router_logits, w13, w2, w13_scale, w2_scale, top_k: int
         st = L.moe_fused_forward_timed(ctypes.byref(args), _ptr(workspace), workspace.numel(),
                                        _stream(stream), arr, len(events))
         _check(st, "moe_fused_forward_timed")
+    if own_ws and T > 0:
+        # nobody else can read a throwaway workspace's status word: read it
+        # here (this synchronises the stream; pass a workspace to avoid that)
+        _check(moe_check_status(workspace, stream), "moe_fused_forward (device status)")
     return out
 
 

@@ -8,8 +8,10 @@
 // latency-critical thread that cannot take the allocator's implicit device
 // synchronisation), and that therefore cannot provide the scratch buffer
 // moe_quantize_e4m3 asks for.
+#include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
+#include <cudaTypedefs.h>
 #include <stdint.h>
 
 #include <algorithm>
@@ -28,19 +30,57 @@ static __device__ __align__(256) float g_noalloc_partials[MOE_NOALLOC_MAX_PARTIA
 
 constexpr int kMaxDevices = 64;
 std::mutex g_mu;
+// Per device: the array's address and the unique id of the CUDA context it
+// was looked up in.  A module's device symbols live in one context, so a new
+// context on the device (after cudaDeviceReset, or another current driver
+// context) gets its address looked up again.
 float* g_ptr[kMaxDevices] = {};
+unsigned long long g_ctx_id[kMaxDevices] = {};
 
-// Device address of the array on the current device, looked up once per
-// device (with that device current) and cached.
+// Unique id of the calling thread's current context (cuCtxGetId: ids are
+// never reused within a process).  0 when it cannot be read.
+unsigned long long current_context_id() {
+  static PFN_cuCtxGetCurrent_v4000 get_cur = nullptr;
+  static PFN_cuCtxGetId_v12000 get_id = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 4000, cudaEnableDefault, &q) ==
+            cudaSuccess && q == cudaDriverEntryPointSuccess)
+      get_cur = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(p);
+    p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess && q == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<PFN_cuCtxGetId_v12000>(p);
+  });
+  CUcontext ctx = nullptr;
+  unsigned long long id = 0;
+  if (!get_cur || !get_id || get_cur(&ctx) != CUDA_SUCCESS || ctx == nullptr ||
+      get_id(ctx, &id) != CUDA_SUCCESS)
+    return 0;
+  return id;
+}
+
+// Device address of the array in the current device's current context.  It
+// is looked up (cudaGetSymbolAddress, with that device current; this also
+// binds the runtime's primary context if none is current yet) on the first
+// call in a context and cached under the context's id; a context whose id
+// cannot be read is looked up on every call.
 cudaError_t scratch_address(int dev, float** out) {
   if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
   std::lock_guard<std::mutex> lock(g_mu);
-  if (g_ptr[dev] == nullptr) {
-    void* p = nullptr;
-    const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_partials);
-    if (e != cudaSuccess) return checked(e, "cudaGetSymbolAddress");
-    g_ptr[dev] = static_cast<float*>(p);
+  unsigned long long ctx = current_context_id();
+  if (ctx != 0 && g_ptr[dev] != nullptr && g_ctx_id[dev] == ctx) {
+    *out = g_ptr[dev];
+    return cudaSuccess;
   }
+  void* p = nullptr;
+  const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_partials);
+  if (e != cudaSuccess) return checked(e, "cudaGetSymbolAddress");
+  ctx = current_context_id();
+  g_ptr[dev] = static_cast<float*>(p);
+  g_ctx_id[dev] = ctx;
   *out = g_ptr[dev];
   return cudaSuccess;
 }
