@@ -206,15 +206,23 @@ typedef struct {
  * and half of the token rows.  This flag runs them on one SM per tile instead
  * (ablation).  Results are the same within fp32 summation order. */
 #define MOE_FLAG_NO_SM_PAIRS 0x10
+/* Small batches (T*top_k <= 2048, E <= 256): run the whole layer as one
+ * cooperative persistent kernel instead of the kernel sequence (one CTA per
+ * SM; its CTAs wait on one another through grid-wide counters, so it needs
+ * every SM of the device at once; not with MOE_FLAG_TOKENS_IN_M).  Results
+ * are the same within fp32 summation order; the sequence is the default
+ * because it was measured as fast or faster on every decode workload. */
+#define MOE_FLAG_ONE_KERNEL 0x20
 #define MOE_TRACE_MAX_CTAS 256
 size_t moe_fused_trace_offset(int T, int H, int I, int E, int top_k, moe_dtype_t dtype);
 
 /* Workspace bytes moe_fused_forward needs for these sizes (0 if invalid). */
 size_t moe_fused_workspace_size(int T, int H, int I, int E, int top_k, moe_dtype_t dtype);
 
-/* Number of kernels one moe_fused_forward call with these sizes launches on
- * its stream (0 for T = 0, -1 if the sizes are invalid or unsupported).  Host
- * only: no CUDA call. */
+/* Number of kernels one moe_fused_forward call with these sizes and
+ * debug_flags = 0 launches on its stream (0 for T = 0, -1 if the sizes are
+ * invalid or unsupported); MOE_FLAG_ONE_KERNEL makes it 1 where it applies.
+ * Host only: no CUDA call. */
 int moe_fused_launch_count(int T, int H, int I, int E, int top_k, moe_dtype_t dtype);
 
 /*

@@ -24,6 +24,7 @@ MOE_DEBUG_TRACE = 0x2
 MOE_FLAG_TOKENS_IN_M = 0x4   # both GEMMs: tokens in the MMA M slot (ablation of the swap)
 MOE_FLAG_WEIGHTS_IN_M = 0x8  # both GEMMs: weight rows in the MMA M slot
 MOE_FLAG_NO_SM_PAIRS = 0x10  # wide FP8 gate/up tiles on one SM each (ablation of the SM pairs)
+MOE_FLAG_ONE_KERNEL = 0x20  # small batches: the whole layer as one cooperative kernel
 TRACE_MAX_CTAS = 256
 STATUS_NAMES = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED",
                 3: "MOE_ERR_WORKSPACE", 4: "MOE_ERR_CUDA", 5: "MOE_ERR_DEVICE_TIMEOUT",
@@ -375,4 +376,4 @@ __all__ = ["load", "moe_route_topk", "moe_align_by_expert", "moe_quantize_e4m3",
            "moe_inv_rope_quant_per_head", "moe_fused_forward", "moe_check_status", "alloc_workspace",
            "status_string", "MoeError", "make_step_events", "MoeFusedArgs", "MOE_DT_BF16", "MOE_DT_FP8_E4M3",
            "MOE_DEBUG_FORCE_TIMEOUT", "MOE_FLAG_TOKENS_IN_M",
-           "MOE_FLAG_WEIGHTS_IN_M", "MOE_FLAG_NO_SM_PAIRS", "LIB_PATH"]
+           "MOE_FLAG_WEIGHTS_IN_M", "MOE_FLAG_NO_SM_PAIRS", "MOE_FLAG_ONE_KERNEL", "LIB_PATH"]

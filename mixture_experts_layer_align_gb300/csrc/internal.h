@@ -60,7 +60,10 @@ struct Ctrl {
   int max_tile_rows;  // rows of the largest row tile
   int num_mtiles_w;     // the same for the list of wide (256-row) tiles, when written
   int max_tile_rows_w;
-  int pad[7];
+  // grid-wide arrival counters of the single-kernel small-batch path (zeroed
+  // by that kernel before its first grid synchronisation)
+  unsigned bar[4];
+  int pad[3];
 };
 static_assert(sizeof(Ctrl) == 64, "Ctrl layout");
 
@@ -97,7 +100,10 @@ struct AlignParams {
 cudaError_t launch_align(const AlignParams& p, cudaStream_t st);
 int align_chunk();
 // Router + alignment in one CTA for small batches (decode).  Used when
-// T*k <= kSmallMaxPairs, E <= kSmallMaxExperts and T*H <= kSmallMaxXElems.
+// T <= kSmallMaxTokens, T*k <= kSmallMaxPairs, E <= kSmallMaxExperts and
+// T*H <= kSmallMaxXElems (beyond 16 tokens the separate router and alignment
+// kernels were measured faster: fine-grained T=256 175 -> 136 us per call).
+constexpr int kSmallMaxTokens = 16;
 constexpr int kSmallMaxPairs = 2048;
 // Above this many pairs: two-pass alignment (per-chunk histograms) and x
 // quantised once per token before a byte-copy gather.
@@ -233,4 +239,48 @@ cudaError_t launch_gemm_pair(const GemmParams& p, const CUtensorMap& tma, const 
                              const CUtensorMap& tmb64, int max_clusters, cudaStream_t st);
 // Row-tile width of the unswapped placement (the token tile fills M = 128).
 constexpr int kTokMRows = 128;
+
+// ------------------------------------------------------------ small batches, one kernel
+// The whole layer for small batches in one cooperative persistent kernel (one
+// CTA per SM): routing, alignment, gather, gate/up GEMM + SiLU*up, h
+// quantisation, down GEMM + combine and the bf16 output, with grid-wide
+// arrival counters between the phases.  Used on request (MOE_FLAG_ONE_KERNEL)
+// when T*k <= kFusedMaxPairs, E <= kFusedMaxExperts and the fp32 combine
+// buffer is used.
+constexpr int kFusedMaxPairs = 2048;
+constexpr int kFusedMaxExperts = 256;
+constexpr int kFusedThreads = kGemmThreads;
+struct FusedParams {
+  const float* logits;
+  const __nv_bfloat16* x;
+  int T, H, I, E, k, renorm;
+  const float* w13_scale;  // [E] (FP8) or null (bf16)
+  const float* w2_scale;
+  __nv_bfloat16* out;      // [T, H]
+  int32_t* ids;            // [T*k] router outputs (caller's arrays or workspace)
+  float* wts;
+  int32_t* counts_out;     // [E] or null
+  Ctrl* ctrl;
+  float* amax_part;        // [gridDim] partial max |x| per CTA
+  int32_t* sorted_ids;     // aligned rows: pair id (T*k for padding)
+  float* sorted_w;         // aligned rows: router weight (0 for padding)
+  void* xs;                // aligned rows of x: E4M3 or bf16 [rows][H]
+  void* h;                 // [rows][I]: fp32 (FP8) or bf16
+  uint8_t* hq;             // [rows][I] E4M3 (FP8)
+  float* acc;              // [T, H] fp32 combine
+  float* part;             // split gate/up tiles: two slots per CTA
+  int* tile_cnt;           // per gate/up tile arrival counters
+  int n_tile_cnt;
+  unsigned stage_smem;     // dynamic shared memory for the pipeline stages
+  unsigned long long timeout_ns;
+  int debug;
+  unsigned long long* trace;  // [2][MOE_TRACE_MAX_CTAS][4] or null
+};
+// tm_*: w13 (128-row boxes), x rows (16/64-row boxes), w2, h codes (16/64).
+cudaError_t launch_fused_small(const FusedParams& p, const CUtensorMap& tm_w13,
+                               const CUtensorMap& tm_xs, const CUtensorMap& tm_xs64,
+                               const CUtensorMap& tm_w2, const CUtensorMap& tm_h,
+                               const CUtensorMap& tm_h64, int grid, cudaStream_t st);
+// Whether the device can run it (cooperative launch, one CTA per SM fits).
+bool fused_small_supported(int device);
 }  // namespace moe

@@ -136,7 +136,9 @@ Layout make_layout(int T, int H, int I, int E, int k, bool fp8) {
   };
   L.ctrl = take(sizeof(Ctrl));
   L.trace = take(sizeof(unsigned long long) * 2 * MOE_TRACE_MAX_CTAS * 4);
-  L.partials = take(sizeof(float) * std::max(L.n_partials, 1));
+  // router amax partials: one per router CTA, or one per CTA of the
+  // single-kernel small-batch path (at most one per SM)
+  L.partials = take(sizeof(float) * std::max(L.n_partials, 1024));
   L.ids = take(sizeof(int32_t) * L.P);
   L.wts = take(sizeof(float) * L.P);
   L.counts = take(sizeof(int32_t) * E);
@@ -320,10 +322,27 @@ size_t moe_fused_workspace_size(int T, int H, int I, int E, int top_k, moe_dtype
 
 namespace {
 
+// On request (MOE_FLAG_ONE_KERNEL), small batches take the single-kernel
+// path: the whole layer in one cooperative persistent kernel (weights in the
+// MMA M slot for both GEMMs).  The shape rule (host only):
+bool fused_small_shape(int T, int H, int I, int E, int k, int flags, const Layout& L) {
+  const long long P = static_cast<long long>(T) * k;
+  if (P > kFusedMaxPairs || E > kFusedMaxExperts || L.combine_rows) return false;
+  if (!(flags & MOE_FLAG_ONE_KERNEL) || (flags & MOE_FLAG_TOKENS_IN_M)) return false;
+  return H % 128 == 0 && I % 128 == 0;
+}
+
+bool fused_small(int T, int H, int I, int E, int k, int flags, const Layout& L, int device,
+                 int num_sms) {
+  if (!fused_small_shape(T, H, I, E, k, flags, L)) return false;
+  if (num_sms < 8 || num_sms > 256) return false;  // one partial slot pair per CTA (<= 256)
+  return fused_small_supported(device);
+}
+
 // Small batches take the single-CTA router + alignment kernel.
 bool small_front(int T, int H, int E, int k) {
   const long long P = static_cast<long long>(T) * k;
-  return P <= kSmallMaxPairs && E <= kSmallMaxExperts &&
+  return T <= kSmallMaxTokens && P <= kSmallMaxPairs && E <= kSmallMaxExperts &&
          static_cast<long long>(T) * H <= kSmallMaxXElems;
 }
 
@@ -403,6 +422,56 @@ moe_status_t fused_forward_impl(const moe_fused_args* a, void* workspace, size_t
 
   cudaStream_t s = stream;
   if (events && cudaEventRecord(events[0], stream) != cudaSuccess) return MOE_ERR_CUDA;
+  int cur_dev = 0;
+  if (cudaGetDevice(&cur_dev) != cudaSuccess) return MOE_ERR_CUDA;
+  if (fused_small(T, H, I, E, k, a->debug_flags, L, cur_dev, dev.num_sms)) {
+    FusedParams fp{};
+    fp.logits = a->router_logits;
+    fp.x = static_cast<const __nv_bfloat16*>(a->x);
+    fp.T = T;
+    fp.H = H;
+    fp.I = I;
+    fp.E = E;
+    fp.k = k;
+    fp.renorm = a->renormalize;
+    fp.w13_scale = fp8 ? a->w13_scale : nullptr;
+    fp.w2_scale = fp8 ? a->w2_scale : nullptr;
+    fp.out = static_cast<__nv_bfloat16*>(a->out);
+    fp.ids = ids;
+    fp.wts = wts;
+    fp.counts_out = a->counts_out;
+    fp.ctrl = ctrl;
+    fp.amax_part = partials;
+    fp.sorted_ids = sorted;
+    fp.sorted_w = sorted_w;
+    fp.xs = xs;
+    fp.h = h;
+    fp.hq = hq;
+    fp.acc = acc;
+    fp.part = part;
+    fp.tile_cnt = tile_cnt;
+    fp.n_tile_cnt = L.n_tile_cnt;
+    fp.timeout_ns = (a->debug_flags & MOE_DEBUG_FORCE_TIMEOUT) ? MOE_DEBUG_TIMEOUT_MS * 1000000ull
+                                                               : kWaitLimitNs;
+    fp.debug = a->debug_flags;
+    fp.trace = (a->debug_flags & MOE_DEBUG_TRACE)
+                   ? reinterpret_cast<unsigned long long*>(ws + L.trace)
+                   : nullptr;
+    const bool bf = !fp8;
+    const void* hb = fp8 ? static_cast<const void*>(hq) : static_cast<const void*>(h);
+    CUtensorMap m_w13, m_xs, m_xs64, m_w2, m_h, m_h64;
+    if (!make_tmap(&m_w13, a->w13, bf, H, static_cast<uint64_t>(E) * 2 * I, 128) ||
+        !make_tmap(&m_xs, xs, bf, H, L.pad_max, 16) || !make_tmap(&m_xs64, xs, bf, H, L.pad_max, 64) ||
+        !make_tmap(&m_w2, a->w2, bf, I, static_cast<uint64_t>(E) * H, 128) ||
+        !make_tmap(&m_h, hb, bf, I, L.pad_max, 16) || !make_tmap(&m_h64, hb, bf, I, L.pad_max, 64))
+      return MOE_ERR_CUDA;
+    if (launch_fused_small(fp, m_w13, m_xs, m_xs64, m_w2, m_h, m_h64, dev.num_sms, s) != cudaSuccess)
+      return MOE_ERR_CUDA;
+    if (events)
+      for (int i = 1; i < MOE_TIMED_EVENTS; ++i)
+        if (cudaEventRecord(events[i], stream) != cudaSuccess) return MOE_ERR_CUDA;
+    return MOE_OK;
+  }
   if (small_front(T, H, E, k)) {
     // 1-2 in one CTA: routing, amax of x, alignment, tile list, s_x
     SmallFrontParams sp{};

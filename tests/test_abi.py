@@ -56,9 +56,17 @@ def test_workspace_size_grows_with_tokens(lib):
 
 def test_launch_count(lib):
     fp8, bf16 = moe.MOE_DT_FP8_E4M3, moe.MOE_DT_BF16
-    # decode: one front kernel, gather, GEMM, quant h, GEMM, finalize
-    assert moe.moe_fused_launch_count(64, 4096, 14336, 8, 2, fp8) == 6
+    # up to 16 tokens: one front kernel (routing + alignment), gather, GEMM,
+    # quant h, GEMM, finalize
+    assert moe.moe_fused_launch_count(16, 4096, 14336, 8, 2, fp8) == 6
     assert moe.moe_fused_launch_count(4, 128, 256, 8, 2, bf16) == 5   # no quant of h
+    # more tokens: separate router and alignment kernels
+    assert moe.moe_fused_launch_count(64, 4096, 14336, 8, 2, fp8) == 7
+    assert moe.moe_fused_launch_count(256, 2048, 768, 128, 8, fp8) == 7
+    # E > 256: router, alignment, gather, GEMM, quant h, GEMM, finalize
+    assert moe.moe_fused_launch_count(4, 2048, 768, 512, 8, fp8) == 7
+    # pairs x H > 8M: rows per pair and a combine kernel instead
+    assert moe.moe_fused_launch_count(2048, 8192, 256, 8, 1, fp8) == 7
     # 512 x 8 pairs: separate router and alignment kernels
     assert moe.moe_fused_launch_count(512, 2048, 768, 128, 8, fp8) == 7
     # > 4096 pairs: chunk histograms as well; x quantised per token and
@@ -146,7 +154,7 @@ def test_binding_constants_match_header():
     enums = {m.group(1): int(m.group(2))
              for m in re.finditer(r"\b(MOE_(?:OK|ERR_\w+|DT_\w+)) = (\d+)", text)}
     for name in ("MOE_DEBUG_FORCE_TIMEOUT", "MOE_DEBUG_TRACE", "MOE_FLAG_TOKENS_IN_M",
-                 "MOE_FLAG_WEIGHTS_IN_M", "MOE_FLAG_NO_SM_PAIRS"):
+                 "MOE_FLAG_WEIGHTS_IN_M", "MOE_FLAG_NO_SM_PAIRS", "MOE_FLAG_ONE_KERNEL"):
         assert getattr(moe, name) == defines[name], name
     assert moe.TRACE_MAX_CTAS == defines["MOE_TRACE_MAX_CTAS"]
     assert len(moe.make_step_events.__defaults__) == 1

@@ -60,11 +60,14 @@ def run_case(moe, w, a, top_k, renorm, rows=None, repeat=1, flags=0):
     (70, 384, 2304, 16, 3, False, "fp8"),   # ragged rows, I > 2048
     (1000, 256, 512, 4, 2, True, "fp8"),    # 500 rows per expert: gate/up on SM pairs
 ])
-@pytest.mark.parametrize("placement", ["auto", "weights_in_m"])
-def test_fused_small(gpu_lib, T, H, I, E, k, renorm, dtype, placement):
+@pytest.mark.parametrize("path", ["auto", "weights_in_m", "one_kernel"])
+def test_fused_small(gpu_lib, T, H, I, E, k, renorm, dtype, path):
+    """The kernel sequence in both placements and, for batches of up to 2048
+    pairs, the single cooperative kernel must compute the same layer."""
     w = inputs.make_weights(H, I, E, dtype, seed=T)
     a = inputs.make_activations(T, H, E, "uniform", seed=T)
-    flags = gpu_lib.MOE_FLAG_WEIGHTS_IN_M if placement == "weights_in_m" else 0
+    flags = {"auto": 0, "weights_in_m": gpu_lib.MOE_FLAG_WEIGHTS_IN_M,
+             "one_kernel": gpu_lib.MOE_FLAG_ONE_KERNEL}[path]
     run_case(gpu_lib, w, a, k, renorm, repeat=2, flags=flags)
 
 
@@ -199,6 +202,16 @@ def test_fused_full_size(gpu_lib, name, T):
     w = _weights(name)
     a = inputs.make_activations(T, c["H"], c["E"], c["routing"], seed=0, device="cuda")
     run_case(gpu_lib, w, a, c["top_k"], True, rows=None)
+
+
+@pytest.mark.parametrize("name,T", [("decode_e8_top2", 1), ("decode_e8_top2", 64),
+                                    ("finegrained_e128", 256), ("skewed_e256", 128)])
+def test_fused_full_size_one_kernel(gpu_lib, name, T):
+    """The single cooperative kernel on the small-batch workloads, every row."""
+    c = inputs.workload(name)
+    w = _weights(name)
+    a = inputs.make_activations(T, c["H"], c["E"], c["routing"], seed=0, device="cuda")
+    run_case(gpu_lib, w, a, c["top_k"], True, rows=None, flags=gpu_lib.MOE_FLAG_ONE_KERNEL)
 
 
 @pytest.mark.parametrize("name,T", [("decode_e8_top2", 1), ("decode_e8_top2", 64),
