@@ -68,6 +68,12 @@ def parse():
     ap.add_argument("--placement", default="auto", choices=["auto", "weights", "tokens"],
                     help="MMA operand placement of both expert GEMMs: weight rows in M (the "
                          "swap), tokens in M (ablation), or the library's default choice")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="skip the per-workload sweep of every measured configuration")
+    ap.add_argument("--config-calls", type=int, default=50,
+                    help="calls per T in the per-workload sweep (at least 50)")
+    ap.add_argument("--one-kernel", action="store_true",
+                    help="small batches as one cooperative kernel (MOE_FLAG_ONE_KERNEL)")
     ap.add_argument("--no-sm-pairs", action="store_true",
                     help="ablation: wide FP8 gate/up tiles on one SM each instead of SM pairs "
                          "(tcgen05 cta_group::2)")
@@ -216,6 +222,156 @@ def tokens_list(args, cfg):
     return list(cfg["T"])
 
 
+def workload_config(name, cfg, Ts):
+    """The `config` object of the JSON line: the workload by name and its
+    sizes.  Both arms (ours and the reference arm) print exactly this dict."""
+    fp8 = cfg["dtype"] == "fp8"
+    return {"workload": name, "tokens": list(Ts), "H": cfg["H"], "I": cfg["I"], "E": cfg["E"],
+            "top_k": cfg["top_k"], "renormalize": True, "routing": cfg["routing"],
+            "weights": "e4m3 per-expert scale" if fp8 else "bf16",
+            "activations": "dynamic per-tensor e4m3" if fp8 else "bf16"}
+
+
+def layer_work(touched, T, H, I, E, k, fp8):
+    """Algorithmic bytes and FLOPs of one layer call (the touched experts'
+    weights, logits, x in, out; 2 x routed pairs x weight rows x K)."""
+    esize = 1 if fp8 else 2
+    nbytes = touched * 3 * H * I * esize + (8 * E if fp8 else 0) + T * E * 4 + 2 * T * H * 2
+    flops = 6.0 * T * k * H * I
+    return nbytes, flops
+
+
+def roofline_fractions(us, nbytes, flops, hbm_gbs, tc_tflops):
+    """(binding limit, fraction of it, HBM fraction, tensor fraction)."""
+    t = us * 1e-6
+    hbm = nbytes / t / 1e9 / hbm_gbs
+    tc = flops / t / 1e12 / tc_tflops
+    t_hbm = nbytes / (hbm_gbs * 1e9)
+    t_tc = flops / (tc_tflops * 1e12)
+    return ("hbm", hbm, hbm, tc) if t_hbm >= t_tc else ("tensor", tc, hbm, tc)
+
+
+def percentile(v, q):
+    v = sorted(v)
+    return v[min(len(v) - 1, max(0, int(round(q * (len(v) - 1)))))]
+
+
+def time_calls(call, n, warm=5):
+    """Device time of each of n back-to-back calls (CUDA events on the
+    current stream between consecutive calls, nothing inside a call), us."""
+    import torch
+    for i in range(warm):
+        call(i)
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(n + 1)]
+    torch.cuda.synchronize()
+    ev[0].record()
+    for i in range(n):
+        call(i)
+        ev[i + 1].record()
+    torch.cuda.synchronize()
+    return [ev[i].elapsed_time(ev[i + 1]) * 1e3 for i in range(n)]
+
+
+L2_BYTES = 129 * 2 ** 20
+
+
+def weight_copies(w, touched_bytes_min, inputs):
+    """Enough copies of the weights that consecutive calls, cycling through
+    them, never find their experts' weights in L2: >= 2 x L2 of distinct
+    weight bytes between two uses of one copy."""
+    n = min(512, max(2, -(-2 * L2_BYTES // max(touched_bytes_min, 1))))
+    out = [w]
+    for _ in range(n - 1):
+        out.append(inputs.Weights(w.w13.clone(), w.w2.clone(), w.w13_scale, w.w2_scale, w.dtype,
+                                  w.H, w.I, w.E))
+    return out
+
+
+def oracle_sample(cfg, Ts, w, acts):
+    """One oracle call per T (the prefill workloads: the smallest T only):
+    tokens/s of the fp64 CPU oracle on this host."""
+    import oracle
+    wc = [t.cpu() if t is not None else None for t in (w.w13, w.w2, w.w13_scale, w.w2_scale)]
+    sample_T = [min(Ts)] if min(Ts) >= 2048 else list(Ts)
+    el, tokens = 0.0, 0
+    for T in sample_T:
+        a = acts[T]
+        x, lg = a.x.cpu(), a.logits.cpu()
+        t0 = time.perf_counter()
+        oracle.moe_forward(x, lg, wc[0], wc[1], wc[2], wc[3], cfg["top_k"], True)
+        el += time.perf_counter() - t0
+        tokens += T
+    cores = oracle.max_threads()
+    return {"value": round(tokens / el, 2), "unit": "tokens/s", "cores": cores, "kind": "oracle",
+            "sample": f"one fp64 oracle call per T in {sample_T} ({tokens} tokens, {el:.1f} s)"}
+
+
+CONFIG_NAMES = ["tiny_bf16", "decode_e8_top2", "finegrained_e128", "skewed_e256",
+                "prefill_e128_uniform", "prefill_e128_zipf"]
+
+
+def config_sweep(moe, inputs, dev, hbm_peak, fp8_peak, bf16_peak, n_calls, with_cpu, flags=0):
+    """Every measured workload: per-T device time of a call (median, p10,
+    p90 over n_calls back-to-back calls, weights cold in L2), tokens/s, and
+    the fraction of the binding roofline (HBM bytes or tensor FLOPs)."""
+    import torch
+    out = {}
+    for name in CONFIG_NAMES:
+        cfg = inputs.workload(name)
+        H, I, E, k = cfg["H"], cfg["I"], cfg["E"], cfg["top_k"]
+        fp8 = cfg["dtype"] == "fp8"
+        dtype = moe.MOE_DT_FP8_E4M3 if fp8 else moe.MOE_DT_BF16
+        tc_peak = fp8_peak if fp8 else bf16_peak
+        Ts = list(cfg["T"])
+        w = inputs.make_weights(H, I, E, cfg["dtype"], seed=0, device=dev)
+        acts = {T: inputs.make_activations(T, H, E, cfg["routing"], seed=0, device=dev) for T in Ts}
+        outs = {T: torch.empty(T, H, dtype=torch.bfloat16, device=dev) for T in Ts}
+        wss = {T: moe.alloc_workspace(T, H, I, E, k, dtype, dev) for T in Ts}
+        touched = {}
+        for T in Ts:
+            cnt = torch.empty(E, dtype=torch.int32, device=dev)
+            a = acts[T]
+            moe.moe_fused_forward(a.x, a.logits, w.w13, w.w2, w.w13_scale, w.w2_scale, k, True,
+                                  out=outs[T], workspace=wss[T], counts_out=cnt, debug_flags=flags)
+            st = moe.moe_check_status(wss[T])
+            if st != 0:
+                raise RuntimeError(f"{name} T={T}: device status {moe.status_string(st)}")
+            touched[T] = int((cnt > 0).sum())
+        esize = 1 if fp8 else 2
+        copies = weight_copies(w, min(touched.values()) * 3 * H * I * esize, inputs)
+        rows = []
+        for T in Ts:
+            a = acts[T]
+
+            def call(i, T=T, a=a):
+                ww = copies[i % len(copies)]
+                moe.moe_fused_forward(a.x, a.logits, ww.w13, ww.w2, ww.w13_scale, ww.w2_scale, k,
+                                      True, out=outs[T], workspace=wss[T], debug_flags=flags)
+
+            us = time_calls(call, n_calls)
+            st = moe.moe_check_status(wss[T])
+            if st != 0:
+                raise RuntimeError(f"{name} T={T}: device status {moe.status_string(st)}")
+            med = statistics.median(us)
+            nbytes, flops = layer_work(touched[T], T, H, I, E, k, fp8)
+            bound, frac, hfrac, tfrac = roofline_fractions(med, nbytes, flops, hbm_peak, tc_peak)
+            rows.append({"T": T, "us_median": round(med, 2), "us_p10": round(percentile(us, 0.1), 2),
+                         "us_p90": round(percentile(us, 0.9), 2), "calls": len(us),
+                         "tokens_per_s": round(T / (med * 1e-6), 1), "touched_experts": touched[T],
+                         "layer_bytes": nbytes, "layer_flops": flops, "bound": bound,
+                         "frac": round(frac, 4), "hbm_frac": round(hfrac, 4),
+                         "tensor_frac": round(tfrac, 4)})
+        entry = {"config": workload_config(name, cfg, Ts), "weight_copies": len(copies),
+                 "per_T": rows,
+                 "tokens_per_s": round(sum(Ts) / (sum(r["us_median"] for r in rows) * 1e-6), 1)}
+        if with_cpu:
+            entry["cpu_baseline"] = oracle_sample(cfg, Ts, w, acts)
+        out[name] = entry
+        del w, copies, acts, outs, wss
+        torch.cuda.empty_cache()
+    return out
+
+
 # --------------------------------------------------------------------------- CPU oracle
 def time_oracle(cfg, Ts, weights_cpu, acts_cpu, min_seconds=10.0, max_passes=8):
     """Wall time of the CPU oracle over the T sweep; repeats whole passes
@@ -275,8 +431,7 @@ def run_reference(args, rank, world):
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": el / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": args.workload, "tokens": Ts, "H": cfg["H"], "I": cfg["I"],
-                   "E": cfg["E"], "top_k": cfg["top_k"], "routing": cfg["routing"]},
+        "config": workload_config(args.workload, cfg, Ts),
         "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
@@ -308,11 +463,9 @@ def run_ours(args, rank, local_rank, world):
              "tokens": moe.MOE_FLAG_TOKENS_IN_M}[args.placement]
     if args.no_sm_pairs:
         flags |= moe.MOE_FLAG_NO_SM_PAIRS
+    if args.one_kernel:
+        flags |= moe.MOE_FLAG_ONE_KERNEL
     w = inputs.make_weights(H, I, E, cfg["dtype"], seed=0, device=dev)
-    # second copy of the same weights in other buffers: consecutive calls
-    # alternate, so no call finds its weights in L2
-    w_alt = inputs.Weights(w.w13.clone(), w.w2.clone(), w.w13_scale, w.w2_scale, w.dtype, H, I, E)
-    copies = [w, w_alt]
     acts = {T: inputs.make_activations(T, H, E, cfg["routing"], seed=0, device=dev) for T in Ts}
     outs = {T: torch.empty(T, H, dtype=torch.bfloat16, device=dev) for T in Ts}
     wss = {T: moe.alloc_workspace(T, H, I, E, k, dtype, dev) for T in Ts}
@@ -338,12 +491,22 @@ def run_ours(args, rank, local_rank, world):
             gemm1_flops=2.0 * P * 2 * I * H, gemm2_flops=2.0 * P * H * I,
             layer_bytes=touched * 3 * H * I * esize + 8 * E + T * E * 4 + 2 * T * H * 2)
 
+    # copies of the weights in other buffers, cycled call to call, so that no
+    # call finds its experts' weights in L2
+    copies = weight_copies(w, min(stats[T]["touched"] for T in Ts) * 3 * I * H * esize, inputs)
+    n_copies = len(copies)
     calls_per_step = len(Ts)
-    launches_per_step = sum(moe.moe_fused_launch_count(T, H, I, E, k, dtype) for T in Ts)
+    def launches(T):
+        # the single cooperative kernel replaces the sequence where it applies
+        if args.one_kernel and T * k <= 2048 and E <= 256 and T * k * H <= (8 << 20):
+            return 1
+        return moe.moe_fused_launch_count(T, H, I, E, k, dtype)
+
+    launches_per_step = sum(launches(T) for T in Ts)
 
     def one_step(step_idx, events=None):
         for j, T in enumerate(Ts):
-            ww = copies[(step_idx * calls_per_step + j) % 2]
+            ww = copies[(step_idx * calls_per_step + j) % len(copies)]
             a = acts[T]
             moe.moe_fused_forward(a.x, a.logits, ww.w13, ww.w2, ww.w13_scale, ww.w2_scale, k,
                                   True, out=outs[T], workspace=wss[T], debug_flags=flags,
@@ -441,18 +604,30 @@ def run_ours(args, rank, local_rank, world):
 
     tokens_per_step = sum(Ts)
     value = job_tokens_per_s(world, tokens_per_step, K, elapsed_ms)
+    # per-T device time of a call without events inside it (events only
+    # between consecutive calls), median / p10 / p90 over >= 50 calls
     sweep = []
     for T in Ts:
-        us = statistics.median(per_T_call_us[T])
+        a = acts[T]
+
+        def call(i, T=T, a=a):
+            ww = copies[i % len(copies)]
+            moe.moe_fused_forward(a.x, a.logits, ww.w13, ww.w2, ww.w13_scale, ww.w2_scale, k,
+                                  True, out=outs[T], workspace=wss[T], debug_flags=flags)
+
+        us_all = time_calls(call, max(50, K))
+        us = statistics.median(us_all)
+        nbytes, flops = layer_work(stats[T]["touched"], T, H, I, E, k, fp8)
+        bound, frac, hfrac, tfrac = roofline_fractions(us, nbytes, flops, hbm_peak, tc_peak)
         sweep.append({
-            "T": T, "us_per_call": round(us, 2), "tokens_per_s": round(T / (us * 1e-6), 1),
+            "T": T, "us_median": round(us, 2), "us_p10": round(percentile(us_all, 0.1), 2),
+            "us_p90": round(percentile(us_all, 0.9), 2), "calls": len(us_all),
+            "tokens_per_s": round(T / (us * 1e-6), 1),
             "touched_experts": stats[T]["touched"], "max_rows_per_expert": stats[T]["max_rows"],
-            "layer_bytes": stats[T]["layer_bytes"],
-            "layer_hbm_frac": round(stats[T]["layer_bytes"] / (us * 1e-6) / 1e9 / hbm_peak, 4),
-            "layer_tensor_frac": round((stats[T]["gemm1_flops"] + stats[T]["gemm2_flops"])
-                                       / (us * 1e-6) / 1e12 / tc_peak, 4),
-            "gemm1_us": round(statistics.median(gemm1_ms[T]) * 1e3, 2),
-            "gemm2_us": round(statistics.median(gemm2_ms[T]) * 1e3, 2)})
+            "layer_bytes": nbytes, "bound": bound, "frac": round(frac, 4),
+            "hbm_frac": round(hfrac, 4), "tensor_frac": round(tfrac, 4),
+            "gemm1_us_events": round(statistics.median(gemm1_ms[T]) * 1e3, 2),
+            "gemm2_us_events": round(statistics.median(gemm2_ms[T]) * 1e3, 2)})
 
     # end to end through the same API: pinned host inputs -> device -> host output
     e2e = None
@@ -484,7 +659,7 @@ def run_ours(args, rank, local_rank, world):
                     dl[T].copy_(hl, non_blocking=True)
                     in_ready[T].record(copier)
             for j, T in enumerate(Ts):
-                ww = copies[(s * calls_per_step + j) % 2]
+                ww = copies[(s * calls_per_step + j) % len(copies)]
                 compute.wait_event(in_ready[T])
                 moe.moe_fused_forward(dx[T], dl[T], ww.w13, ww.w2, ww.w13_scale, ww.w2_scale, k,
                                       True, out=outs[T], workspace=wss[T], debug_flags=flags)
@@ -527,21 +702,29 @@ def run_ours(args, rank, local_rank, world):
         if dist is not None:
             dist.destroy_process_group()
         return
+    configs = None
+    if rank == 0 and world == 1 and not args.no_configs:
+        del copies
+        torch.cuda.empty_cache()
+        with ClockSampler(uuid) as clk2:
+            clk2.mark(True)
+            configs = config_sweep(moe, inputs, dev, hbm_peak, bf16_peak * FP8_OVER_BF16,
+                                   bf16_peak, max(50, args.config_calls),
+                                   not args.no_cpu_baseline, flags)
+            clk2.mark(False)
+        configs_clocks = clk2.summary()
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": K,
         "warmup": args.warmup, "ms_per_step": elapsed_ms / K, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "e4m3" if fp8 else "bf16",
         "data": "synthetic",
-        "config": {
-            "workload": f"{args.workload}: T in {Ts}, H={H}, I={I}, E={E}, top_k={k}, "
-                        f"renormalised, {cfg['routing']} routing, "
-                        + ("FP8 E4M3 weights (per-expert scale) + dynamic per-tensor FP8 "
-                           "activations" if fp8 else "bf16 weights"),
+        "config": workload_config(args.workload, cfg, Ts),
+        "setup": {
             "step": f"one moe_fused_forward per T ({calls_per_step} calls, {tokens_per_step} "
                     "tokens)",
-            "l2": "inputs larger than L2: two copies of the "
-                  f"{(w.w13.numel() + w.w2.numel()) * esize / 1e9:.2f} GB weights alternate "
-                  "call to call",
+            "l2": f"inputs larger than L2: {n_copies} copies of the "
+                  f"{(w.w13.numel() + w.w2.numel()) * esize / 1e9:.2f} GB weights, cycled call "
+                  "to call",
             "parallelism": f"replicas x{world}",
             "placement": {"auto": "gate/up: weights in the MMA M slot; down: weights in M "
                                    "if I > 2048 else tokens in M",
@@ -549,8 +732,11 @@ def run_ours(args, rank, local_rank, world):
                            "tokens": "tokens in the MMA M slot for both GEMMs (no swap)"}[
                               args.placement] + (
                               "; wide gate/up tiles on one SM each" if args.no_sm_pairs
-                              else "")},
+                              else "") + ("; small batches as one cooperative kernel"
+                                          if args.one_kernel else "")},
         "sweep": sweep,
+        "sweep_timing": "per call: CUDA events between consecutive back-to-back calls "
+                        "(none inside a call), weights cold in L2",
         "kernel_share": {n: round(step_ms[n] / total_kernel_ms, 4) for n in STEP_NAMES},
         "kernel_timing": "CUDA events between the kernels of every call, second pass of the "
                          f"same {K} steps ({instrumented_ms / K:.3f} ms/step with events)",
@@ -560,6 +746,15 @@ def run_ours(args, rank, local_rank, world):
         "e2e": e2e,
         "cpu_baseline": cpu,
     }
+    if configs is not None:
+        line["configs"] = configs
+        line["configs_timing"] = ("every measured workload: device time per call from CUDA "
+                                  "events between back-to-back calls (median, p10, p90), "
+                                  "weights cycled through enough copies to stay out of L2; "
+                                  "frac = fraction of the binding roofline (HBM bytes of the "
+                                  "touched experts + x/logits/out against measured hbm_gbs, or "
+                                  "6 x pairs x H x I FLOPs against the tensor peak)")
+        line["configs_clocks"] = configs_clocks
     print(json.dumps(line), flush=True)
     if dist is not None:
         dist.destroy_process_group()
