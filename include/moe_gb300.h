@@ -240,6 +240,32 @@ moe_status_t moe_fused_forward(const moe_fused_args* args, void* workspace, size
                                moe_stream_t stream);
 
 /*
+ * The same forward in two calls, for tensor-parallel shards (the pages
+ * measure at 8-way tensor parallelism, section "Triton JIT recompilation
+ * elimination").  A rank holds, per expert, the gate and up rows of its slice
+ * of I in w13 and the same columns of w2 (args.I = the slice; per-expert
+ * scales unchanged); routing is replicated.
+ *   moe_fused_forward_gate_up: routing, alignment, the x rows, the gate/up
+ *     GEMM + SiLU*up; leaves the max |h| of this rank's h as an fp32 word at
+ *     byte offset moe_fused_h_amax_offset() of the workspace (device memory).
+ *   moe_fused_forward_down: the E4M3 codes of h with the scale (that word) /
+ *     448, the down GEMM and the top-k weighted combine into args.out (this
+ *     rank's partial output).
+ * Between the two the caller replaces the word by its maximum over the ranks
+ * (e.g. an all-reduce MAX of that one float on the same stream), so every
+ * rank quantises h with the scale of the whole tensor, and after the second
+ * call sums the ranks' outputs (all-reduce SUM).  Both calls take the same
+ * args and workspace, with no other use of the workspace in between; the
+ * first call's status word and errors are as for moe_fused_forward.  With
+ * bf16 weights h is not quantised and the word is unused.
+ */
+moe_status_t moe_fused_forward_gate_up(const moe_fused_args* args, void* workspace,
+                                       size_t workspace_bytes, moe_stream_t stream);
+moe_status_t moe_fused_forward_down(const moe_fused_args* args, void* workspace,
+                                    size_t workspace_bytes, moe_stream_t stream);
+size_t moe_fused_h_amax_offset(void);
+
+/*
  * Same operation as moe_fused_forward, with the duration of every step made
  * measurable: events[i] (a cudaEvent_t created by the caller) is recorded on
  * `stream` before step i and events[7] after the last step.  Steps: 0 routing,

@@ -96,13 +96,18 @@ def load():
         L.moe_fused_forward.argtypes = [ctypes.POINTER(MoeFusedArgs), P, sz, P]
         L.moe_fused_forward_timed.argtypes = [ctypes.POINTER(MoeFusedArgs), P, sz, P,
                                                ctypes.POINTER(ctypes.c_void_p), i]
+        L.moe_fused_forward_gate_up.argtypes = [ctypes.POINTER(MoeFusedArgs), P, sz, P]
+        L.moe_fused_forward_down.argtypes = [ctypes.POINTER(MoeFusedArgs), P, sz, P]
+        L.moe_fused_h_amax_offset.argtypes = []
+        L.moe_fused_h_amax_offset.restype = sz
         L.moe_check_status.argtypes = [P, P]
         L.moe_status_string.argtypes = [i]
         L.moe_status_string.restype = ctypes.c_char_p
         L.moe_last_error_detail.argtypes = []
         L.moe_last_error_detail.restype = ctypes.c_char_p
         for name in ("moe_route_topk", "moe_align_by_expert", "moe_quantize_e4m3",
-                     "moe_fused_forward", "moe_fused_forward_timed", "moe_check_status"):
+                     "moe_fused_forward", "moe_fused_forward_timed", "moe_check_status",
+                     "moe_fused_forward_gate_up", "moe_fused_forward_down"):
             getattr(L, name).restype = ctypes.c_int
         _lib = L
         return _lib
@@ -347,6 +352,37 @@ def moe_fused_forward(x, router_logits, w13, w2, w13_scale, w2_scale, top_k: int
     return out
 
 
+def moe_fused_forward_gate_up(x, router_logits, w13, w2, w13_scale, w2_scale, top_k: int,
+                              renormalize: bool, out, workspace, stream=None):
+    """First of the two calls of a tensor-parallel shard (include/moe_gb300.h):
+    routing through the gate/up GEMM; this rank's max |h| is left in the
+    workspace (see h_amax_view)."""
+    args, _ = _fused_args(x, router_logits, w13, w2, w13_scale, w2_scale, top_k, renormalize,
+                          out, None, None, None, 0)
+    _check(load().moe_fused_forward_gate_up(ctypes.byref(args), _ptr(workspace),
+                                            workspace.numel(), _stream(stream)),
+           "moe_fused_forward_gate_up")
+
+
+def moe_fused_forward_down(x, router_logits, w13, w2, w13_scale, w2_scale, top_k: int,
+                           renormalize: bool, out, workspace, stream=None):
+    """Second call: h codes with the scale from the workspace's max |h| word,
+    the down GEMM and the combine into `out` (this rank's partial output)."""
+    args, _ = _fused_args(x, router_logits, w13, w2, w13_scale, w2_scale, top_k, renormalize,
+                          out, None, None, None, 0)
+    _check(load().moe_fused_forward_down(ctypes.byref(args), _ptr(workspace),
+                                         workspace.numel(), _stream(stream)),
+           "moe_fused_forward_down")
+    return out
+
+
+def h_amax_view(workspace):
+    """The workspace's fp32 max |h| word as a one-element tensor view."""
+    import torch
+    off = int(load().moe_fused_h_amax_offset())
+    return workspace[off:off + 4].view(torch.float32)
+
+
 def make_step_events(n: int = 8):
     """n timing events, each recorded once so that its CUDA handle exists."""
     import torch
@@ -371,7 +407,8 @@ def moe_check_status(workspace, stream=None) -> int:
     return int(load().moe_check_status(_ptr(workspace), _stream(stream)))
 
 
-__all__ = ["load", "moe_route_topk", "moe_align_by_expert", "moe_quantize_e4m3",
+__all__ = ["load", "moe_fused_forward_gate_up", "moe_fused_forward_down", "h_amax_view",
+           "moe_route_topk", "moe_align_by_expert", "moe_quantize_e4m3",
            "moe_fused_workspace_size", "moe_fused_launch_count", "moe_inv_rope_scratch_size",
            "moe_inv_rope_quant_per_head", "moe_fused_forward", "moe_check_status", "alloc_workspace",
            "status_string", "MoeError", "make_step_events", "MoeFusedArgs", "MOE_DT_BF16", "MOE_DT_FP8_E4M3",

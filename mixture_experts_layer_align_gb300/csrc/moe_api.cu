@@ -4,6 +4,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
+#include <stddef.h>
 #include <stdint.h>
 #include <stdio.h>
 
@@ -348,8 +349,11 @@ bool small_front(int T, int H, int E, int k) {
 
 // The launch sequence.  When `events` is non-null, events[i] is recorded on
 // the stream before step i (i = 0..6) and events[7] after the last step.
+// phase 0: the whole layer; 1: routing through the gate/up GEMM; 2: the
+// quantisation of h (with the max |h| found in the workspace), the down GEMM
+// and the output (tensor-parallel shards reduce the max between the two).
 moe_status_t fused_forward_impl(const moe_fused_args* a, void* workspace, size_t workspace_bytes,
-                                moe_stream_t stream, cudaEvent_t const* events) {
+                                moe_stream_t stream, cudaEvent_t const* events, int phase = 0) {
   if (!a) return MOE_ERR_INVALID_ARG;
   const int T = a->T, H = a->H, I = a->I, E = a->E, k = a->top_k;
   if (T < 0 || H <= 0 || I <= 0 || E < 1 || E > kMaxExperts || k < 1 || k > E)
@@ -424,7 +428,7 @@ moe_status_t fused_forward_impl(const moe_fused_args* a, void* workspace, size_t
   if (events && cudaEventRecord(events[0], stream) != cudaSuccess) return MOE_ERR_CUDA;
   int cur_dev = 0;
   if (cudaGetDevice(&cur_dev) != cudaSuccess) return MOE_ERR_CUDA;
-  if (fused_small(T, H, I, E, k, a->debug_flags, L, cur_dev, dev.num_sms)) {
+  if (phase == 0 && fused_small(T, H, I, E, k, a->debug_flags, L, cur_dev, dev.num_sms)) {
     FusedParams fp{};
     fp.logits = a->router_logits;
     fp.x = static_cast<const __nv_bfloat16*>(a->x);
@@ -472,7 +476,9 @@ moe_status_t fused_forward_impl(const moe_fused_args* a, void* workspace, size_t
         if (cudaEventRecord(events[i], stream) != cudaSuccess) return MOE_ERR_CUDA;
     return MOE_OK;
   }
-  if (small_front(T, H, E, k)) {
+  if (phase == 2) {
+    // (routing, alignment and the x rows were written by the first call)
+  } else if (small_front(T, H, E, k)) {
     // 1-2 in one CTA: routing, amax of x, alignment, tile list, s_x
     SmallFrontParams sp{};
     sp.logits = a->router_logits;
@@ -539,7 +545,9 @@ moe_status_t fused_forward_impl(const moe_fused_args* a, void* workspace, size_t
   //    FP8 batches quantise each token once and scatter it to its k rows,
   //    smaller ones gather (and quantise) per aligned row; zero the combine
   //    buffer
-  if (L.large && fp8) {
+  if (phase == 2) {
+    // (written by the first call)
+  } else if (L.large && fp8) {
     if (launch_quant_scatter(static_cast<const __nv_bfloat16*>(a->x), T, H, k, inv_slot, counts,
                              offsets, E, ctrl, static_cast<uint8_t*>(xs), acc, acc_elems,
                              dev.num_sms, s) != cudaSuccess)
@@ -606,7 +614,9 @@ moe_status_t fused_forward_impl(const moe_fused_args* a, void* workspace, size_t
   const long long work1 = max_tiles1 * g1.nb_count * g1.k_steps;
   const int grid1 = static_cast<int>(std::max<long long>(1, std::min<long long>(ctas, work1)));
   if (events && cudaEventRecord(events[3], stream) != cudaSuccess) return MOE_ERR_CUDA;
-  if (pair1) {
+  if (phase == 2) {
+    // (the gate/up GEMM ran in the first call)
+  } else if (pair1) {
     GemmParams gp = g1;
     gp.nb_count = I / 256;  // units: (wide row tile, pair of weight blocks)
     const long long units = max_tiles1 * gp.nb_count;
@@ -618,6 +628,8 @@ moe_status_t fused_forward_impl(const moe_fused_args* a, void* workspace, size_t
              cudaSuccess) {
     return MOE_ERR_CUDA;
   }
+
+  if (phase == 1) return MOE_OK;  // max |h| of this call is in the workspace
 
   // 5. dynamic scale of h and its E4M3 codes
   if (events && cudaEventRecord(events[4], stream) != cudaSuccess) return MOE_ERR_CUDA;
@@ -679,6 +691,18 @@ moe_status_t moe_fused_forward(const moe_fused_args* a, void* workspace, size_t 
                                moe_stream_t stream) {
   return fused_forward_impl(a, workspace, workspace_bytes, stream, nullptr);
 }
+
+moe_status_t moe_fused_forward_gate_up(const moe_fused_args* a, void* workspace,
+                                       size_t workspace_bytes, moe_stream_t stream) {
+  return fused_forward_impl(a, workspace, workspace_bytes, stream, nullptr, 1);
+}
+
+moe_status_t moe_fused_forward_down(const moe_fused_args* a, void* workspace,
+                                    size_t workspace_bytes, moe_stream_t stream) {
+  return fused_forward_impl(a, workspace, workspace_bytes, stream, nullptr, 2);
+}
+
+size_t moe_fused_h_amax_offset(void) { return offsetof(Ctrl, amax_h); }
 
 size_t moe_fused_trace_offset(int T, int H, int I, int E, int top_k, moe_dtype_t dtype) {
   if (moe_fused_workspace_size(T, H, I, E, top_k, dtype) == 0) return 0;

@@ -61,7 +61,7 @@ def lib():
             L.oracle_align.argtypes = [P, i, i, i, i, P, P, P, P, P]
             L.oracle_align.restype = None
             L.oracle_moe_forward.argtypes = [P, P, P, P, P, P, i, i, i, i, i, i, i, P, i, P, P, P,
-                                             P, P, P, i]
+                                             P, P, P, ctypes.c_float, P, i]
             L.oracle_moe_forward.restype = ctypes.c_int
             L.oracle_inv_rope_quant.argtypes = [P, P, P, P, i, i, i, i, P, P, P]
             L.oracle_inv_rope_quant.restype = i
@@ -157,13 +157,16 @@ def align(ids, E: int, block_m: int):
 
 
 def moe_forward(x, logits, w13, w2, w13_scale, w2_scale, top_k: int, renormalize: bool,
-                rows=None, nthreads: int = 0):
+                rows=None, nthreads: int = 0, h_amax: float | None = None):
     """Whole-layer oracle.
 
     x: bf16 [T,H] (torch) or int16/uint16 bits; logits fp32 [T,E];
     w13 [E,2I,H], w2 [E,H,I]: uint8 E4M3 codes (scales given) or bf16 (scales None).
     rows: optional token indices whose output rows are wanted (all when None).
-    Returns dict(out fp64 [n_rows,H], ids, weights, counts, s_x, s_h).
+    h_amax: FP8 only: the max |h| the scale of h is taken from instead of this
+    call's own (a tensor-parallel shard passes the max over all shards).
+    Returns dict(out fp64 [n_rows,H], ids, weights, counts, s_x, s_h, h_amax)
+    where h_amax is this call's own max |h| over its routed pairs.
     """
     xb = _np(x, np.uint16)
     lg = _np(logits, np.float32)
@@ -190,14 +193,17 @@ def moe_forward(x, logits, w13, w2, w13_scale, w2_scale, top_k: int, renormalize
     counts = np.zeros(E, np.int32)
     sx = np.zeros(1, np.float32)
     sh = np.zeros(1, np.float32)
+    ha = np.zeros(1, np.float32)
     rc = lib().oracle_moe_forward(_ptr(xb), _ptr(lg), _ptr(w13n), _ptr(w2n), _ptr(s13), _ptr(s2),
                                   int(is_fp8), T, H, I, E, top_k, int(bool(renormalize)),
                                   _ptr(rows_np), n_rows, _ptr(out), _ptr(ids), _ptr(w),
-                                  _ptr(counts), _ptr(sx), _ptr(sh), int(nthreads))
+                                  _ptr(counts), _ptr(sx), _ptr(sh),
+                                  float(h_amax) if h_amax is not None else 0.0, _ptr(ha),
+                                  int(nthreads))
     if rc != 0:
         raise RuntimeError(f"oracle_moe_forward failed ({rc})")
     return dict(out=out[:n_rows], ids=ids[:P].reshape(T, top_k), weights=w[:P].reshape(T, top_k),
-                counts=counts, s_x=float(sx[0]), s_h=float(sh[0]))
+                counts=counts, s_x=float(sx[0]), s_h=float(sh[0]), h_amax=float(ha[0]))
 
 
 def inv_rope_quant(x, positions, cos_tab, sin_tab):

@@ -220,6 +220,11 @@ static double silu(double z) { return z / (1.0 + exp(-z)); }
  *            `rows` (all T tokens in order when rows == NULL, n_rows = T)
  *   ids, weights, counts   routing results [T,k], [T,k], [E] (may be NULL)
  *   s_x_out, s_h_out       the activation scales used (FP8; may be NULL)
+ *   h_amax_in              > 0: the max |h| the scale of h is taken from, in
+ *                          place of this call's own (tensor-parallel shards:
+ *                          the max over every shard's h); <= 0: this call's
+ *   h_amax_out             this call's own max |h| over its routed pairs (FP8;
+ *                          may be NULL)
  *   nthreads               OpenMP threads (<= 0: runtime default)
  * The dynamic scale of h spans every routed pair of the call, so in the FP8
  * path h is formed for all pairs even when only some output rows are asked for.
@@ -229,7 +234,8 @@ int oracle_moe_forward(const uint16_t* x, const float* logits, const void* w13, 
                        const float* w13_scale, const float* w2_scale, int is_fp8, int T, int H,
                        int I, int E, int k, int renormalize, const int32_t* rows, int n_rows,
                        double* out, int32_t* ids_out, double* weights_out, int32_t* counts_out,
-                       float* s_x_out, float* s_h_out, int nthreads) {
+                       float* s_x_out, float* s_h_out, float h_amax_in, float* h_amax_out,
+                       int nthreads) {
   if (T < 0 || H <= 0 || I <= 0 || E <= 0 || k <= 0 || k > E) return 1;
   if (rows == NULL) n_rows = T;
 #ifdef _OPENMP
@@ -315,7 +321,8 @@ int oracle_moe_forward(const uint16_t* x, const float* logits, const void* w13, 
       float a = fabsf((float)h[i]);
       if (a > amax) amax = a;
     }
-    s_h = act_scale_from_amax(amax);
+    if (h_amax_out) *h_amax_out = amax;
+    s_h = act_scale_from_amax(h_amax_in > 0.0f ? h_amax_in : amax);
 #pragma omp parallel for schedule(static)
     for (long i = 0; i < P * (long)I; ++i)
       h[i] = dec[quantize(h[i], s_h)] * (double)s_h;
