@@ -383,8 +383,14 @@ __global__ void __launch_bounds__(kAlignThreads, 1) route_align_small_kernel(Sma
   __syncthreads();
   const int c = tid < E ? s_cnt[tid] : 0;
   const int padded = (c + kAlignBlock - 1) / kAlignBlock * kAlignBlock;
-  int total = 0;
-  const int off = block_exclusive_scan_1024(padded, s_tmp, &total);
+  // one scan for both prefixes: padded rows (high bits) and row tiles (low 12
+  // bits; at most (P + 142 E) / 128 < 4096 tiles)
+  const int nt = (tid < E && padded > 0) ? (padded + p.bn_max - 1) / p.bn_max : 0;
+  int tot_packed = 0;
+  const int packed = block_exclusive_scan_1024((padded << 12) | nt, s_tmp, &tot_packed);
+  const int off = packed >> 12;
+  const int first_tile = packed & 0xfff;
+  const int total = tot_packed >> 12;
   if (tid < E) s_run[tid] = off;
   __syncthreads();
   // stable placement in pair-id order (one warp), padding sentinels
@@ -421,7 +427,17 @@ __global__ void __launch_bounds__(kAlignThreads, 1) route_align_small_kernel(Sma
     p.ids[q] = s_ids[q];
     p.wts[q] = s_w[q];
   }
-  const int2 tl = write_mtiles(tid, E, padded, off, kAlignBlock, p.bn_max, p.mtiles, s_tmp);
+  // GEMM row tiles of each expert (as write_mtiles, from the packed scan)
+  const int per = nt > 0 ? ((padded + nt - 1) / nt + kAlignBlock - 1) / kAlignBlock * kAlignBlock : 0;
+  for (int j = 0; j < nt; ++j)
+    p.mtiles[first_tile + j] = make_int4(tid, off + j * per, min(per, padded - j * per) | (nt << 12),
+                                         first_tile);
+  const int wmax = static_cast<int>(__reduce_max_sync(kFull, static_cast<unsigned>(per)));
+  if (lane == 0) s_tmp[warp] = wmax;  // (s_tmp is free again after the scan's last sync)
+  __syncthreads();
+  int2 tl = make_int2(tot_packed & 0xfff, 0);
+  for (int w = 0; w < 32; ++w) tl.y = max(tl.y, s_tmp[w]);
+  __syncthreads();
   const int2 tw = p.mtiles_w ? write_mtiles(tid, E, padded, off, kAlignBlock, kWideRows, p.mtiles_w,
                                             s_tmp)
                              : make_int2(0, 0);

@@ -114,6 +114,7 @@ __device__ void route_token_reg(const float* __restrict__ src, int E, int k, int
     z = warp_sum(z);
   }
   float sel = 0.f;
+  uint32_t my_key = 0u;  // k <= 32: lane j keeps the j-th selected key
   for (int j = 0; j < k; ++j) {
     uint32_t bk = 0u;
     int bi = 0;
@@ -131,12 +132,22 @@ __device__ void route_token_reg(const float* __restrict__ src, int E, int k, int
       for (int i = 0; i < R; ++i)
         if (i == (win >> 5)) key[i] = 0u;
     }
-    const float ex = expf(key_float(kmax) - m);
-    sel += ex;
-    if (lane == 0) {
-      id_row[j] = win;
-      w_row[j] = ex;
+    if (lane == 0) id_row[j] = win;
+    if (k <= 32) {
+      if (lane == j) my_key = kmax;
+    } else {
+      const float ex = expf(key_float(kmax) - m);
+      sel += ex;
+      if (lane == 0) w_row[j] = ex;
     }
+  }
+  if (k <= 32) {
+    // the k probabilities in parallel, one lane each
+    const float ex = lane < k ? expf(key_float(my_key) - m) : 0.f;
+    const float denom = renorm ? warp_sum(ex) : z;
+    if (lane < k) w_row[lane] = __fdiv_rn(ex, denom);
+    __syncwarp();
+    return;
   }
   __syncwarp();
   const float denom = renorm ? sel : z;
