@@ -947,7 +947,8 @@ def run_rope(args, rank, local_rank):
     line = {"metric": "inverse-RoPE + per-head FP8 quant tokens/s (32 heads x 128)",
             "value": big["tokens_per_s"], "unit": "tokens/s", "steps": K, "warmup": args.warmup,
             "config": {"workload": "x bf16 [T, 32, 128], positions < 8192, fp32 cos/sin tables; "
-                                   "two kernels (per-head amax, quantise)",
+                                   "one cooperative kernel up to 1216 tokens, else three "
+                                   "launches (per-head amax, scale fold, quantise)",
                        "l2": "four input copies rotate call to call"},
             "sweep": sweep,
             "roofline": {"bound": "hbm", "achieved": round(big["algorithmic_bytes"] /

@@ -15,25 +15,36 @@
 // Shapes are runtime values: one binary for every T, head count and (power of
 // two) head size.
 //
-// Two passes over x (bf16 [T][NH][D]), three launches:
+// Two passes over x (bf16 [T][NH][D]).  Large inputs, three launches:
 //   1. rope_pass_kernel<false>: per-head maxima of |y| per CTA -> partials;
 //   2. rope_fold_kernel (one CTA): the NH scales and the status word;
 //   3. rope_pass_kernel<true>: rotate again, divide by the head's scale,
 //      write the codes.
-// A warp takes one token at a time: one load of its position and of the
+// Small inputs (at most two rounds of two work items per warp on one CTA of
+// 512 threads per SM), one cooperative launch, rope_coop_kernel: pass 1,
+// one grid synchronisation, every CTA folds the maxima itself, pass 2 (the
+// latency of the three launches is what small inputs pay for; at 8192 tokens
+// of 32 heads the single launch's 16 warps per SM keep too few loads in
+// flight: 82 against 55 us).
+// Three-launch path: a warp takes one token at a time: one load of its position and of the
 // cos/sin entries of its lane's 4 pairs, then the token's heads, 32/(D/8) per
 // iteration (a group of D/8 lanes per head vector, 8 elements per lane: one
 // 16-byte load of x, one 8-byte store of codes), several iterations' loads in
 // flight.  Per-head maxima reduce inside each group, then one shared-memory
 // atomic per group.
+#include <cooperative_groups.h>
 #include <cuda_bf16.h>
 #include <stdint.h>
+
+#include <algorithm>
 
 #include "internal.h"
 #include "ptx.cuh"
 
 namespace moe {
 namespace {
+
+namespace cg = cooperative_groups;
 
 constexpr int kRopeThreads = 256;  // 8 warps: 8 tokens at a time per CTA
 constexpr int kRopeBatch = 4;      // head iterations whose x loads are in flight together
@@ -169,6 +180,152 @@ __global__ void __launch_bounds__(1024)
   }
 }
 
+constexpr int kCoopThreads = 512;  // 16 warps per CTA, at most one CTA per SM
+constexpr int kCoopBatch = 2;      // warp iterations of head vectors per item
+
+// One pass over this CTA's share of the work.  An item is (token, group of
+// hp * kCoopBatch head vectors); a warp takes two items per round, so that
+// the round costs two dependent memory round trips for both (x and the
+// positions, then the cos/sin entries of those positions).  kQuant = false:
+// the CTA's per-head maxima of |y| into s_head (max |y| bits), a position
+// outside the tables into *bad_out.  kQuant = true: codes with the scales in
+// s_head (fp32 bits).
+template <bool kQuant>
+__device__ __forceinline__ void rope_items_pass(const __nv_bfloat16* __restrict__ x,
+                                          const int32_t* __restrict__ pos,
+                                          const float* __restrict__ cos_t,
+                                          const float* __restrict__ sin_t, int T, int NH, int D,
+                                          int max_pos, unsigned* s_head,
+                                          uint8_t* __restrict__ codes, int* bad_out) {
+  const int lane = threadIdx.x & 31;
+  const int n8 = D >> 3;              // lanes per head vector (a power of two <= 32)
+  const int lg8 = __ffs(n8) - 1;
+  const int hp = 32 >> lg8;           // head vectors per warp iteration
+  const int c8 = lane & (n8 - 1);
+  const int hoff = lane >> lg8;
+  const int gh = hp * kCoopBatch;     // head vectors per item
+  const int ngroups = (NH + gh - 1) / gh;
+  const long long n_items = static_cast<long long>(T) * ngroups;
+  const long long nwarps = static_cast<long long>(gridDim.x) * (blockDim.x >> 5);
+  const long long w0 = static_cast<long long>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  int bad = 0;
+  for (long long i0 = w0; i0 < n_items; i0 += 2 * nwarps) {
+    uint4 v[2][kCoopBatch];
+    int pp[2], tt[2], hb[2];
+    bool live[2];
+#pragma unroll
+    for (int it = 0; it < 2; ++it) {
+      const long long i = i0 + it * nwarps;
+      live[it] = i < n_items;
+      tt[it] = live[it] ? static_cast<int>(i / ngroups) : 0;
+      hb[it] = live[it] ? static_cast<int>(i - static_cast<long long>(tt[it]) * ngroups) * gh : 0;
+      pp[it] = live[it] ? pos[tt[it]] : 0;
+      const size_t row0 = static_cast<size_t>(tt[it]) * NH;
+#pragma unroll
+      for (int u = 0; u < kCoopBatch; ++u) {
+        const int h = hb[it] + u * hp + hoff;
+        v[it][u] = (live[it] && h < NH) ? *reinterpret_cast<const uint4*>(x + (row0 + h) * D + c8 * 8)
+                                        : make_uint4(0, 0, 0, 0);
+      }
+    }
+    float4 cs[2], sn[2];
+#pragma unroll
+    for (int it = 0; it < 2; ++it) {
+      int p = pp[it];
+      if (live[it] && (p < 0 || p >= max_pos)) {
+        bad = 1;
+        p = 0;
+      }
+      const size_t tab = static_cast<size_t>(live[it] ? p : 0) * (D / 2) + c8 * 4;
+      cs[it] = *reinterpret_cast<const float4*>(cos_t + tab);
+      sn[it] = *reinterpret_cast<const float4*>(sin_t + tab);
+    }
+#pragma unroll
+    for (int it = 0; it < 2; ++it) {
+      if (!live[it]) continue;  // uniform over the warp
+      const size_t row0 = static_cast<size_t>(tt[it]) * NH;
+#pragma unroll
+      for (int u = 0; u < kCoopBatch; ++u) {
+        const int h = hb[it] + u * hp + hoff;
+        float y[8];
+        rotate8(v[it][u], cs[it], sn[it], y);
+        if (kQuant) {
+          if (h < NH) {
+            const float sc = __uint_as_float(s_head[h]);
+            const float rsc = __frcp_rn(sc);  // codes of y / sc (see div_for_e4m3)
+            uint2 q;
+            q.x = static_cast<uint32_t>(quant2(y[0], y[1], sc, rsc)) |
+                  (static_cast<uint32_t>(quant2(y[2], y[3], sc, rsc)) << 16);
+            q.y = static_cast<uint32_t>(quant2(y[4], y[5], sc, rsc)) |
+                  (static_cast<uint32_t>(quant2(y[6], y[7], sc, rsc)) << 16);
+            *reinterpret_cast<uint2*>(codes + (row0 + h) * D + c8 * 8) = q;
+          }
+        } else {
+          float m = 0.f;
+#pragma unroll
+          for (int j = 0; j < 8; ++j) m = fmaxf(m, fabsf(y[j]));
+          // maximum over the group of lanes of one head vector
+          for (int o = n8 >> 1; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+          if (c8 == 0 && h < NH && m > 0.f) atomicMax(&s_head[h], __float_as_uint(m));
+        }
+      }
+    }
+  }
+  if (!kQuant && bad) *bad_out = 1;
+}
+
+// The whole operation: pass 1, grid synchronisation, per-head scales, pass 2.
+// partials: [NH][gridDim] per-CTA maxima (head-major: a head's maxima are
+// contiguous), then [gridDim] flags.
+__global__ void __launch_bounds__(kCoopThreads, 1)
+    rope_coop_kernel(const __nv_bfloat16* __restrict__ x, const int32_t* __restrict__ pos,
+                     const float* __restrict__ cos_t, const float* __restrict__ sin_t, int T,
+                     int NH, int D, int max_pos, float* __restrict__ partials,
+                     float* __restrict__ scales, uint8_t* __restrict__ codes, Ctrl* ctrl) {
+  extern __shared__ unsigned s_head[];  // [NH]: max|y| bits, then the scales
+  __shared__ int s_bad;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
+  const int G = static_cast<int>(gridDim.x);
+  for (int h = threadIdx.x; h < NH; h += blockDim.x) s_head[h] = 0u;
+  if (threadIdx.x == 0) s_bad = 0;
+  __syncthreads();
+  rope_items_pass<false>(x, pos, cos_t, sin_t, T, NH, D, max_pos, s_head, nullptr, &s_bad);
+  __syncthreads();
+  for (int h = threadIdx.x; h < NH; h += blockDim.x)
+    partials[static_cast<size_t>(h) * G + blockIdx.x] = __uint_as_float(s_head[h]);
+  if (threadIdx.x == 0) partials[static_cast<size_t>(G) * NH + blockIdx.x] = s_bad ? 1.f : 0.f;
+  // nothing above waits on another CTA, so every CTA arrives here
+  cg::this_grid().sync();
+  // every CTA folds the per-CTA maxima into the scales (a warp per head)
+  for (int h = warp; h < NH; h += nwarps) {
+    const float* ph = partials + static_cast<size_t>(h) * G;
+    float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;  // independent chains: loads in flight
+    int b = lane;
+    for (; b + 96 < G; b += 128) {
+      a0 = fmaxf(a0, __ldcg(ph + b));
+      a1 = fmaxf(a1, __ldcg(ph + b + 32));
+      a2 = fmaxf(a2, __ldcg(ph + b + 64));
+      a3 = fmaxf(a3, __ldcg(ph + b + 96));
+    }
+    for (; b < G; b += 32) a0 = fmaxf(a0, __ldcg(ph + b));
+    float a = fmaxf(fmaxf(a0, a1), fmaxf(a2, a3));
+    for (int o = 16; o > 0; o >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
+    const float sc = a > 0.f ? __fdiv_rn(a, 448.f) : 1.f;
+    if (lane == 0) {
+      s_head[h] = __float_as_uint(sc);
+      if (blockIdx.x == 0) scales[h] = sc;
+    }
+  }
+  if (blockIdx.x == 0 && warp == 0) {
+    int bad = 0;
+    for (int b = lane; b < G; b += 32) bad |= __ldcg(partials + static_cast<size_t>(G) * NH + b) != 0.f;
+    bad = __any_sync(0xffffffffu, bad);
+    if (lane == 0) ctrl->err = bad ? kDevErrRange : 0;
+  }
+  __syncthreads();
+  rope_items_pass<true>(x, pos, cos_t, sin_t, T, NH, D, max_pos, s_head, codes, nullptr);
+}
+
 }  // namespace
 
 int rope_grid(long long T, int NH, int D, int num_sms) {
@@ -185,8 +342,29 @@ cudaError_t launch_inv_rope_quant(const __nv_bfloat16* x, const int32_t* pos, co
                                   const float* sin_t, int T, int NH, int D, int max_pos,
                                   uint8_t* codes, float* scales, Ctrl* ctrl, float* partials,
                                   int num_sms, cudaStream_t st) {
-  const int grid = rope_grid(T, NH, D, num_sms);
   const size_t smem = static_cast<size_t>(NH) * sizeof(float);
+  // small inputs: at most two rounds of two items per warp on one CTA per SM
+  const int gh = (32 / (D / 8)) * kCoopBatch;
+  const long long items = static_cast<long long>(T) * ((NH + gh - 1) / gh);
+  const long long per_cta = 2 * (kCoopThreads / 32);
+  if (items <= 2 * per_cta * num_sms && num_sms <= kRopeMaxCtas) {
+    const int g = static_cast<int>(
+        std::min<long long>(num_sms, std::max<long long>(1, (items + per_cta - 1) / per_cta)));
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(g);
+    cfg.blockDim = dim3(kCoopThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;  // the CTAs synchronise once
+    attr[0].val.cooperative = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return checked(cudaLaunchKernelEx(&cfg, rope_coop_kernel, x, pos, cos_t, sin_t, T, NH, D,
+                                      max_pos, partials, scales, codes, ctrl),
+                   "cooperative kernel launch");
+  }
+  const int grid = rope_grid(T, NH, D, num_sms);
   cudaError_t e = launch_pdl(rope_pass_kernel<false>, dim3(grid), dim3(kRopeThreads), smem, st, x,
                              pos, cos_t, sin_t, T, NH, D, max_pos, partials,
                              static_cast<const float*>(nullptr), static_cast<uint8_t*>(nullptr));
