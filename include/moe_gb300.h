@@ -189,7 +189,12 @@ typedef struct {
  * They go to uint64 [2][MOE_TRACE_MAX_CTAS][4] at byte offset
  * moe_fused_trace_offset() of the workspace (gate/up kernel first); rows of
  * CTAs that are not launched keep their previous contents (zero the region
- * first to tell them apart). */
+ * first to tell them apart).  On SM pairs (wide FP8 gate/up tiles) the third
+ * stamp of the second CTA of a pair is its first accumulator ready (that
+ * CTA's stages complete on the first CTA's barriers).  With
+ * MOE_FLAG_ONE_KERNEL the single kernel records [0][cta] = entry, token rows
+ * ready, first gate/up stage, gate/up epilogue done and [1][cta] = h written
+ * everywhere, h codes ready, first down stage, exit. */
 #define MOE_DEBUG_TRACE 0x2
 /* Operand placement (section "Swap-AB for WGMMA utilization").  By default
  * the gate/up GEMM puts the expert's weight rows in the MMA's M slot (the

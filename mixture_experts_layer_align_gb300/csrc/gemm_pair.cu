@@ -85,6 +85,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
   const int lane = threadIdx.x & 31;
   const uint32_t rank = cluster_ctarank();
   const bool leader = rank == 0;
+  // per-CTA stamps (MOE_DEBUG_TRACE): entry, inputs ready, first stage landed
+  // (the leader's MMA warp; the other CTA of the pair: its first accumulator
+  // ready), exit
+  unsigned long long* trace =
+      (p.trace != nullptr && blockIdx.x < MOE_TRACE_MAX_CTAS) ? p.trace + blockIdx.x * 4 : nullptr;
+  if (trace && threadIdx.x == 0) trace[0] = global_timer_ns();
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
@@ -121,6 +127,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
     pdl_wait();
     pdl_trigger();
   }
+  if (trace && threadIdx.x == 64) trace[1] = global_timer_ns();
 
   const int K = p.k_steps;
   const int units = p.ctrl->num_mtiles_w * p.nb_count;
@@ -204,6 +211,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
             ok = false;
             break;
           }
+          if (trace && it == 0) trace[2] = global_timer_ns();
           tc_fence_after_sync();
           const uint32_t sa = smem_addr(smem + static_cast<size_t>(s) * kPairStageBytes);
           const uint64_t da0 = sdesc_kmajor_sw128(sa);
@@ -240,6 +248,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
       const PairTile t = pair_tile(p, u, rank);
       int got = 0;
       if (lane == 0) got = mbar_wait(tfull, tt & 1u, abort_flag, limit) ? 1 : 0;
+      if (trace && !leader && tt == 0 && threadIdx.x == 64) trace[2] = global_timer_ns();
       got = __shfl_sync(0xffffffffu, got, 0);
       if (!named_barrier_and(kPairEpiBarrier, kPairEpiThreads, got != 0)) {
         if (lane == 0) {
@@ -289,6 +298,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
   if (warp == 1) {
     tc_fence_after_sync();
     tmem_dealloc_pair(tmem, kPairTmemCols);
+  }
+  if (trace && threadIdx.x == 0) {
+    __threadfence();
+    trace[3] = global_timer_ns();
   }
 }
 

@@ -259,12 +259,14 @@ def test_fused_prefill_8192(gpu_lib, name):
     run_case(gpu_lib, w, a, c["top_k"], True, rows=None)
 
 
-def test_fused_timed_and_traced_call(gpu_lib):
+# (64, 256, 2176, 8, 2): single-SM kernels; (1024, 256, 512, 2, 2): 1024 rows
+# per expert, so the gate/up GEMM runs 256-token tiles on SM pairs.
+@pytest.mark.parametrize("T,H,I,E,k", [(64, 256, 2176, 8, 2), (1024, 256, 512, 2, 2)])
+def test_fused_timed_and_traced_call(gpu_lib, T, H, I, E, k):
     """moe_fused_forward_timed: eight events bracket the steps in order and the
     output agrees with the untimed call's; MOE_DEBUG_TRACE: every CTA of the two
     expert GEMMs that ran leaves stamps with entry and "inputs ready" before
     "first stage landed" and exit."""
-    T, H, I, E, k = 64, 256, 2176, 8, 2
     w = inputs.make_weights(H, I, E, "fp8", seed=9, device="cuda")
     a = inputs.make_activations(T, H, E, "uniform", seed=9, device="cuda")
     ws = gpu_lib.alloc_workspace(T, H, I, E, k, gpu_lib.MOE_DT_FP8_E4M3)
