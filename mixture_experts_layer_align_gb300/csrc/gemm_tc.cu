@@ -32,8 +32,9 @@
 //                         running amax|h|) or bf16 (bf16 path)
 //               down:     y * s * topk_weight added into the fp32 combine
 //                         buffer with bulk asynchronous reductions staged in
-//                         shared memory, or written as bf16 rows per pair
-//                         (expert aggregation fused into the GEMM).
+//                         shared memory, or written as bf16 rows at the
+//                         pairs' aligned rows (tokens in M: staged in shared
+//                         memory and written with TMA tensor stores).
 // The accumulator is double-buffered in TMEM when it fits, so the epilogue of
 // one segment overlaps the MMAs of the next.  Every wait is bounded; on
 // timeout the CTA records kDevErrTimeout and leaves.
@@ -97,13 +98,16 @@ __device__ __forceinline__ float* part_slot(const GemmParams& p, int c, long lon
 // the 128-row token tile is the A operand in the M slot and the weight block
 // is B with N = 128 weight rows; lanes then hold tokens and TMEM columns hold
 // weight rows.  kPair (down projection, unswapped): a tile covers two
-// consecutive 128-row weight blocks against one token tile, two MMAs into two
-// accumulators like gate and up, so the token bytes serve twice the FLOPs.
+// consecutive 128-row weight blocks against one token tile, one N = 256 MMA
+// per K slice (the two blocks are contiguous in the stage, the two
+// accumulators in TMEM), so the token bytes serve twice the FLOPs and the
+// token operand is read from shared memory once per 256 columns.
 template <bool kBF16, bool kSwiGLU, bool kTokM, bool kPair>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     moe_gemm_kernel(const __grid_constant__ GemmParams p, const __grid_constant__ CUtensorMap tm_a,
                     const __grid_constant__ CUtensorMap tm_b,
-                    const __grid_constant__ CUtensorMap tm_b64) {
+                    const __grid_constant__ CUtensorMap tm_b64,
+                    const __grid_constant__ CUtensorMap tm_o) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -126,9 +130,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(never + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   volatile int* s_last = abort_flag + 1;  // "this CTA finishes the split tile" flag
-  // down projection: per epilogue warp, two 16-column x 32-row fp32 staging
-  // buffers for the bulk reductions into the combine buffer
-  float* stage_out = reinterpret_cast<float*>(smem + static_cast<size_t>(S) * stage_bytes + 256);
+  // down projection: 4 KB of staging per epilogue warp (1024-byte aligned,
+  // after the barriers): two 16-column x 32-row fp32 buffers for the bulk
+  // reductions into the combine buffer, or 32 bf16 rows of 128 bytes in the
+  // 128-byte swizzle for the TMA stores of rows per pair
+  uint8_t* stage_epi = smem + static_cast<size_t>(S) * stage_bytes + 1024;
+  float* stage_out = reinterpret_cast<float*>(stage_epi);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -153,6 +160,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     prefetch_tensormap(&tm_a);
     prefetch_tensormap(&tm_b);
     prefetch_tensormap(&tm_b64);
+    if (kTokM && !kSwiGLU && p.pair_out != nullptr) prefetch_tensormap(&tm_o);
   }
   if (warp == 1) {
     tmem_alloc(tmem_slot, static_cast<uint32_t>(p.tmem_cols));
@@ -299,7 +307,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           break;
         }
         tc_fence_after_sync();
-        const uint32_t idesc = umma_idesc(kBF16, 128, n_cur);
+        // tokens in M with two weight blocks: one N = 256 MMA over both blocks
+        // (contiguous in the stage) into both accumulators (contiguous in TMEM)
+        constexpr bool kWideN = kTokM && kPair;
+        const uint32_t idesc = umma_idesc(kBF16, 128, kWideN ? 256 : n_cur);
         const uint32_t d0 = tmem + a * static_cast<uint32_t>(p.acc_stride);
         const uint32_t d1 = d0 + static_cast<uint32_t>(p.bn_max);
         for (int kk = k0; kk < k1; ++kk, ++it) {
@@ -324,10 +335,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             const uint64_t a1 = kTokM ? db : da1, b1 = kTokM ? da1 : db;
             if (kBF16) {
               umma_bf16(d0, a0 + 2 * k4, b0 + 2 * k4, idesc, acc);
-              if (kTwoB) umma_bf16(d1, a1 + 2 * k4, b1 + 2 * k4, idesc, acc);
+              if (kTwoB && !kWideN) umma_bf16(d1, a1 + 2 * k4, b1 + 2 * k4, idesc, acc);
             } else {
               umma_f8(d0, a0 + 2 * k4, b0 + 2 * k4, idesc, acc);
-              if (kTwoB) umma_f8(d1, a1 + 2 * k4, b1 + 2 * k4, idesc, acc);
+              if (kTwoB && !kWideN) umma_f8(d1, a1 + 2 * k4, b1 + 2 * k4, idesc, acc);
             }
           }
           umma_commit(empty + s);
@@ -501,45 +512,64 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             }
           }
         }
+      } else if (p.pair_out != nullptr && kTokM) {
+        // large batches, tokens in M: y * s * topk_weight as bf16 at the
+        // tile's aligned rows (tiles are whole here, see the range split; the
+        // token sum comes after).  Per weight block this warp takes 64
+        // columns of its 32 rows, stages them as 128-byte rows in the
+        // 128-byte swizzle (16-byte chunk c of row r at chunk c ^ (r & 7), no
+        // bank conflicts) and stores them with one TMA box per 16 rows.  Row
+        // tiles are multiples of 16 rows: a box is inside the tile or not
+        // stored (its rows belong to the next tile).  Padding rows carry
+        // router weight 0.
+        uint8_t* wst = stage_epi + static_cast<size_t>(warp - 2) * 4096;
+        const float w_r = sc * cw[0];
+        const int c_lo = 64 * half;
+        const int r0 = q * 32;
+        for (int b2i = 0; b2i < (kPair ? 2 : 1); ++b2i) {
+          float y[4][16];
+          const uint32_t tb = tbase + static_cast<uint32_t>(b2i * p.bn_max + c_lo);
+          tmem_ld16x2(tb, tb + 16, y[0], y[1]);
+          tmem_ld16x2(tb + 32, tb + 48, y[2], y[3]);
+          if (lane == 0) bulk_wait_read<0>();  // the previous box has left the buffer
+          __syncwarp();
+#pragma unroll
+          for (int c = 0; c < 8; ++c) {
+            const float* yy = &y[c >> 1][(c & 1) * 8];
+            uint4 o;
+            uint32_t* ow = reinterpret_cast<uint32_t*>(&o);
+#pragma unroll
+            for (int j2 = 0; j2 < 4; ++j2) {
+              __nv_bfloat162 b2 = __floats2bfloat162_rn(yy[2 * j2] * w_r, yy[2 * j2 + 1] * w_r);
+              ow[j2] = *reinterpret_cast<uint32_t*>(&b2);
+            }
+            *reinterpret_cast<uint4*>(wst + lane * 128 + ((c ^ (lane & 7)) << 4)) = o;
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            const int col0 = t.nb * p.wblock_rows + b2i * 128 + c_lo;
+            if (r0 < t.n) tma_store_2d(&tm_o, wst, col0, t.row0 + r0);
+            if (r0 + 16 < t.n) tma_store_2d(&tm_o, wst + 2048, col0, t.row0 + r0 + 16);
+            bulk_commit();
+          }
+        }
       } else if (p.pair_out != nullptr) {
-        // large batches: y * s * topk_weight as bf16 at the pair's row (tiles
-        // are whole here, see the range split); the token sum comes after
+        // large batches, weights in M: y * s * topk_weight as bf16 at the
+        // pair's aligned row (the tile's column), 32 consecutive output
+        // columns per store instruction
         for (int c0 = c_begin; c0 < ncols; c0 += 32) {
           float y[16];
           tmem_ld16(tbase + c0, y);
-          if (kTokM) {
-            // 16 consecutive output columns of this thread's pair (and, for a
-            // pair of weight blocks, the same 16 of the second block)
-            float y1[16];
-            if (kPair) tmem_ld16(tbase + p.bn_max + c0, y1);
-            if (row_ok && cpid[0] < p.P) {
-              const float w_r = sc * cw[0];
+          const int pid_c = pickn<kMetaN>(cpid, c0 >> 5);
+          const float w_c = sc * pickn<kMetaN>(cw, c0 >> 5);
 #pragma unroll
-              for (int b2i = 0; b2i < (kPair ? 2 : 1); ++b2i) {
-                const float* yy = b2i == 0 ? y : y1;
-                uint4 o[2];
-                uint32_t* ow = reinterpret_cast<uint32_t*>(o);
-#pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                  __nv_bfloat162 b2 = __floats2bfloat162_rn(yy[2 * j] * w_r, yy[2 * j + 1] * w_r);
-                  ow[j] = *reinterpret_cast<uint32_t*>(&b2);
-                }
-                uint4* dst = reinterpret_cast<uint4*>(p.pair_out + static_cast<size_t>(cpid[0]) * p.ldo +
-                                                      t.nb * p.wblock_rows + b2i * 128 + c0);
-                dst[0] = o[0];
-                dst[1] = o[1];
-              }
-            }
-          } else {
-            const int pid_c = pickn<kMetaN>(cpid, c0 >> 5);
-            const float w_c = sc * pickn<kMetaN>(cw, c0 >> 5);
-#pragma unroll
-            for (int j = 0; j < 16; ++j) {
-              const int pj = __shfl_sync(0xffffffffu, pid_c, (c0 & 31) + j);
-              const float wj = __shfl_sync(0xffffffffu, w_c, (c0 & 31) + j);
-              if (pj < p.P)
-                p.pair_out[static_cast<size_t>(pj) * p.ldo + col] = __float2bfloat16_rn(y[j] * wj);
-            }
+          for (int j = 0; j < 16; ++j) {
+            const int pj = __shfl_sync(0xffffffffu, pid_c, (c0 & 31) + j);
+            const float wj = __shfl_sync(0xffffffffu, w_c, (c0 & 31) + j);
+            if (pj < p.P)
+              p.pair_out[static_cast<size_t>(t.row0 + c0 + j) * p.ldo + col] =
+                  __float2bfloat16_rn(y[j] * wj);
           }
         }
       } else if (kTokM) {
@@ -631,7 +661,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 
 template <bool kBF16, bool kSwiGLU, bool kTokM, bool kPair = false>
 cudaError_t launch_one(const GemmParams& p, const CUtensorMap& ta, const CUtensorMap& tb,
-                       const CUtensorMap& tb64, int grid, cudaStream_t st) {
+                       const CUtensorMap& tb64, const CUtensorMap& to, int grid, cudaStream_t st) {
   static thread_local int configured_device = -1;
   int dev = 0;
   cudaGetDevice(&dev);
@@ -643,37 +673,40 @@ cudaError_t launch_one(const GemmParams& p, const CUtensorMap& ta, const CUtenso
   }
   const size_t smem = kSmemLimit;
   return launch_pdl(moe_gemm_kernel<kBF16, kSwiGLU, kTokM, kPair>, dim3(grid), dim3(kGemmThreads), smem, st, p,
-                    ta, tb, tb64);
+                    ta, tb, tb64, to);
 }
 
 }  // namespace
 
-// Combine staging of the down projection: per epilogue warp 2 buffers x 16 x 32 fp32.
-constexpr size_t kCombineStaging = kGemmEpiWarps * 2 * 16 * 32 * sizeof(float);
+// Epilogue staging of the down projection: 4 KB per epilogue warp, 1024 bytes
+// after the stages (barriers first); up to 1023 bytes go to aligning the base.
+constexpr size_t kCombineStaging = kGemmEpiWarps * 4096;
+static_assert(kCombineStaging == kGemmEpiWarps * 2 * 16 * 32 * sizeof(float),
+              "fp32 reduction staging: two 16 x 32 buffers per warp");
 
 size_t gemm_stage_smem(bool swiglu) {
-  return kSmemLimit - kSmemSlack - (swiglu ? 0 : kCombineStaging);
+  return swiglu ? kSmemLimit - kSmemSlack : kSmemLimit - 2048 - kCombineStaging;
 }
 
 cudaError_t launch_gemm(bool bf16, bool swiglu, bool tok_m, bool pair, const GemmParams& p,
                         const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tb64,
-                        int grid, cudaStream_t st) {
+                        const CUtensorMap& to, int grid, cudaStream_t st) {
   if (pair && tok_m && !swiglu)
-    return bf16 ? launch_one<true, false, true, true>(p, ta, tb, tb64, grid, st)
-                : launch_one<false, false, true, true>(p, ta, tb, tb64, grid, st);
+    return bf16 ? launch_one<true, false, true, true>(p, ta, tb, tb64, to, grid, st)
+                : launch_one<false, false, true, true>(p, ta, tb, tb64, to, grid, st);
   if (pair) return cudaErrorInvalidValue;  // pairs exist for the unswapped down GEMM only
   if (tok_m) {
     if (bf16)
-      return swiglu ? launch_one<true, true, true>(p, ta, tb, tb64, grid, st)
-                    : launch_one<true, false, true>(p, ta, tb, tb64, grid, st);
-    return swiglu ? launch_one<false, true, true>(p, ta, tb, tb64, grid, st)
-                  : launch_one<false, false, true>(p, ta, tb, tb64, grid, st);
+      return swiglu ? launch_one<true, true, true>(p, ta, tb, tb64, to, grid, st)
+                    : launch_one<true, false, true>(p, ta, tb, tb64, to, grid, st);
+    return swiglu ? launch_one<false, true, true>(p, ta, tb, tb64, to, grid, st)
+                  : launch_one<false, false, true>(p, ta, tb, tb64, to, grid, st);
   }
   if (bf16)
-    return swiglu ? launch_one<true, true, false>(p, ta, tb, tb64, grid, st)
-                  : launch_one<true, false, false>(p, ta, tb, tb64, grid, st);
-  return swiglu ? launch_one<false, true, false>(p, ta, tb, tb64, grid, st)
-                : launch_one<false, false, false>(p, ta, tb, tb64, grid, st);
+    return swiglu ? launch_one<true, true, false>(p, ta, tb, tb64, to, grid, st)
+                  : launch_one<true, false, false>(p, ta, tb, tb64, to, grid, st);
+  return swiglu ? launch_one<false, true, false>(p, ta, tb, tb64, to, grid, st)
+                : launch_one<false, false, false>(p, ta, tb, tb64, to, grid, st);
 }
 
 }  // namespace moe

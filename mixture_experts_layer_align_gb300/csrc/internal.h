@@ -193,9 +193,10 @@ struct GemmParams {
   int ldh;
   float* acc_out;        // down, combine by reduction: [T, H] fp32
   int ldo;
-  // down, combine by rows (large batches): y * s * topk_weight as bf16 at row
-  // `pair` of [T*k, H]; a separate kernel sums each token's k rows.  Null
-  // selects the bulk reductions into acc_out.
+  // down, combine by rows (large batches): y * s * topk_weight as bf16 at the
+  // pair's aligned row of [rows, H] (the tile's own rows; tokens in M: TMA
+  // stores through the tensor map passed to the kernel); a separate kernel
+  // sums each token's k rows.  Null selects the bulk reductions into acc_out.
   __nv_bfloat16* pair_out;
   // gate/up tiles split across CTAs: per-tile arrival counters (zeroed by the
   // router kernel) and two partial-accumulator slots per CTA
@@ -207,10 +208,16 @@ struct GemmParams {
   unsigned long long* trace;  // [MOE_TRACE_MAX_CTAS][4] stamps or null
 };
 
-// Sum of the k weighted expert rows of every token: out[t] = sum_j rows[t*k+j]
-// (fp32 accumulation, bf16 result).
-cudaError_t launch_combine_rows(const __nv_bfloat16* rows, int T, int k, int H,
-                                __nv_bfloat16* out, int num_sms, cudaStream_t st);
+// Sum of the k weighted expert rows of every token: out[t] = sum_j
+// rows[inv_slot[t*k+j]] (aligned row of each pair; fp32 accumulation in slot
+// order, bf16 result).
+cudaError_t launch_combine_rows(const __nv_bfloat16* rows, const int32_t* inv_slot, int T, int k,
+                                int H, __nv_bfloat16* out, int num_sms, cudaStream_t st);
+
+// The down projection combines through bf16 rows per pair (and a separate
+// sum) instead of fp32 reductions into [T, H] when P x H exceeds this.
+constexpr long long kCombineRowsElems = 8ll << 20;
+inline bool combine_by_rows(long long P, long long H) { return P * H > kCombineRowsElems; }
 
 // Widest row tile of any GEMM (wide gate/up tiles).
 constexpr int kWideRows = 256;
@@ -228,9 +235,12 @@ size_t gemm_stage_smem(bool swiglu);
 // tmb / tmb64: the token operand with 16-row and 64-row boxes.  tok_m: tokens
 // in the MMA M slot (the unswapped placement; row tiles of up to 128 rows).
 // pair: the unswapped down GEMM with two weight blocks per tile (H % 256 == 0).
+// tmo: bf16 rows per pair [rows, H] with 64-column x 16-row boxes (128-byte
+// swizzle), the target of the down GEMM's stores with tokens in M and
+// p.pair_out set; any valid map otherwise (unused).
 cudaError_t launch_gemm(bool bf16, bool swiglu, bool tok_m, bool pair, const GemmParams& p,
                         const CUtensorMap& tma, const CUtensorMap& tmb, const CUtensorMap& tmb64,
-                        int grid, cudaStream_t st);
+                        const CUtensorMap& tmo, int grid, cudaStream_t st);
 // Gate/up GEMM of wide row tiles (256 tokens) on SM pairs (cluster of two,
 // tcgen05 cta_group::2): E4M3, weights in M, I % 256 == 0, whole tiles;
 // p.mtiles is the wide tile list and p.nb_count = I / 256.  At most

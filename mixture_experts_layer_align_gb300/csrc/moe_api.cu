@@ -107,12 +107,14 @@ struct Layout {
   int ctas = 0;
   int n_tile_cnt = 0;
   // Combine of the down projection: bulk reductions into an fp32 [T, H]
-  // buffer (small batches), or weighted bf16 rows per pair summed by a
-  // separate kernel (large batches, where the reductions would saturate L2).
+  // buffer (small batches), or weighted bf16 rows at the pairs' aligned rows
+  // summed by a separate kernel through inv_slot (large batches, where the
+  // reductions would saturate L2).
   bool combine_rows = false;
   size_t rows = 0;
   // Large batches: two-pass alignment (per-chunk histograms); FP8: x quantised
-  // once per token and scattered to its aligned rows (inv_slot: row of each pair).
+  // once per token and scattered to its aligned rows (inv_slot: row of each
+  // pair, also read by the row combine).
   bool large = false;
   size_t chunk_hist = 0, inv_slot = 0;
   size_t ctrl = 0, trace = 0, partials = 0, ids = 0, wts = 0, counts = 0, offsets = 0,
@@ -156,10 +158,10 @@ Layout make_layout(int T, int H, int I, int E, int k, bool fp8) {
   L.hq = take(fp8 ? static_cast<size_t>(L.pad_max) * I : 0);
   L.large = L.P > kLargePairs;
   L.chunk_hist = take(L.large ? sizeof(int32_t) * E * ((L.P + align_chunk() - 1) / align_chunk()) : 0);
-  L.inv_slot = take(L.large && fp8 ? sizeof(int32_t) * L.P : 0);
-  L.combine_rows = L.P * H > (8ll << 20);
+  L.combine_rows = combine_by_rows(L.P, H);
+  L.inv_slot = take((L.large && fp8) || L.combine_rows ? sizeof(int32_t) * L.P : 0);
   L.acc = take(L.combine_rows ? 0 : static_cast<size_t>(T) * H * sizeof(float));
-  L.rows = take(L.combine_rows ? static_cast<size_t>(L.P) * H * 2 : 0);
+  L.rows = take(L.combine_rows ? static_cast<size_t>(L.pad_max) * H * 2 : 0);
   L.total = off;
   return L;
 }
@@ -340,11 +342,12 @@ bool fused_small(int T, int H, int I, int E, int k, int flags, const Layout& L, 
   return fused_small_supported(device);
 }
 
-// Small batches take the single-CTA router + alignment kernel.
+// Small batches take the single-CTA router + alignment kernel (which writes
+// no inverse slot map, so not where the down projection combines by rows).
 bool small_front(int T, int H, int E, int k) {
   const long long P = static_cast<long long>(T) * k;
   return T <= kSmallMaxTokens && P <= kSmallMaxPairs && E <= kSmallMaxExperts &&
-         static_cast<long long>(T) * H <= kSmallMaxXElems;
+         static_cast<long long>(T) * H <= kSmallMaxXElems && !combine_by_rows(P, H);
 }
 
 // The launch sequence.  When `events` is non-null, events[i] is recorded on
@@ -523,7 +526,7 @@ moe_status_t fused_forward_impl(const moe_fused_args* a, void* workspace, size_t
   ap.sorted_ids = sorted;
   ap.wts = wts;
   ap.sorted_w = sorted_w;
-  ap.inv_slot = (L.large && fp8) ? inv_slot : nullptr;
+  ap.inv_slot = ((L.large && fp8) || L.combine_rows) ? inv_slot : nullptr;
   ap.tile_expert = nullptr;
   ap.num_padded = nullptr;
   ap.mtiles = mtiles;
@@ -559,7 +562,7 @@ moe_status_t fused_forward_impl(const moe_fused_args* a, void* workspace, size_t
   }
 
   // TMA descriptors
-  CUtensorMap tm_w13, tm_xs, tm_xs64, tm_w2, tm_h, tm_h64;
+  CUtensorMap tm_w13, tm_xs, tm_xs64, tm_w2, tm_h, tm_h64, tm_rows;
   const bool bf16 = !fp8;
   const void* hb = fp8 ? static_cast<const void*>(hq) : static_cast<const void*>(h);
   if (!make_tmap(&tm_w13, a->w13, bf16, H, static_cast<uint64_t>(E) * 2 * I, 128) ||
@@ -569,6 +572,10 @@ moe_status_t fused_forward_impl(const moe_fused_args* a, void* workspace, size_t
       !make_tmap(&tm_h, hb, bf16, I, L.pad_max, 16) ||
       !make_tmap(&tm_h64, hb, bf16, I, L.pad_max, 64))
     return MOE_ERR_CUDA;
+  // bf16 rows per pair (the down GEMM's TMA stores); else a stand-in
+  if (L.combine_rows ? !make_tmap(&tm_rows, pair_rows, true, H, L.pad_max, 16) : false)
+    return MOE_ERR_CUDA;
+  if (!L.combine_rows) tm_rows = tm_h;
 
   const int k_elems = fp8 ? 128 : 64;
   const long long max_tiles = std::min<long long>(L.max_mtiles, (L.pad_max + bn_max - 1) / bn_max + touched);
@@ -624,8 +631,8 @@ moe_status_t fused_forward_impl(const moe_fused_args* a, void* workspace, size_t
         static_cast<int>(std::max<long long>(1, std::min<long long>(ctas / 2, units)));
     if (launch_gemm_pair(gp, tm_w13, tm_xs, tm_xs64, max_clusters, s) != cudaSuccess)
       return MOE_ERR_CUDA;
-  } else if (launch_gemm(bf16, true, tok_m1, false, g1, tm_w13, tm_xs, tm_xs64, grid1, s) !=
-             cudaSuccess) {
+  } else if (launch_gemm(bf16, true, tok_m1, false, g1, tm_w13, tm_xs, tm_xs64, tm_rows, grid1,
+                         s) != cudaSuccess) {
     return MOE_ERR_CUDA;
   }
 
@@ -666,14 +673,15 @@ moe_status_t fused_forward_impl(const moe_fused_args* a, void* workspace, size_t
   g2.trace = (a->debug_flags & MOE_DEBUG_TRACE) ? trace + MOE_TRACE_MAX_CTAS * 4 : nullptr;
   const long long work2 = max_tiles * g2.nb_count * g2.k_steps;
   const int grid2 = static_cast<int>(std::max<long long>(1, std::min<long long>(ctas, work2)));
-  if (launch_gemm(bf16, false, tok_m2, pair2, g2, tm_w2, tm_h, tm_h64, grid2, s) != cudaSuccess)
+  if (launch_gemm(bf16, false, tok_m2, pair2, g2, tm_w2, tm_h, tm_h64, tm_rows, grid2, s) !=
+      cudaSuccess)
     return MOE_ERR_CUDA;
 
   // 7. fp32 combine buffer -> bf16 output, or the sum of each token's k rows
   if (events && cudaEventRecord(events[6], stream) != cudaSuccess) return MOE_ERR_CUDA;
   if (L.combine_rows) {
-    if (launch_combine_rows(pair_rows, T, k, H, static_cast<__nv_bfloat16*>(a->out), dev.num_sms,
-                            s) != cudaSuccess)
+    if (launch_combine_rows(pair_rows, inv_slot, T, k, H, static_cast<__nv_bfloat16*>(a->out),
+                            dev.num_sms, s) != cudaSuccess)
       return MOE_ERR_CUDA;
   } else if (launch_finalize(acc, static_cast<__nv_bfloat16*>(a->out),
                              static_cast<long long>(T) * H, dev.num_sms, s) != cudaSuccess) {

@@ -455,6 +455,16 @@ __device__ __forceinline__ void red_add_v4_f32(float* dst, float a, float b, flo
                : "memory");
 }
 
+// TMA tensor store of one box from shared memory at coordinates (c0, c1),
+// tracked in the issuing thread's bulk group.
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* tm, const void* src, int32_t c0,
+                                             int32_t c1) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+                   reinterpret_cast<uint64_t>(tm)),
+               "r"(smem_addr(src)), "r"(c0), "r"(c1)
+               : "memory");
+}
+
 __device__ __forceinline__ void bulk_commit() {
   asm volatile("cp.async.bulk.commit_group;" ::: "memory");
 }

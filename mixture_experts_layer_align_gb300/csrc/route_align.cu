@@ -599,14 +599,34 @@ __global__ void __launch_bounds__(256)
   const long long n16 = static_cast<long long>(ctrl->num_padded) * I / 16;
   const float4* src = reinterpret_cast<const float4*>(h);
   uint4* dst = reinterpret_cast<uint4*>(hq);
-  for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < n16;
-       i += static_cast<long long>(gridDim.x) * blockDim.x) {
+  // Last rows first: the gate/up GEMM writes h in row order (experts in
+  // turn), so its last rows are the ones still in L2.  Two groups of 16
+  // values per thread in flight.
+  const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
+  for (long long j = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; j < n16;
+       j += 2 * stride) {
+    const long long i0 = n16 - 1 - j;
+    const long long i1 = i0 - stride;
+    float4 a[4], b[4];
+#pragma unroll
+    for (int c = 0; c < 4; ++c) a[c] = src[4 * i0 + c];
+    if (i1 >= 0) {
+#pragma unroll
+      for (int c = 0; c < 4; ++c) b[c] = src[4 * i1 + c];
+    }
     uint4 r;
-    r.x = quant4(src[4 * i + 0], s, rs);
-    r.y = quant4(src[4 * i + 1], s, rs);
-    r.z = quant4(src[4 * i + 2], s, rs);
-    r.w = quant4(src[4 * i + 3], s, rs);
-    dst[i] = r;
+    r.x = quant4(a[0], s, rs);
+    r.y = quant4(a[1], s, rs);
+    r.z = quant4(a[2], s, rs);
+    r.w = quant4(a[3], s, rs);
+    dst[i0] = r;
+    if (i1 >= 0) {
+      r.x = quant4(b[0], s, rs);
+      r.y = quant4(b[1], s, rs);
+      r.z = quant4(b[2], s, rs);
+      r.w = quant4(b[3], s, rs);
+      dst[i1] = r;
+    }
   }
 }
 
@@ -634,10 +654,12 @@ __global__ void __launch_bounds__(256)
 }
 
 // ------------------------------------------------------------------ combine rows
-// out[t] = sum over the k slots of the weighted expert rows of token t, fp32
-// accumulation in slot order, one bf16 rounding.  8 columns per thread.
+// out[t] = sum over the k slots of the weighted expert rows of token t (row
+// inv_slot[t*k+j] of the aligned order), fp32 accumulation in slot order, one
+// bf16 rounding.  8 columns per thread.
 __global__ void __launch_bounds__(256)
-    combine_rows_kernel(const __nv_bfloat16* __restrict__ rows, int T, int k, int H,
+    combine_rows_kernel(const __nv_bfloat16* __restrict__ rows,
+                        const int32_t* __restrict__ inv_slot, int T, int k, int H,
                         __nv_bfloat16* __restrict__ out) {
   pdl_wait();
   pdl_trigger();
@@ -651,7 +673,7 @@ __global__ void __launch_bounds__(256)
     const long long c = i - t * per_row;
     float a[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
     for (int j = 0; j < k; ++j) {
-      const uint4 v = __ldg(src + (t * k + j) * per_row + c);
+      const uint4 v = __ldg(src + static_cast<long long>(__ldg(inv_slot + t * k + j)) * per_row + c);
       a[0] += bf16_lo(v.x);
       a[1] += bf16_hi(v.x);
       a[2] += bf16_lo(v.y);
@@ -817,10 +839,11 @@ cudaError_t launch_finalize(const float* acc, __nv_bfloat16* out, long long n, i
   return launch_pdl(finalize_kernel, dim3(grid), dim3(256), 0, st, acc, out, n / 8);
 }
 
-cudaError_t launch_combine_rows(const __nv_bfloat16* rows, int T, int k, int H,
-                                __nv_bfloat16* out, int num_sms, cudaStream_t st) {
+cudaError_t launch_combine_rows(const __nv_bfloat16* rows, const int32_t* inv_slot, int T, int k,
+                                int H, __nv_bfloat16* out, int num_sms, cudaStream_t st) {
   const int grid = capped_grid(static_cast<long long>(T) * H / 8, 256, num_sms, 8);
-  return launch_pdl(combine_rows_kernel, dim3(grid), dim3(256), 0, st, rows, T, k, H, out);
+  return launch_pdl(combine_rows_kernel, dim3(grid), dim3(256), 0, st, rows, inv_slot, T, k, H,
+                    out);
 }
 
 cudaError_t launch_quantize_e4m3(const __nv_bfloat16* x, long long n, uint8_t* xq, float* scale,
