@@ -657,7 +657,7 @@ __global__ void __launch_bounds__(256)
 // out[t] = sum over the k slots of the weighted expert rows of token t (row
 // inv_slot[t*k+j] of the aligned order), fp32 accumulation in slot order, one
 // bf16 rounding.  8 columns per thread.
-__global__ void __launch_bounds__(256)
+__global__ void __launch_bounds__(256, 4)
     combine_rows_kernel(const __nv_bfloat16* __restrict__ rows,
                         const int32_t* __restrict__ inv_slot, int T, int k, int H,
                         __nv_bfloat16* __restrict__ out) {
@@ -672,16 +672,26 @@ __global__ void __launch_bounds__(256)
     const long long t = i / per_row;
     const long long c = i - t * per_row;
     float a[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-    for (int j = 0; j < k; ++j) {
-      const uint4 v = __ldg(src + static_cast<long long>(__ldg(inv_slot + t * k + j)) * per_row + c);
-      a[0] += bf16_lo(v.x);
-      a[1] += bf16_hi(v.x);
-      a[2] += bf16_lo(v.y);
-      a[3] += bf16_hi(v.y);
-      a[4] += bf16_lo(v.z);
-      a[5] += bf16_hi(v.z);
-      a[6] += bf16_lo(v.w);
-      a[7] += bf16_hi(v.w);
+    const int32_t* sl = inv_slot + t * k;
+    for (int j0 = 0; j0 < k; j0 += 8) {
+      // up to 8 rows in flight, summed in slot order
+      uint4 v[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u)
+        if (j0 + u < k) v[u] = __ldg(src + static_cast<long long>(__ldg(sl + j0 + u)) * per_row + c);
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        if (j0 + u < k) {
+          a[0] += bf16_lo(v[u].x);
+          a[1] += bf16_hi(v[u].x);
+          a[2] += bf16_lo(v[u].y);
+          a[3] += bf16_hi(v[u].y);
+          a[4] += bf16_lo(v[u].z);
+          a[5] += bf16_hi(v[u].z);
+          a[6] += bf16_lo(v[u].w);
+          a[7] += bf16_hi(v[u].w);
+        }
+      }
     }
     __nv_bfloat162 b0 = __floats2bfloat162_rn(a[0], a[1]);
     __nv_bfloat162 b1 = __floats2bfloat162_rn(a[2], a[3]);
@@ -841,7 +851,7 @@ cudaError_t launch_finalize(const float* acc, __nv_bfloat16* out, long long n, i
 
 cudaError_t launch_combine_rows(const __nv_bfloat16* rows, const int32_t* inv_slot, int T, int k,
                                 int H, __nv_bfloat16* out, int num_sms, cudaStream_t st) {
-  const int grid = capped_grid(static_cast<long long>(T) * H / 8, 256, num_sms, 8);
+  const int grid = capped_grid(static_cast<long long>(T) * H / 8, 256, num_sms, 4);
   return launch_pdl(combine_rows_kernel, dim3(grid), dim3(256), 0, st, rows, inv_slot, T, k, H,
                     out);
 }
