@@ -608,8 +608,13 @@ moe_status_t fused_forward_impl(const moe_fused_args* a, void* workspace, size_t
   g1.ldh = I;
   g1.tile_cnt = tile_cnt;
   g1.part = part;
-  // a weight block serves one row tile when an expert's rows fit one tile
-  g1.weights_evict_first = (P + touched - 1) / touched <= bn1 ? 1 : 0;
+  // A weight block serves one row tile when an expert's rows fit one tile:
+  // streamed once, evict-first, the whole (tile, K step) space split evenly.
+  // From half a tile per expert on average, busier experts split into two
+  // tiles whose weight blocks are better read once and reused from L2 (whole
+  // tiles round-robin, evict-last): measured at 128 rows per expert on
+  // average, gate/up 127 -> 107 us (E=128, H=2048, I=768, 2048 tokens, k=8).
+  g1.weights_evict_first = (P + touched - 1) / touched <= bn1 / 2 ? 1 : 0;
   g1.pair_out = nullptr;
   g1.timeout_ns = (a->debug_flags & MOE_DEBUG_FORCE_TIMEOUT) ? MOE_DEBUG_TIMEOUT_MS * 1000000ull
                                                              : kWaitLimitNs;
