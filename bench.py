@@ -71,7 +71,8 @@ def parse():
     ap.add_argument("--no-configs", action="store_true",
                     help="skip the per-workload sweep of every measured configuration")
     ap.add_argument("--config-calls", type=int, default=50,
-                    help="calls per T in the per-workload sweep (at least 50)")
+                    help="blocks of back-to-back calls per T in the per-workload sweep (at "
+                         "least 50)")
     ap.add_argument("--one-kernel", action="store_true",
                     help="small batches as one cooperative kernel (MOE_FLAG_ONE_KERNEL)")
     ap.add_argument("--no-sm-pairs", action="store_true",
@@ -256,20 +257,27 @@ def percentile(v, q):
     return v[min(len(v) - 1, max(0, int(round(q * (len(v) - 1)))))]
 
 
-def time_calls(call, n, warm=5):
-    """Device time of each of n back-to-back calls (CUDA events on the
-    current stream between consecutive calls, nothing inside a call), us."""
+CALL_BLOCK = 5
+
+
+def time_calls(call, n, block=CALL_BLOCK, warm=5):
+    """Device time per call, us, of each of n blocks of `block` back-to-back
+    calls: CUDA events on the current stream between blocks, none between the
+    calls of a block (an event between two calls keeps the next call's first
+    kernel from overlapping the previous call's last one, which back-to-back
+    calls otherwise do) and none inside a call."""
     import torch
     for i in range(warm):
         call(i)
     ev = [torch.cuda.Event(enable_timing=True) for _ in range(n + 1)]
     torch.cuda.synchronize()
     ev[0].record()
-    for i in range(n):
-        call(i)
-        ev[i + 1].record()
+    for b in range(n):
+        for j in range(block):
+            call(b * block + j)
+        ev[b + 1].record()
     torch.cuda.synchronize()
-    return [ev[i].elapsed_time(ev[i + 1]) * 1e3 for i in range(n)]
+    return [ev[b].elapsed_time(ev[b + 1]) * 1e3 / block for b in range(n)]
 
 
 L2_BYTES = 129 * 2 ** 20
@@ -312,8 +320,9 @@ CONFIG_NAMES = ["tiny_bf16", "decode_e8_top2", "finegrained_e128", "skewed_e256"
 
 def config_sweep(moe, inputs, dev, hbm_peak, fp8_peak, bf16_peak, n_calls, with_cpu, flags=0):
     """Every measured workload: per-T device time of a call (median, p10,
-    p90 over n_calls back-to-back calls, weights cold in L2), tokens/s, and
-    the fraction of the binding roofline (HBM bytes or tensor FLOPs)."""
+    p90 over n_calls blocks of back-to-back calls, weights cold in L2),
+    tokens/s, and the fraction of the binding roofline (HBM bytes or tensor
+    FLOPs)."""
     import torch
     out = {}
     for name in CONFIG_NAMES:
@@ -356,7 +365,7 @@ def config_sweep(moe, inputs, dev, hbm_peak, fp8_peak, bf16_peak, n_calls, with_
             nbytes, flops = layer_work(touched[T], T, H, I, E, k, fp8)
             bound, frac, hfrac, tfrac = roofline_fractions(med, nbytes, flops, hbm_peak, tc_peak)
             rows.append({"T": T, "us_median": round(med, 2), "us_p10": round(percentile(us, 0.1), 2),
-                         "us_p90": round(percentile(us, 0.9), 2), "calls": len(us),
+                         "us_p90": round(percentile(us, 0.9), 2), "calls": len(us) * CALL_BLOCK,
                          "tokens_per_s": round(T / (med * 1e-6), 1), "touched_experts": touched[T],
                          "layer_bytes": nbytes, "layer_flops": flops, "bound": bound,
                          "frac": round(frac, 4), "hbm_frac": round(hfrac, 4),
@@ -604,8 +613,8 @@ def run_ours(args, rank, local_rank, world):
 
     tokens_per_step = sum(Ts)
     value = job_tokens_per_s(world, tokens_per_step, K, elapsed_ms)
-    # per-T device time of a call without events inside it (events only
-    # between consecutive calls), median / p10 / p90 over >= 50 calls
+    # per-T device time of a call without events inside it (events between
+    # blocks of back-to-back calls), median / p10 / p90 over >= 50 blocks
     sweep = []
     for T in Ts:
         a = acts[T]
@@ -621,7 +630,7 @@ def run_ours(args, rank, local_rank, world):
         bound, frac, hfrac, tfrac = roofline_fractions(us, nbytes, flops, hbm_peak, tc_peak)
         sweep.append({
             "T": T, "us_median": round(us, 2), "us_p10": round(percentile(us_all, 0.1), 2),
-            "us_p90": round(percentile(us_all, 0.9), 2), "calls": len(us_all),
+            "us_p90": round(percentile(us_all, 0.9), 2), "calls": len(us_all) * CALL_BLOCK,
             "tokens_per_s": round(T / (us * 1e-6), 1),
             "touched_experts": stats[T]["touched"], "max_rows_per_expert": stats[T]["max_rows"],
             "layer_bytes": nbytes, "bound": bound, "frac": round(frac, 4),
@@ -735,8 +744,10 @@ def run_ours(args, rank, local_rank, world):
                               else "") + ("; small batches as one cooperative kernel"
                                           if args.one_kernel else "")},
         "sweep": sweep,
-        "sweep_timing": "per call: CUDA events between consecutive back-to-back calls "
-                        "(none inside a call), weights cold in L2",
+        "sweep_timing": f"per call: CUDA events between blocks of {CALL_BLOCK} back-to-back "
+                        "calls (none between the calls of a block, none inside a call); "
+                        "median / p10 / p90 over the blocks' per-call times; weights cold "
+                        "in L2",
         "kernel_share": {n: round(step_ms[n] / total_kernel_ms, 4) for n in STEP_NAMES},
         "kernel_timing": "CUDA events between the kernels of every call, second pass of the "
                          f"same {K} steps ({instrumented_ms / K:.3f} ms/step with events)",
@@ -749,7 +760,8 @@ def run_ours(args, rank, local_rank, world):
     if configs is not None:
         line["configs"] = configs
         line["configs_timing"] = ("every measured workload: device time per call from CUDA "
-                                  "events between back-to-back calls (median, p10, p90), "
+                                  f"events between blocks of {CALL_BLOCK} back-to-back calls "
+                                  "(median, p10, p90 over the blocks), "
                                   "weights cycled through enough copies to stay out of L2; "
                                   "frac = fraction of the binding roofline (HBM bytes of the "
                                   "touched experts + x/logits/out against measured hbm_gbs, or "
@@ -930,26 +942,51 @@ def run_rope(args, rank, local_rank):
         torch.cuda.synchronize()
         e0 = torch.cuda.Event(enable_timing=True)
         e1 = torch.cuda.Event(enable_timing=True)
+        # eager: K back-to-back calls from Python (small T: paced by the host)
         e0.record()
         for i in range(K):
             call(i)
         e1.record()
         torch.cuda.synchronize()
+        eager_us = e0.elapsed_time(e1) * 1e3 / K
+        # device time: the same K calls captured once in a CUDA graph, replayed
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):
+            call(0)
+        torch.cuda.current_stream().wait_stream(side)
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            for i in range(K):
+                call(i)
+        graph.replay()
+        torch.cuda.synchronize()
+        reps = 3
+        e0.record()
+        for _ in range(reps):
+            graph.replay()
+        e1.record()
+        torch.cuda.synchronize()
         if moe.moe_check_status(scratch) != 0:
             raise RuntimeError("device status")
-        us = e0.elapsed_time(e1) * 1e3 / K
+        us = e0.elapsed_time(e1) * 1e3 / (K * reps)
         # algorithmic bytes: x once, codes, positions, the cos/sin rows used, scales
         nbytes = T * NH * D * 2 + T * NH * D + T * 4 + T * D * 4 + NH * 4
-        sweep.append({"T": T, "us_per_call": round(us, 2), "tokens_per_s": round(T / (us * 1e-6), 1),
+        sweep.append({"T": T, "us_per_call": round(us, 2), "eager_us_per_call": round(eager_us, 2),
+                      "tokens_per_s": round(T / (us * 1e-6), 1),
                       "algorithmic_bytes": nbytes,
                       "hbm_frac": round(nbytes / (us * 1e-6) / 1e9 / hbm_peak, 4)})
     big = sweep[-1]
     line = {"metric": "inverse-RoPE + per-head FP8 quant tokens/s (32 heads x 128)",
             "value": big["tokens_per_s"], "unit": "tokens/s", "steps": K, "warmup": args.warmup,
             "config": {"workload": "x bf16 [T, 32, 128], positions < 8192, fp32 cos/sin tables; "
-                                   "one cooperative kernel up to 1216 tokens, else three "
-                                   "launches (per-head amax, scale fold, quantise)",
-                       "l2": "four input copies rotate call to call"},
+                                   "one cooperative kernel up to 1216 tokens, else two "
+                                   "launches (per-head amax; scale fold + quantise)",
+                       "l2": "four input copies rotate call to call",
+                       "timing": "us_per_call: K calls captured in one CUDA graph, replayed "
+                                 "(device time); eager_us_per_call: the same calls launched "
+                                 "from Python one by one"},
             "sweep": sweep,
             "roofline": {"bound": "hbm", "achieved": round(big["algorithmic_bytes"] /
                                                            (big["us_per_call"] * 1e-6) / 1e9, 1),

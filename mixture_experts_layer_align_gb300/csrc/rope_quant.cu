@@ -15,23 +15,19 @@
 // Shapes are runtime values: one binary for every T, head count and (power of
 // two) head size.
 //
-// Two passes over x (bf16 [T][NH][D]).  Large inputs, three launches:
-//   1. rope_pass_kernel<false>: per-head maxima of |y| per CTA -> partials;
-//   2. rope_fold_kernel (one CTA): the NH scales and the status word;
-//   3. rope_pass_kernel<true>: rotate again, divide by the head's scale,
-//      write the codes.
+// Two passes over x (bf16 [T][NH][D]), a group of D/8 lanes per head vector,
+// 8 elements per lane (one 16-byte load of x, one 8-byte store of codes);
+// per-head maxima reduce inside each group, then one shared-memory atomic per
+// group.
 // Small inputs (at most two rounds of two work items per warp on one CTA of
-// 512 threads per SM), one cooperative launch, rope_coop_kernel: pass 1,
-// one grid synchronisation, every CTA folds the maxima itself, pass 2 (the
-// latency of the three launches is what small inputs pay for; at 8192 tokens
-// of 32 heads the single launch's 16 warps per SM keep too few loads in
-// flight: 82 against 55 us).
-// Three-launch path: a warp takes one token at a time: one load of its position and of the
-// cos/sin entries of its lane's 4 pairs, then the token's heads, 32/(D/8) per
-// iteration (a group of D/8 lanes per head vector, 8 elements per lane: one
-// 16-byte load of x, one 8-byte store of codes), several iterations' loads in
-// flight.  Per-head maxima reduce inside each group, then one shared-memory
-// atomic per group.
+// 512 threads per SM), one cooperative launch, rope_coop_kernel: pass 1, one
+// grid synchronisation, every CTA folds the per-CTA maxima itself, pass 2
+// (the latency of separate launches is what small inputs pay for).
+// Large inputs: a zeroed word per head, then two launches of rope_pass_kernel
+// (a warp per token, eight warps per CTA, up to eight CTAs per SM): pass 1
+// adds each CTA's maxima with one global atomic max per head; pass 2 forms the
+// scales in every CTA from those words and writes the codes.  At 8192 tokens
+// of 32 heads x 128 the second pass finds most of x in L2.
 #include <cooperative_groups.h>
 #include <cuda_bf16.h>
 #include <stdint.h>
@@ -46,8 +42,6 @@ namespace {
 
 namespace cg = cooperative_groups;
 
-constexpr int kRopeThreads = 256;  // 8 warps: 8 tokens at a time per CTA
-constexpr int kRopeBatch = 4;      // head iterations whose x loads are in flight together
 
 __device__ __forceinline__ float lo16(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float hi16(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
@@ -66,23 +60,40 @@ __device__ __forceinline__ void rotate8(uint4 v, float4 c, float4 s, float (&y)[
   }
 }
 
-// kQuant = false: per-CTA per-head maxima of |y| into partials [NH][grid]
-// (head-major, so the fold reads each head's maxima contiguously), then one
-// flag per CTA (a position outside the tables, treated as 0) after them.
-// kQuant = true: codes with the per-head scales.
+constexpr int kRopeThreads = 256;  // 8 warps: 8 tokens at a time per CTA
+constexpr int kRopeBatch = 4;      // head iterations whose x loads are in flight together
+
+// Large inputs, a warp per token.  kQuant = false: the CTA's per-head maxima
+// of |y| go to the call's global maxima `gmax` [NH] (max |y| bits, zeroed
+// before the launch) with one atomic max per head, and a position outside the
+// tables sets gmax[NH].  kQuant = true: every CTA forms the NH scales from
+// gmax (CTA 0 also stores them and the status word), then writes the codes.
+// The token's first kRopeBatch loads of x are issued before its position is
+// read, so they overlap the position -> cos/sin chain.
 template <bool kQuant>
 __global__ void __launch_bounds__(kRopeThreads)
     rope_pass_kernel(const __nv_bfloat16* __restrict__ x, const int32_t* __restrict__ pos,
                      const float* __restrict__ cos_t, const float* __restrict__ sin_t, int T,
-                     int NH, int D, int max_pos, float* __restrict__ partials,
-                     const float* __restrict__ scales, uint8_t* __restrict__ codes) {
+                     int NH, int D, int max_pos, unsigned* __restrict__ gmax,
+                     float* __restrict__ scales, uint8_t* __restrict__ codes, Ctrl* ctrl) {
   extern __shared__ unsigned s_head[];  // [NH]: max|y| bits, or the scales
   __shared__ int s_bad;
   pdl_wait();
   pdl_trigger();
-  for (int h = threadIdx.x; h < NH; h += blockDim.x)
-    s_head[h] = kQuant ? __float_as_uint(scales[h]) : 0u;
-  if (threadIdx.x == 0) s_bad = 0;
+  for (int h = threadIdx.x; h < NH; h += blockDim.x) {
+    if (kQuant) {
+      const float a = __uint_as_float(__ldcg(gmax + h));
+      const float sc = a > 0.f ? __fdiv_rn(a, 448.f) : 1.f;
+      s_head[h] = __float_as_uint(sc);
+      if (blockIdx.x == 0) scales[h] = sc;
+    } else {
+      s_head[h] = 0u;
+    }
+  }
+  if (threadIdx.x == 0) {
+    s_bad = 0;
+    if (kQuant && blockIdx.x == 0) ctrl->err = __ldcg(gmax + NH) != 0u ? kDevErrRange : 0;
+  }
   __syncthreads();
   const int lane = threadIdx.x & 31;
   const int n8 = D >> 3;              // lanes per head vector (a power of two <= 32)
@@ -93,30 +104,36 @@ __global__ void __launch_bounds__(kRopeThreads)
   const int nwarps = gridDim.x * (blockDim.x >> 5);
   int bad = 0;
   for (int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); t < T; t += nwarps) {
-    int p = pos[t];
+    const size_t row0 = static_cast<size_t>(t) * NH;
+    uint4 v[kRopeBatch];
+#pragma unroll
+    for (int u = 0; u < kRopeBatch; ++u) {
+      const int h = u * hp + hoff;
+      v[u] = h < NH ? __ldg(reinterpret_cast<const uint4*>(x + (row0 + h) * D + c8 * 8))
+                    : make_uint4(0, 0, 0, 0);
+    }
+    int p = __ldg(pos + t);
     if (p < 0 || p >= max_pos) {
       bad = 1;
       p = 0;
     }
     const size_t tab = static_cast<size_t>(p) * (D / 2) + c8 * 4;
-    const float4 c = *reinterpret_cast<const float4*>(cos_t + tab);
-    const float4 s = *reinterpret_cast<const float4*>(sin_t + tab);
-    const size_t row0 = static_cast<size_t>(t) * NH;
-    // kRopeBatch iterations' loads of x are issued before any is used
+    const float4 c = __ldg(reinterpret_cast<const float4*>(cos_t + tab));
+    const float4 s = __ldg(reinterpret_cast<const float4*>(sin_t + tab));
     for (int hb = 0; hb < NH; hb += hp * kRopeBatch) {
-      uint4 v[kRopeBatch];
+      if (hb > 0) {
 #pragma unroll
-      for (int u = 0; u < kRopeBatch; ++u) {
-        const int h = hb + u * hp + hoff;
-        v[u] = h < NH ? *reinterpret_cast<const uint4*>(x + (row0 + h) * D + c8 * 8)
-                      : make_uint4(0, 0, 0, 0);
+        for (int u = 0; u < kRopeBatch; ++u) {
+          const int h = hb + u * hp + hoff;
+          v[u] = h < NH ? __ldg(reinterpret_cast<const uint4*>(x + (row0 + h) * D + c8 * 8))
+                        : make_uint4(0, 0, 0, 0);
+        }
       }
 #pragma unroll
       for (int u = 0; u < kRopeBatch; ++u) {
         const int h = hb + u * hp + hoff;
         float y[8];
         rotate8(v[u], c, s, y);
-        float m = 0.f;
         if (kQuant) {
           if (h < NH) {
             const float sc = __uint_as_float(s_head[h]);
@@ -129,6 +146,7 @@ __global__ void __launch_bounds__(kRopeThreads)
             *reinterpret_cast<uint2*>(codes + (row0 + h) * D + c8 * 8) = q;
           }
         } else {
+          float m = 0.f;
 #pragma unroll
           for (int j = 0; j < 8; ++j) m = fmaxf(m, fabsf(y[j]));
           // maximum over the group of lanes of one head vector
@@ -142,41 +160,8 @@ __global__ void __launch_bounds__(kRopeThreads)
     if (bad) s_bad = 1;
     __syncthreads();
     for (int h = threadIdx.x; h < NH; h += blockDim.x)
-      partials[static_cast<size_t>(h) * gridDim.x + blockIdx.x] = __uint_as_float(s_head[h]);
-    if (threadIdx.x == 0)
-      partials[static_cast<size_t>(gridDim.x) * NH + blockIdx.x] = s_bad ? 1.f : 0.f;
-  }
-}
-
-// One CTA: a warp per head folds the per-CTA maxima into the head's scale;
-// the status word records a position outside the tables.
-__global__ void __launch_bounds__(1024)
-    rope_fold_kernel(const float* __restrict__ partials, int n_part, int NH,
-                     float* __restrict__ scales, Ctrl* ctrl) {
-  pdl_wait();
-  pdl_trigger();
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
-  for (int h = warp; h < NH; h += nwarps) {
-    const float* ph = partials + static_cast<size_t>(h) * n_part;
-    float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;  // independent chains: loads in flight
-    int b = lane;
-    for (; b + 96 < n_part; b += 128) {
-      a0 = fmaxf(a0, ph[b]);
-      a1 = fmaxf(a1, ph[b + 32]);
-      a2 = fmaxf(a2, ph[b + 64]);
-      a3 = fmaxf(a3, ph[b + 96]);
-    }
-    for (; b < n_part; b += 32) a0 = fmaxf(a0, ph[b]);
-    float a = fmaxf(fmaxf(a0, a1), fmaxf(a2, a3));
-    for (int o = 16; o > 0; o >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
-    if (lane == 0) scales[h] = a > 0.f ? __fdiv_rn(a, 448.f) : 1.f;
-  }
-  if (warp == 0) {
-    int bad = 0;
-    for (int b = lane; b < n_part; b += 32)
-      bad |= partials[static_cast<size_t>(n_part) * NH + b] != 0.f;
-    bad = __any_sync(0xffffffffu, bad);
-    if (lane == 0) ctrl->err = bad ? kDevErrRange : 0;
+      if (s_head[h] != 0u) atomicMax(gmax + h, s_head[h]);
+    if (threadIdx.x == 0 && s_bad) atomicOr(gmax + NH, 1u);
   }
 }
 
@@ -184,13 +169,13 @@ constexpr int kCoopThreads = 512;  // 16 warps per CTA, at most one CTA per SM
 constexpr int kCoopBatch = 2;      // warp iterations of head vectors per item
 
 // One pass over this CTA's share of the work.  An item is (token, group of
-// hp * kCoopBatch head vectors); a warp takes two items per round, so that
-// the round costs two dependent memory round trips for both (x and the
-// positions, then the cos/sin entries of those positions).  kQuant = false:
-// the CTA's per-head maxima of |y| into s_head (max |y| bits), a position
-// outside the tables into *bad_out.  kQuant = true: codes with the scales in
-// s_head (fp32 bits).
-template <bool kQuant>
+// hp * kB head vectors); a warp takes two items per round, so that the round
+// costs two dependent memory round trips for both (x and the positions, then
+// the cos/sin entries of those positions), with 2 kB 16-byte loads of x per
+// lane in flight.  kQuant = false: the CTA's per-head maxima of |y| into
+// s_head (max |y| bits), a position outside the tables into *bad_out.
+// kQuant = true: codes with the scales in s_head (fp32 bits).
+template <bool kQuant, int kB>
 __device__ __forceinline__ void rope_items_pass(const __nv_bfloat16* __restrict__ x,
                                           const int32_t* __restrict__ pos,
                                           const float* __restrict__ cos_t,
@@ -203,14 +188,14 @@ __device__ __forceinline__ void rope_items_pass(const __nv_bfloat16* __restrict_
   const int hp = 32 >> lg8;           // head vectors per warp iteration
   const int c8 = lane & (n8 - 1);
   const int hoff = lane >> lg8;
-  const int gh = hp * kCoopBatch;     // head vectors per item
+  const int gh = hp * kB;     // head vectors per item
   const int ngroups = (NH + gh - 1) / gh;
   const long long n_items = static_cast<long long>(T) * ngroups;
   const long long nwarps = static_cast<long long>(gridDim.x) * (blockDim.x >> 5);
   const long long w0 = static_cast<long long>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
   int bad = 0;
   for (long long i0 = w0; i0 < n_items; i0 += 2 * nwarps) {
-    uint4 v[2][kCoopBatch];
+    uint4 v[2][kB];
     int pp[2], tt[2], hb[2];
     bool live[2];
 #pragma unroll
@@ -222,7 +207,7 @@ __device__ __forceinline__ void rope_items_pass(const __nv_bfloat16* __restrict_
       pp[it] = live[it] ? pos[tt[it]] : 0;
       const size_t row0 = static_cast<size_t>(tt[it]) * NH;
 #pragma unroll
-      for (int u = 0; u < kCoopBatch; ++u) {
+      for (int u = 0; u < kB; ++u) {
         const int h = hb[it] + u * hp + hoff;
         v[it][u] = (live[it] && h < NH) ? *reinterpret_cast<const uint4*>(x + (row0 + h) * D + c8 * 8)
                                         : make_uint4(0, 0, 0, 0);
@@ -245,7 +230,7 @@ __device__ __forceinline__ void rope_items_pass(const __nv_bfloat16* __restrict_
       if (!live[it]) continue;  // uniform over the warp
       const size_t row0 = static_cast<size_t>(tt[it]) * NH;
 #pragma unroll
-      for (int u = 0; u < kCoopBatch; ++u) {
+      for (int u = 0; u < kB; ++u) {
         const int h = hb[it] + u * hp + hoff;
         float y[8];
         rotate8(v[it][u], cs[it], sn[it], y);
@@ -274,29 +259,13 @@ __device__ __forceinline__ void rope_items_pass(const __nv_bfloat16* __restrict_
   if (!kQuant && bad) *bad_out = 1;
 }
 
-// The whole operation: pass 1, grid synchronisation, per-head scales, pass 2.
-// partials: [NH][gridDim] per-CTA maxima (head-major: a head's maxima are
-// contiguous), then [gridDim] flags.
-__global__ void __launch_bounds__(kCoopThreads, 1)
-    rope_coop_kernel(const __nv_bfloat16* __restrict__ x, const int32_t* __restrict__ pos,
-                     const float* __restrict__ cos_t, const float* __restrict__ sin_t, int T,
-                     int NH, int D, int max_pos, float* __restrict__ partials,
-                     float* __restrict__ scales, uint8_t* __restrict__ codes, Ctrl* ctrl) {
-  extern __shared__ unsigned s_head[];  // [NH]: max|y| bits, then the scales
-  __shared__ int s_bad;
+// The per-CTA maxima [NH][G] (head-major) folded into the NH scales, a warp
+// per head, into s_head (fp32 bits); `scales` and `ctrl` (status word from the
+// G flags after the maxima) when not null.
+__device__ __forceinline__ void rope_fold_heads(const float* __restrict__ partials, int G, int NH,
+                                                unsigned* s_head, float* __restrict__ scales,
+                                                Ctrl* ctrl) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
-  const int G = static_cast<int>(gridDim.x);
-  for (int h = threadIdx.x; h < NH; h += blockDim.x) s_head[h] = 0u;
-  if (threadIdx.x == 0) s_bad = 0;
-  __syncthreads();
-  rope_items_pass<false>(x, pos, cos_t, sin_t, T, NH, D, max_pos, s_head, nullptr, &s_bad);
-  __syncthreads();
-  for (int h = threadIdx.x; h < NH; h += blockDim.x)
-    partials[static_cast<size_t>(h) * G + blockIdx.x] = __uint_as_float(s_head[h]);
-  if (threadIdx.x == 0) partials[static_cast<size_t>(G) * NH + blockIdx.x] = s_bad ? 1.f : 0.f;
-  // nothing above waits on another CTA, so every CTA arrives here
-  cg::this_grid().sync();
-  // every CTA folds the per-CTA maxima into the scales (a warp per head)
   for (int h = warp; h < NH; h += nwarps) {
     const float* ph = partials + static_cast<size_t>(h) * G;
     float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;  // independent chains: loads in flight
@@ -313,17 +282,46 @@ __global__ void __launch_bounds__(kCoopThreads, 1)
     const float sc = a > 0.f ? __fdiv_rn(a, 448.f) : 1.f;
     if (lane == 0) {
       s_head[h] = __float_as_uint(sc);
-      if (blockIdx.x == 0) scales[h] = sc;
+      if (scales != nullptr) scales[h] = sc;
     }
   }
-  if (blockIdx.x == 0 && warp == 0) {
+  if (ctrl != nullptr && warp == 0) {
     int bad = 0;
     for (int b = lane; b < G; b += 32) bad |= __ldcg(partials + static_cast<size_t>(G) * NH + b) != 0.f;
     bad = __any_sync(0xffffffffu, bad);
     if (lane == 0) ctrl->err = bad ? kDevErrRange : 0;
   }
+}
+
+// The whole operation: pass 1, grid synchronisation, per-head scales, pass 2.
+// partials: [NH][gridDim] per-CTA maxima (head-major: a head's maxima are
+// contiguous), then [gridDim] flags.
+__global__ void __launch_bounds__(kCoopThreads, 1)
+    rope_coop_kernel(const __nv_bfloat16* __restrict__ x, const int32_t* __restrict__ pos,
+                     const float* __restrict__ cos_t, const float* __restrict__ sin_t, int T,
+                     int NH, int D, int max_pos, float* __restrict__ partials,
+                     float* __restrict__ scales, uint8_t* __restrict__ codes, Ctrl* ctrl) {
+  extern __shared__ unsigned s_head[];  // [NH]: max|y| bits, then the scales
+  __shared__ int s_bad;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
+  const int G = static_cast<int>(gridDim.x);
+  for (int h = threadIdx.x; h < NH; h += blockDim.x) s_head[h] = 0u;
+  if (threadIdx.x == 0) s_bad = 0;
   __syncthreads();
-  rope_items_pass<true>(x, pos, cos_t, sin_t, T, NH, D, max_pos, s_head, codes, nullptr);
+  rope_items_pass<false, kCoopBatch>(x, pos, cos_t, sin_t, T, NH, D, max_pos, s_head, nullptr,
+                                     &s_bad);
+  __syncthreads();
+  for (int h = threadIdx.x; h < NH; h += blockDim.x)
+    partials[static_cast<size_t>(h) * G + blockIdx.x] = __uint_as_float(s_head[h]);
+  if (threadIdx.x == 0) partials[static_cast<size_t>(G) * NH + blockIdx.x] = s_bad ? 1.f : 0.f;
+  // nothing above waits on another CTA, so every CTA arrives here
+  cg::this_grid().sync();
+  // every CTA folds the per-CTA maxima into the scales
+  rope_fold_heads(partials, G, NH, s_head, blockIdx.x == 0 ? scales : nullptr,
+                  blockIdx.x == 0 ? ctrl : nullptr);
+  __syncthreads();
+  rope_items_pass<true, kCoopBatch>(x, pos, cos_t, sin_t, T, NH, D, max_pos, s_head, codes,
+                                    nullptr);
 }
 
 }  // namespace
@@ -364,17 +362,18 @@ cudaError_t launch_inv_rope_quant(const __nv_bfloat16* x, const int32_t* pos, co
                                       max_pos, partials, scales, codes, ctrl),
                    "cooperative kernel launch");
   }
-  const int grid = rope_grid(T, NH, D, num_sms);
-  cudaError_t e = launch_pdl(rope_pass_kernel<false>, dim3(grid), dim3(kRopeThreads), smem, st, x,
-                             pos, cos_t, sin_t, T, NH, D, max_pos, partials,
-                             static_cast<const float*>(nullptr), static_cast<uint8_t*>(nullptr));
+  // the call's per-head maxima and flag word, zeroed, then the two passes
+  unsigned* gmax = reinterpret_cast<unsigned*>(partials);
+  cudaError_t e = checked(cudaMemsetAsync(gmax, 0, sizeof(unsigned) * (static_cast<size_t>(NH) + 1), st),
+                          "memset");
   if (e != cudaSuccess) return e;
-  e = launch_pdl(rope_fold_kernel, dim3(1), dim3(1024), 0, st,
-                 static_cast<const float*>(partials), grid, NH, scales, ctrl);
+  const int grid = rope_grid(T, NH, D, num_sms);
+  e = launch_pdl(rope_pass_kernel<false>, dim3(grid), dim3(kRopeThreads), smem, st, x, pos, cos_t,
+                 sin_t, T, NH, D, max_pos, gmax, static_cast<float*>(nullptr),
+                 static_cast<uint8_t*>(nullptr), static_cast<Ctrl*>(nullptr));
   if (e != cudaSuccess) return e;
   return launch_pdl(rope_pass_kernel<true>, dim3(grid), dim3(kRopeThreads), smem, st, x, pos,
-                    cos_t, sin_t, T, NH, D, max_pos, static_cast<float*>(nullptr),
-                    static_cast<const float*>(scales), codes);
+                    cos_t, sin_t, T, NH, D, max_pos, gmax, scales, codes, ctrl);
 }
 
 }  // namespace moe

@@ -15,6 +15,9 @@ pytestmark = pytest.mark.gpu
 @pytest.mark.parametrize("T,NH,D,max_pos", [
     (1, 1, 8, 4), (37, 6, 64, 512), (257, 8, 128, 4096), (1000, 3, 256, 2048),
     (129, 5, 16, 64), (4096, 32, 128, 8192), (8192, 8, 32, 8192),
+    (20000, 3, 256, 2048),   # two launches, one head vector per warp iteration
+    (12000, 40, 16, 64),     # two launches, a partial group of heads
+    (2000, 1024, 8, 64),     # two launches with the fold kernel between them
 ])
 def test_inv_rope_quant_matches_oracle(gpu_lib, T, NH, D, max_pos):
     r = inputs.make_rope_inputs(T, NH, D, max_pos, seed=T)
