@@ -149,8 +149,9 @@ moe_status_t moe_quantize_e4m3_noalloc(const void* x, int T, int H, uint8_t* x_q
  *              as 0)
  * Requires T >= 0 (0 enqueues nothing), 1 <= NH <= 4096, D in {8, 16, 32, 64,
  * 128, 256}, max_pos >= 1, 16-byte aligned x / cos_tab / sin_tab, 8-byte
- * aligned codes; T*NH*D >= 2^31 returns MOE_ERR_UNSUPPORTED.  Two kernels on
- * `stream`; all sizes are runtime values.
+ * aligned codes; T*NH*D >= 2^31 returns MOE_ERR_UNSUPPORTED.  Enqueues on
+ * `stream` one cooperative kernel (small inputs), or a memset of NH + 1 words
+ * of the scratch and two kernels (large inputs); all sizes are runtime values.
  */
 size_t moe_inv_rope_scratch_size(int T, int NH, int D);
 moe_status_t moe_inv_rope_quant_per_head(const void* x, const int32_t* positions,
