@@ -206,11 +206,13 @@ typedef struct {
  * the same within fp32 summation order. */
 #define MOE_FLAG_TOKENS_IN_M 0x4
 #define MOE_FLAG_WEIGHTS_IN_M 0x8
-/* FP8 gate/up tiles of 256 tokens (experts averaging more than 256 routed
- * rows: prefill) run on SM pairs by default: a cluster of two CTAs issues
- * tcgen05 MMAs with M = 256 (cta_group::2), each SM holding its 128 weight rows
- * and half of the token rows.  This flag runs them on one SM per tile instead
- * (ablation).  Results are the same within fp32 summation order. */
+/* FP8 gate/up tiles of 256 tokens (I % 256 == 0 and experts averaging at
+ * least 128 routed rows: prefill) run on SM pairs by default: a cluster of two
+ * CTAs issues tcgen05 MMAs with M = 256 (cta_group::2), each SM holding its 128
+ * weight rows and half of the token rows.  This flag runs the gate/up GEMM on
+ * one SM per tile instead (ablation): 256-token tiles when experts average more
+ * than 256 rows, else 128-token tiles.  Results are the same within fp32
+ * summation order. */
 #define MOE_FLAG_NO_SM_PAIRS 0x10
 /* Small batches (T*top_k <= 2048, E <= 256): run the whole layer as one
  * cooperative persistent kernel instead of the kernel sequence (one CTA per

@@ -84,11 +84,13 @@ def test_fused_large_batch_paths(gpu_lib, T, H, I, E, k, placement):
     run_case(gpu_lib, w, a, k, True, rows=None, flags=flags)
 
 
-# Wide gate/up tiles (experts averaging more than 256 rows, I % 256 == 0) run on
-# SM pairs (tcgen05 cta_group::2) by default; MOE_FLAG_NO_SM_PAIRS runs the same
-# tiles on one SM each.
+# Wide gate/up tiles (I % 256 == 0, experts averaging at least 128 rows) run on
+# SM pairs (tcgen05 cta_group::2) by default; MOE_FLAG_NO_SM_PAIRS runs the
+# gate/up GEMM on one SM per tile (256-row tiles from 256 rows per expert on
+# average, else 128-row tiles).
 @pytest.mark.parametrize("T,H,I,E,k,routing", [
     (1200, 256, 512, 4, 2, "uniform"),    # one alignment kernel, gather
+    (700, 256, 512, 8, 2, "uniform"),     # 175 rows per expert: pairs from 128 on average
     (1100, 384, 768, 4, 3, "uniform"),    # ragged tiles, three weight-block pairs
     (3000, 256, 512, 8, 2, "zipf"),       # > 4096 pairs: two-pass alignment, skew
 ])
