@@ -16,11 +16,13 @@ pytestmark = pytest.mark.gpu
 # the single cooperative kernel (its CTAs also wait on grid-wide counters):
 # (8, ...) decode-style tiles (I = 2176 > 2048 keeps the down weights in M);
 # (600, ...) 300 rows per expert: wide gate/up tiles on one SM each (I = 128),
-# tokens in M for down.  (1200, ...) wide gate/up tiles on SM pairs.
+# tokens in M for down.  (1200, ...) wide gate/up tiles on SM pairs;
+# (4096, ...) the same, with the down GEMM combining through bf16 rows (TMA
+# stores) and the row-combine kernel.
 @pytest.mark.parametrize("T,H,I,E,k,flags", [
     (8, 256, 256, 8, 2, 0), (8, 256, 2176, 4, 2, 0), (600, 256, 128, 4, 2, 0),
     (8, 256, 256, 8, 2, 0x20), (8, 256, 2176, 4, 2, 0x20), (600, 256, 128, 4, 2, 0x20),
-    (1200, 256, 512, 4, 2, 0)])
+    (1200, 256, 512, 4, 2, 0), (4096, 1024, 256, 4, 2, 0)])
 def test_forced_timeout_reports_status_and_context_survives(gpu_lib, T, H, I, E, k, flags):
     assert flags in (0, gpu_lib.MOE_FLAG_ONE_KERNEL)
     w = inputs.make_weights(H, I, E, "fp8", seed=11)
