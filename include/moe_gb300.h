@@ -263,9 +263,12 @@ moe_status_t moe_fused_forward(const moe_fused_args* args, void* workspace, size
  * (e.g. an all-reduce MAX of that one float on the same stream), so every
  * rank quantises h with the scale of the whole tensor, and after the second
  * call sums the ranks' outputs (all-reduce SUM).  Both calls take the same
- * args and workspace, with no other use of the workspace in between; the
- * first call's status word and errors are as for moe_fused_forward.  With
- * bf16 weights h is not quantised and the word is unused.
+ * args and workspace, with no other use of the workspace in between, and
+ * each moe_fused_forward_down follows its own moe_fused_forward_gate_up (the
+ * first call leaves the routing, the tile lists and h in the workspace for the
+ * second); the first call's status word and errors are as for
+ * moe_fused_forward.  With bf16 weights h is not quantised and the word is
+ * unused.
  */
 moe_status_t moe_fused_forward_gate_up(const moe_fused_args* args, void* workspace,
                                        size_t workspace_bytes, moe_stream_t stream);
