@@ -75,6 +75,7 @@ def test_fused_small(gpu_lib, T, H, I, E, k, renorm, dtype, path):
     (2600, 256, 128, 16, 2),    # > 4096 pairs: two-pass alignment, tokens quantised once
     (2048, 1024, 128, 32, 8),   # pairs x H > 8M: combine through per-pair rows
     (2048, 1152, 128, 32, 8),   # the same with H % 256 != 0: one weight block per tile
+    (512, 4096, 256, 16, 8),    # rows per pair at <= 4096 pairs: one alignment kernel, gather
     (3000, 1024, 256, 8, 4),    # skewed counts: experts with odd numbers of row tiles
     (2500, 1280, 128, 6, 3),    # ragged tiles, five column blocks of 256
 ])
