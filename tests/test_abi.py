@@ -168,3 +168,39 @@ def test_binding_constants_match_header():
     flags = [defines[n] for n in defines if n.startswith(("MOE_FLAG_", "MOE_DEBUG_"))
              and n != "MOE_DEBUG_TIMEOUT_MS"]
     assert all(f & (f - 1) == 0 for f in flags) and len(set(flags)) == len(flags)
+
+
+def test_header_compiles_as_c_and_the_library_links_from_c(lib, tmp_path):
+    """A plain C11 program that includes the header, takes the address of
+    every declared entry point (so the linker must resolve each one in the
+    library) and calls two host-only functions."""
+    import shutil
+    import subprocess
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    names = declared_functions()
+    src = tmp_path / "abi_check.c"
+    src.write_text(
+        "#include <stdio.h>\n#include \"moe_gb300.h\"\n"
+        "typedef void (*fn_t)(void);\n"
+        "static fn_t table[] = {\n" +
+        "".join(f"  (fn_t){n},\n" for n in names) +
+        "};\n"
+        "int main(void) {\n"
+        "  printf(\"%d %s %zu\\n\", (int)(sizeof(table) / sizeof(table[0])),\n"
+        "         moe_status_string(MOE_OK),\n"
+        "         moe_fused_workspace_size(16, 256, 256, 8, 2, MOE_DT_FP8_E4M3));\n"
+        "  return 0;\n}\n")
+    libdir = os.path.dirname(moe.LIB_PATH)
+    exe = tmp_path / "abi_check"
+    r = subprocess.run([cc, "-std=c11", "-Wall", "-Werror", "-I", os.path.join(ROOT, "include"),
+                        str(src), "-o", str(exe), moe.LIB_PATH, f"-Wl,-rpath,{libdir}"],
+                       capture_output=True, text=True)
+    assert r.returncode == 0, r.stdout + r.stderr
+    out = subprocess.run([str(exe)], capture_output=True, text=True, timeout=60)
+    assert out.returncode == 0, out.stderr
+    n, status, ws = out.stdout.split()
+    assert int(n) == len(names)
+    assert status == lib.moe_status_string(0).decode()
+    assert int(ws) == lib.moe_fused_workspace_size(16, 256, 256, 8, 2, moe.MOE_DT_FP8_E4M3)
