@@ -55,3 +55,52 @@ def test_position_outside_tables_is_reported(gpu_lib):
     _, _, scratch = gpu_lib.moe_inv_rope_quant_per_head(
         r.x.cuda(), pos.cuda(), r.cos.cuda(), r.sin.cuda(), scratch=scratch)
     assert gpu_lib.moe_check_status(scratch) == 0
+
+
+def test_position_outside_tables_large_input(gpu_lib):
+    """The two-launch path (per-head words by atomic max, flag word after
+    them) reports a bad position and clears the status on the next call."""
+    r = inputs.make_rope_inputs(4096, 32, 128, 8192, seed=12)
+    pos = r.positions.clone()
+    pos[1000] = -1
+    codes, scales, scratch = gpu_lib.moe_inv_rope_quant_per_head(
+        r.x.cuda(), pos.cuda(), r.cos.cuda(), r.sin.cuda())
+    assert gpu_lib.moe_check_status(scratch) == 6  # MOE_ERR_DEVICE_RANGE
+    pos[1000] = 0
+    ref = oracle.inv_rope_quant(r.x, pos, r.cos, r.sin)
+    assert np.array_equal(scales.cpu().numpy(), ref["scales"])
+    assert np.array_equal(codes.cpu().numpy(), ref["codes"])
+    _, _, scratch = gpu_lib.moe_inv_rope_quant_per_head(
+        r.x.cuda(), pos.cuda(), r.cos.cuda(), r.sin.cuda(), scratch=scratch)
+    assert gpu_lib.moe_check_status(scratch) == 0
+
+
+@pytest.mark.parametrize("T", [64, 4096])  # one cooperative launch; memset + two launches
+def test_graph_replay_equals_eager(gpu_lib, T):
+    """Captured once in a CUDA graph and replayed on new inputs written into
+    the same buffers, the operation gives the eager (and oracle) result."""
+    NH, D, max_pos = 32, 128, 8192
+    a = inputs.make_rope_inputs(T, NH, D, max_pos, seed=T)
+    b = inputs.make_rope_inputs(T, NH, D, max_pos, seed=T + 1)
+    x, pos = a.x.cuda(), a.positions.cuda()
+    cos_t, sin_t = a.cos.cuda(), a.sin.cuda()
+    codes = torch.empty(T, NH, D, dtype=torch.uint8, device="cuda")
+    scales = torch.empty(NH, dtype=torch.float32, device="cuda")
+    scratch = torch.empty(gpu_lib.moe_inv_rope_scratch_size(T, NH, D), dtype=torch.uint8,
+                          device="cuda")
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        gpu_lib.moe_inv_rope_quant_per_head(x, pos, cos_t, sin_t, codes, scales, scratch)
+    torch.cuda.current_stream().wait_stream(side)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        gpu_lib.moe_inv_rope_quant_per_head(x, pos, cos_t, sin_t, codes, scales, scratch)
+    x.copy_(b.x.cuda())
+    pos.copy_(b.positions.cuda())
+    graph.replay()
+    torch.cuda.synchronize()
+    assert gpu_lib.moe_check_status(scratch) == 0
+    ref = oracle.inv_rope_quant(b.x, b.positions, a.cos, a.sin)
+    assert np.array_equal(scales.cpu().numpy(), ref["scales"])
+    assert np.array_equal(codes.cpu().numpy(), ref["codes"])
