@@ -24,10 +24,9 @@
 // grid synchronisation, every CTA folds the per-CTA maxima itself, pass 2
 // (the latency of separate launches is what small inputs pay for).
 // Large inputs: a zeroed word per head, then two launches of rope_pass_kernel
-// (a warp per token, eight warps per CTA, up to eight CTAs per SM): pass 1
-// adds each CTA's maxima with one global atomic max per head; pass 2 forms the
-// scales in every CTA from those words and writes the codes.  At 8192 tokens
-// of 32 heads x 128 the second pass finds most of x in L2.
+// (a warp per token, eight warps per CTA, a grid of at most eight CTAs per
+// SM): pass 1 adds each CTA's maxima with one global atomic max per head;
+// pass 2 forms the scales in every CTA from those words and writes the codes.
 #include <cooperative_groups.h>
 #include <cuda_bf16.h>
 #include <stdint.h>
