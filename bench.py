@@ -280,6 +280,34 @@ def time_calls(call, n, block=CALL_BLOCK, warm=5):
     return [ev[b].elapsed_time(ev[b + 1]) * 1e3 / block for b in range(n)]
 
 
+def graph_call_us(call, n=20, reps=5):
+    """Device time per call when n back-to-back calls (cycling the same
+    inputs and weight copies as `call`) are captured once in a CUDA graph and
+    the graph is replayed: the launch path a serving loop would use.  Not the
+    headline `value` (that is eager calls), reported beside it."""
+    import torch
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        call(0)
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        for i in range(n):
+            call(i)
+    graph.replay()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(reps):
+        graph.replay()
+    e1.record()
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) * 1e3 / (n * reps)
+
+
 L2_BYTES = 129 * 2 ** 20
 
 
@@ -626,6 +654,7 @@ def run_ours(args, rank, local_rank, world):
 
         us_all = time_calls(call, max(50, K))
         us = statistics.median(us_all)
+        graph_us = graph_call_us(call)
         nbytes, flops = layer_work(stats[T]["touched"], T, H, I, E, k, fp8)
         bound, frac, hfrac, tfrac = roofline_fractions(us, nbytes, flops, hbm_peak, tc_peak)
         sweep.append({
@@ -636,7 +665,10 @@ def run_ours(args, rank, local_rank, world):
             "layer_bytes": nbytes, "bound": bound, "frac": round(frac, 4),
             "hbm_frac": round(hfrac, 4), "tensor_frac": round(tfrac, 4),
             "gemm1_us_events": round(statistics.median(gemm1_ms[T]) * 1e3, 2),
-            "gemm2_us_events": round(statistics.median(gemm2_ms[T]) * 1e3, 2)})
+            "gemm2_us_events": round(statistics.median(gemm2_ms[T]) * 1e3, 2),
+            "graph_us_per_call": round(graph_us, 2),
+            "graph_frac": round(roofline_fractions(graph_us, nbytes, flops, hbm_peak,
+                                                   tc_peak)[1], 4)})
 
     # end to end through the same API: pinned host inputs -> device -> host output
     e2e = None
@@ -747,7 +779,8 @@ def run_ours(args, rank, local_rank, world):
         "sweep_timing": f"per call: CUDA events between blocks of {CALL_BLOCK} back-to-back "
                         "calls (none between the calls of a block, none inside a call); "
                         "median / p10 / p90 over the blocks' per-call times; weights cold "
-                        "in L2",
+                        "in L2; graph_us_per_call: 20 of the same calls captured in one "
+                        "CUDA graph and replayed (reported beside, not in value)",
         "kernel_share": {n: round(step_ms[n] / total_kernel_ms, 4) for n in STEP_NAMES},
         "kernel_timing": "CUDA events between the kernels of every call, second pass of the "
                          f"same {K} steps ({instrumented_ms / K:.3f} ms/step with events)",
