@@ -310,7 +310,11 @@ __device__ int2 write_mtiles(int tid, int E, int padded, int seg_off, int bm, in
   const int first = block_exclusive_scan_1024(nt, s_tmp, &n_tiles);
   for (int j = 0; j < nt; ++j) {
     const int rows = min(per, padded - j * per);
-    mtiles[first + j] = make_int4(tid, seg_off + j * per, rows | (nt << 12), first);
+    // the tile count above bit 12 is informational (the GEMMs read the low 12
+    // bits); unsigned so that experts of more than 2^19 tiles wrap, not overflow
+    mtiles[first + j] = make_int4(tid, seg_off + j * per,
+                                  static_cast<int>(static_cast<unsigned>(rows) | (static_cast<unsigned>(nt) << 12)),
+                                  first);
   }
   // the largest tile is some expert's first one
   const int wmax = static_cast<int>(__reduce_max_sync(kFull, static_cast<unsigned>(per)));
