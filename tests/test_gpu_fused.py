@@ -59,6 +59,9 @@ def run_case(moe, w, a, top_k, renorm, rows=None, repeat=1, flags=0):
     (8, 256, 2176, 4, 2, True, "fp8"),      # I > 2048: down weights in M by default
     (70, 384, 2304, 16, 3, False, "fp8"),   # ragged rows, I > 2048
     (1000, 256, 512, 4, 2, True, "fp8"),    # 500 rows per expert: gate/up on SM pairs
+    (3, 256, 256, 1024, 4, True, "bf16"),   # the largest E: routing outside the one-CTA front
+    (500, 128, 128, 1024, 8, True, "fp8"),  # the largest E, 4000 pairs over about 980 experts
+    (50, 128, 256, 64, 40, False, "fp8"),   # k = 40 of 64
 ])
 @pytest.mark.parametrize("path", ["auto", "weights_in_m", "one_kernel"])
 def test_fused_small(gpu_lib, T, H, I, E, k, renorm, dtype, path):
