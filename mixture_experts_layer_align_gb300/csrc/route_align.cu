@@ -352,25 +352,31 @@ __global__ void __launch_bounds__(kAlignThreads, 1) route_align_small_kernel(Sma
   for (int i = tid; i < p.n_zero; i += kAlignThreads) p.zero_ints[i] = 0;
   for (int e = tid; e < E; e += kAlignThreads) s_cnt[e] = 0;
 
+  // amax |x| (FP8), 8 vector loads in flight per thread; the first batch goes
+  // out before the routing, so that its round trip overlaps the logits'
+  const uint4* xv = reinterpret_cast<const uint4*>(p.x);
+  const long long n8 = p.x != nullptr ? static_cast<long long>(T) * p.H / 8 : 0;
+  uint4 v[8];
+#pragma unroll
+  for (int u = 0; u < 8; ++u) {
+    const long long i = u * kAlignThreads + tid;
+    v[u] = i < n8 ? __ldg(xv + i) : make_uint4(0, 0, 0, 0);
+  }
   // routing, one warp per token
   for (int t = warp; t < T; t += 32)
     route_token_any(p.logits + static_cast<size_t>(t) * E, E, k, p.renorm, s_logits + warp * E,
                 s_ids + t * k, s_w + t * k, lane);
-  // amax |x| (FP8), 8 vector loads in flight per thread
   float xmax = 0.f;
-  if (p.x != nullptr) {
-    const uint4* xv = reinterpret_cast<const uint4*>(p.x);
-    const long long n8 = static_cast<long long>(T) * p.H / 8;
-    for (long long i0 = 0; i0 < n8; i0 += 8 * kAlignThreads) {
-      uint4 v[8];
+  for (long long i0 = 0; i0 < n8; i0 += 8 * kAlignThreads) {
+    if (i0 > 0) {
 #pragma unroll
       for (int u = 0; u < 8; ++u) {
         const long long i = i0 + u * kAlignThreads + tid;
         v[u] = i < n8 ? __ldg(xv + i) : make_uint4(0, 0, 0, 0);
       }
-#pragma unroll
-      for (int u = 0; u < 8; ++u) xmax = absmax8(v[u], xmax);
     }
+#pragma unroll
+    for (int u = 0; u < 8; ++u) xmax = absmax8(v[u], xmax);
   }
   xmax = warp_max(xmax);
   if (lane == 0) s_red[warp] = xmax;
