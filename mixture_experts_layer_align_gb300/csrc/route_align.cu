@@ -123,21 +123,66 @@ __device__ int2 write_mtiles(int tid, int E, int padded, int seg_off, int bm, in
 // Inside the chunk each warp owns a contiguous sub-range: per-warp counts are
 // scanned column-wise over the 32 warps, then every warp places its pairs in
 // order with __match_any_sync ranks.  The resulting order is exactly the
-// ascending pair id order within each expert.
+// ascending pair id order within each expert.  The chunk's ids are read from
+// global memory once (kept in shared memory for both passes over the chunk),
+// and CTA 0 writes the tile lists from the same prefix-sum pass as the
+// offsets.
 constexpr int kAlignThreads = 1024;
 constexpr int kAlignChunk = 1024;  // pairs per CTA (<= 65535: per-warp counts are uint16)
 constexpr int kAlignUnroll = 8;    // id loads in flight per thread in the histogram pass
 
+// Block-wide exclusive scan of three ints per thread (blockDim.x == 1024),
+// one pass of synchronisations for all three.  `tmp` holds 32 int3.
+__device__ int3 block_exclusive_scan3_1024(int3 v, int3* tmp, int3* total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int3 incl = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int nx = __shfl_up_sync(kFull, incl.x, o);
+    const int ny = __shfl_up_sync(kFull, incl.y, o);
+    const int nz = __shfl_up_sync(kFull, incl.z, o);
+    if (lane >= o) {
+      incl.x += nx;
+      incl.y += ny;
+      incl.z += nz;
+    }
+  }
+  if (lane == 31) tmp[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    int3 si = tmp[lane];
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int nx = __shfl_up_sync(kFull, si.x, o);
+      const int ny = __shfl_up_sync(kFull, si.y, o);
+      const int nz = __shfl_up_sync(kFull, si.z, o);
+      if (lane >= o) {
+        si.x += nx;
+        si.y += ny;
+        si.z += nz;
+      }
+    }
+    tmp[lane] = si;
+  }
+  __syncthreads();
+  const int3 before = warp > 0 ? tmp[warp - 1] : make_int3(0, 0, 0);
+  *total = tmp[31];
+  __syncthreads();
+  return make_int3(incl.x - v.x + before.x, incl.y - v.y + before.y, incl.z - v.z + before.z);
+}
+
 __global__ void __launch_bounds__(kAlignThreads) align_kernel(AlignParams p) {
   extern __shared__ int s_align[];
-  __shared__ int s_tmp[32];
+  __shared__ int3 s_tmp3[32];
   __shared__ float s_red[32];
+  __shared__ int s_max_rows[2];  // largest row tile of each tile list
   const int E = p.E;
   int* hist_all = s_align;
   int* hist_before = hist_all + E;
   int* base = hist_before + E;
   int* seg_off = base + E;
   uint16_t* seg = reinterpret_cast<uint16_t*>(seg_off + E);  // [32][E]
+  int* s_ids = reinterpret_cast<int*>(seg + 32 * E);         // this CTA's chunk of expert ids
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int P = p.P;
   const int cs = blockIdx.x * p.chunk;
@@ -146,17 +191,24 @@ __global__ void __launch_bounds__(kAlignThreads) align_kernel(AlignParams p) {
   const int seglen = (clen + 31) / 32;
   const int s0 = cs + warp * seglen;
   const int s1 = min(s0 + seglen, ce);
+  const bool tiles = p.mtiles != nullptr && blockIdx.x == 0;
   pdl_wait();
   pdl_trigger();
+  // the router's per-CTA maxima of |x| (read at the end) are in flight meanwhile
+  const float am_first =
+      (tiles && p.amax_partials != nullptr && tid < p.n_partials) ? __ldg(p.amax_partials + tid) : 0.f;
 
   for (int e = tid; e < E; e += kAlignThreads) {
     hist_all[e] = 0;
     hist_before[e] = 0;
   }
   for (int i = tid; i < 32 * E; i += kAlignThreads) seg[i] = 0;
+  if (tid < 2) s_max_rows[tid] = 0;
   __syncthreads();
 
   if (p.chunk_hist != nullptr) {
+    // this chunk's ids into shared memory (read by both passes below)
+    for (int q = cs + tid; q < ce; q += kAlignThreads) s_ids[q - cs] = __ldg(p.ids + q);
     // totals and the pairs before this chunk from the per-chunk histograms:
     // thread (e, r) sums chunks r, r + R, ... of expert e (R = 1024 / E
     // threads per expert, so all threads have loads in flight), then shared
@@ -174,10 +226,10 @@ __global__ void __launch_bounds__(kAlignThreads) align_kernel(AlignParams p) {
       if (tot) atomicAdd(&hist_all[e], tot);
       if (bef) atomicAdd(&hist_before[e], bef);
     }
-    __syncthreads();
   }
   // histograms of every pair, and of the pairs before this chunk (loads of
-  // kAlignUnroll rounds issued together: this pass is latency bound)
+  // kAlignUnroll rounds issued together: this pass is latency bound); the
+  // chunk's own ids are kept in shared memory on the way
   for (int p0 = 0; p.chunk_hist == nullptr && p0 < P; p0 += kAlignThreads * kAlignUnroll) {
     int ev[kAlignUnroll];
 #pragma unroll
@@ -189,6 +241,7 @@ __global__ void __launch_bounds__(kAlignThreads) align_kernel(AlignParams p) {
     for (int u = 0; u < kAlignUnroll; ++u) {
       const int q = p0 + u * kAlignThreads + tid;
       const int e = ev[u];
+      if (q >= cs && q < ce) s_ids[q - cs] = e;
       const bool valid = q < P && static_cast<unsigned>(e) < static_cast<unsigned>(E);
       const unsigned mask = __match_any_sync(kFull, valid ? e : -1);
       if (valid && lane == __ffs(mask) - 1) {
@@ -198,10 +251,11 @@ __global__ void __launch_bounds__(kAlignThreads) align_kernel(AlignParams p) {
       }
     }
   }
+  __syncthreads();
   // per-warp counts of this CTA's chunk
   for (int q0 = s0; q0 < s1; q0 += 32) {
     const int q = q0 + lane;
-    const int e = q < s1 ? p.ids[q] : -1;
+    const int e = q < s1 ? s_ids[q - cs] : -1;
     const bool valid = q < s1 && static_cast<unsigned>(e) < static_cast<unsigned>(E);
     const unsigned mask = __match_any_sync(kFull, valid ? e : -1);
     if (valid && lane == __ffs(mask) - 1) seg[warp * E + e] += static_cast<uint16_t>(__popc(mask));
@@ -209,11 +263,16 @@ __global__ void __launch_bounds__(kAlignThreads) align_kernel(AlignParams p) {
   }
   __syncthreads();
 
-  // padded offsets (one expert per thread; E <= 1024)
+  // padded offsets and the row tiles of both tile lists (one expert per
+  // thread; E <= 1024), all three prefix sums in one scan
   const int c = tid < E ? hist_all[tid] : 0;
   const int padded = (c + p.bm - 1) / p.bm * p.bm;
-  int total = 0;
-  const int off = block_exclusive_scan_1024(padded, s_tmp, &total);
+  const int nt = (p.mtiles != nullptr && padded > 0) ? (padded + p.bn_max - 1) / p.bn_max : 0;
+  const int ntw = (p.mtiles_w != nullptr && padded > 0) ? (padded + kWideRows - 1) / kWideRows : 0;
+  int3 tot;
+  const int3 ex = block_exclusive_scan3_1024(make_int3(padded, nt, ntw), s_tmp3, &tot);
+  const int off = ex.x;
+  const int total = tot.x;
   if (tid < E) {
     base[tid] = off + hist_before[tid];
     seg_off[tid] = off;
@@ -240,7 +299,7 @@ __global__ void __launch_bounds__(kAlignThreads) align_kernel(AlignParams p) {
   // stable scatter of this CTA's chunk
   for (int q0 = s0; q0 < s1; q0 += 32) {
     const int q = q0 + lane;
-    const int e = q < s1 ? p.ids[q] : -1;
+    const int e = q < s1 ? s_ids[q - cs] : -1;
     const bool valid = q < s1 && static_cast<unsigned>(e) < static_cast<unsigned>(E);
     const unsigned mask = __match_any_sync(kFull, valid ? e : -1);
     const int leader = __ffs(mask) - 1;
@@ -261,27 +320,47 @@ __global__ void __launch_bounds__(kAlignThreads) align_kernel(AlignParams p) {
 
   if (blockIdx.x != 0) return;  // uniform per block
 
-  // padding sentinels and the per-block expert map
-  if (tid < E) {
-    const int o = seg_off[tid];
-    for (int i = c; i < padded; ++i) {
-      p.sorted_ids[o + i] = P;
-      if (p.sorted_w) p.sorted_w[o + i] = 0.f;
+  // padding sentinels, spread over the CTA: thread i takes row r = i % bm of
+  // expert i / bm's padding (rows c .. padded - 1 of its segment)
+  for (int i = tid; i < E * p.bm; i += kAlignThreads) {
+    const int e = i / p.bm, r = i - e * p.bm;
+    const int ce2 = hist_all[e];
+    const int pe = (ce2 + p.bm - 1) / p.bm * p.bm;
+    if (ce2 + r < pe) {
+      p.sorted_ids[seg_off[e] + ce2 + r] = P;
+      if (p.sorted_w) p.sorted_w[seg_off[e] + ce2 + r] = 0.f;
     }
-    if (p.tile_expert)
-      for (int b = o / p.bm; b < (o + padded) / p.bm; ++b) p.tile_expert[b] = tid;
+  }
+  if (p.tile_expert && tid < E) {
+    const int o = seg_off[tid];
+    for (int b = o / p.bm; b < (o + padded) / p.bm; ++b) p.tile_expert[b] = tid;
   }
 
   if (p.mtiles != nullptr) {
-    // GEMM row tiles
-    const int2 tl = write_mtiles(tid, p.E, padded, tid < p.E ? seg_off[tid] : 0, p.bm, p.bn_max,
-                                 p.mtiles, s_tmp);
-    const int2 tw = p.mtiles_w ? write_mtiles(tid, p.E, padded, tid < p.E ? seg_off[tid] : 0, p.bm,
-                                              kWideRows, p.mtiles_w, s_tmp)
-                               : make_int2(0, 0);
+    // GEMM row tiles of this thread's expert: ceil(padded / bn) tiles of equal
+    // rows rounded up to the alignment block (the largest is the first)
+    if (nt > 0) {
+      const int per = ((padded + nt - 1) / nt + p.bm - 1) / p.bm * p.bm;
+      for (int j = 0; j < nt; ++j)
+        p.mtiles[ex.y + j] = make_int4(tid, off + j * per,
+                                       static_cast<int>(static_cast<unsigned>(min(per, padded - j * per)) |
+                                                        (static_cast<unsigned>(nt) << 12)),
+                                       ex.y);
+      atomicMax(&s_max_rows[0], per);
+    }
+    if (ntw > 0) {
+      const int per = ((padded + ntw - 1) / ntw + p.bm - 1) / p.bm * p.bm;
+      for (int j = 0; j < ntw; ++j)
+        p.mtiles_w[ex.z + j] = make_int4(tid, off + j * per,
+                                         static_cast<int>(static_cast<unsigned>(min(per, padded - j * per)) |
+                                                          (static_cast<unsigned>(ntw) << 12)),
+                                         ex.z);
+      atomicMax(&s_max_rows[1], per);
+    }
     // activation scale of x from the router's per-CTA amax values
-    float m = 0.f;
-    for (int i = tid; i < p.n_partials; i += kAlignThreads) m = fmaxf(m, p.amax_partials[i]);
+    float m = am_first;
+    for (int i = tid + kAlignThreads; i < p.n_partials; i += kAlignThreads)
+      m = fmaxf(m, p.amax_partials[i]);
     m = warp_max(m);
     if (lane == 0) s_red[warp] = m;
     __syncthreads();
@@ -289,10 +368,10 @@ __global__ void __launch_bounds__(kAlignThreads) align_kernel(AlignParams p) {
       float a = 0.f;
       for (int w = 0; w < 32; ++w) a = fmaxf(a, s_red[w]);
       p.ctrl->s_x = p.amax_partials ? scale_from_amax(a) : 1.f;
-      p.ctrl->num_mtiles = tl.x;
-      p.ctrl->max_tile_rows = tl.y;
-      p.ctrl->num_mtiles_w = tw.x;
-      p.ctrl->max_tile_rows_w = tw.y;
+      p.ctrl->num_mtiles = tot.y;
+      p.ctrl->max_tile_rows = s_max_rows[0];
+      p.ctrl->num_mtiles_w = p.mtiles_w != nullptr ? tot.z : 0;
+      p.ctrl->max_tile_rows_w = p.mtiles_w != nullptr ? s_max_rows[1] : 0;
     }
   }
 }
@@ -788,13 +867,16 @@ cudaError_t launch_route_topk(const float* logits, int T, int E, int k, int reno
 int align_chunk() { return kAlignChunk; }
 
 cudaError_t launch_align(const AlignParams& p, cudaStream_t st) {
-  const size_t smem = static_cast<size_t>(p.E) * 4 * sizeof(int) + 32u * p.E * sizeof(uint16_t);
+  // 4 ints and 32 per-warp counts per expert, then the CTA's chunk of ids
+  const size_t smem = static_cast<size_t>(p.E) * 4 * sizeof(int) + 32u * p.E * sizeof(uint16_t) +
+                      static_cast<size_t>(p.chunk) * sizeof(int);
   static thread_local int configured_device = -1;
   int dev = 0;
   cudaGetDevice(&dev);
   if (configured_device != dev) {
     cudaError_t e = checked(cudaFuncSetAttribute(align_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         4 * 1024 * 4 + 32 * 1024 * 2), "smem attribute");
+                                         4 * 1024 * 4 + 32 * 1024 * 2 + kAlignChunk * 4),
+                            "smem attribute");
     if (e != cudaSuccess) return e;
     configured_device = dev;
   }
