@@ -156,6 +156,29 @@ def test_fused_tokens_in_m_large_batch_paths(gpu_lib, T, H, I, E, k):
              flags=gpu_lib.MOE_FLAG_TOKENS_IN_M)
 
 
+# Each path switch of the layer, taken on both sides of its threshold (the
+# plan is chosen per call from the shape and the routing statistics):
+@pytest.mark.parametrize("T,H,I,E,k,dtype", [
+    (16, 256, 256, 8, 2, "fp8"),      # at most 16 tokens: one-CTA front
+    (17, 256, 256, 8, 2, "fp8"),      # 17: router + alignment kernels
+    (8, 256, 256, 256, 4, "fp8"),     # E = 256: one-CTA front
+    (8, 256, 256, 257, 4, "fp8"),     # E = 257: router + alignment kernels
+    (2048, 256, 256, 8, 2, "fp8"),    # 4096 pairs: one alignment kernel, rows gathered
+    (4097, 256, 256, 8, 1, "fp8"),    # 4097 pairs: two-pass alignment, x quantised once per token
+    (4096, 2048, 128, 16, 1, "fp8"),  # pairs x H = 8M: fp32 reductions into the combine buffer
+    (4096, 2176, 128, 16, 1, "fp8"),  # pairs x H > 8M: bf16 rows per pair, then the row sum
+    (254, 128, 512, 4, 2, "fp8"),     # 127 rows per expert on average: single-SM gate/up tiles
+    (256, 128, 512, 4, 2, "fp8"),     # 128 rows per expert on average: SM pairs
+    (64, 256, 2048, 4, 2, "fp8"),     # I = 2048: down GEMM with tokens in M
+    (64, 256, 2176, 4, 2, "fp8"),     # I = 2176: down GEMM with the weights in M
+    (17, 256, 256, 8, 2, "bf16"),     # the bf16 path past the one-CTA front
+])
+def test_fused_path_boundaries(gpu_lib, T, H, I, E, k, dtype):
+    w = inputs.make_weights(H, I, E, dtype, seed=T + E)
+    a = inputs.make_activations(T, H, E, "uniform", seed=T + E)
+    run_case(gpu_lib, w, a, k, True, rows=None)
+
+
 def test_fused_zipf_skew(gpu_lib):
     T, H, I, E, k = 300, 256, 256, 64, 8
     w = inputs.make_weights(H, I, E, "fp8", seed=5)
