@@ -58,6 +58,10 @@ def parse():
                     help="first-call vs steady-state time for every T in 1..--max-tokens "
                          "in one process, plus CUDA-graph capture per T bucket")
     ap.add_argument("--max-tokens", type=int, default=8192)
+    ap.add_argument("--tp-sweep", action="store_true",
+                    help="per-rank device time of the layer sharded over the intermediate "
+                         "size for W = 1..8 ranks, the shards run one after another on this "
+                         "GPU (tensor-parallel row; the all-reduce itself is not timed)")
     ap.add_argument("--cta-trace", action="store_true",
                     help="per-CTA timeline of the two expert GEMMs (MOE_DEBUG_TRACE stamps: "
                          "entry, inputs ready, first stage landed, exit) for the workload's T "
@@ -1030,6 +1034,116 @@ def run_rope(args, rank, local_rank):
     print(json.dumps(line), flush=True)
 
 
+def run_tp_sweep(args, rank, local_rank):
+    """Tensor-parallel shards over the intermediate size, timed on one GPU.
+
+    For W ranks every rank holds I/W of each expert's gate, up and down
+    weights and runs the layer as two library calls with an all-reduce (MAX)
+    of one fp32 word between them and an all-reduce (SUM) of the output after.
+    Here the W shards run one after another on this GPU: the W gate/up calls
+    back to back, the MAX over the W words (not timed), the W down calls back
+    to back.  us_per_rank = device time of the two timed phases / W, i.e. what
+    one GPU of the W-way group spends in the layer without the collectives.
+    Two copies of every shard alternate so that no call finds its weights in
+    L2 from the previous one."""
+    import torch
+    import mixture_experts_layer_align_gb300 as moe
+    from mixture_experts_layer_align_gb300 import inputs
+    from mixture_experts_layer_align_gb300 import tp
+
+    if rank != 0:
+        return
+    moe.load()
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    plan = [("decode_e8_top2", (1, 8, 64), (1, 2, 4, 8)),
+            ("skewed_e256", (8, 128), (1, 2, 4, 8)),
+            ("prefill_e128_uniform", (2048, 8192), (1, 2, 3, 6))]
+    if args.workload != "decode_e8_top2":
+        plan = [p for p in plan if p[0] == args.workload] or plan
+    reps = max(5, min(args.steps, 20))
+    rows = []
+    for wl, Ts, Ws in plan:
+        cfg = inputs.workload(wl)
+        H, I, E, k = cfg["H"], cfg["I"], cfg["E"], cfg["top_k"]
+        w = inputs.make_weights(H, I, E, cfg["dtype"], seed=0, device=dev)
+        for W in Ws:
+            if (I // W) % 128 != 0 or I % W != 0:
+                continue
+            shards = [[tp.shard_weights(w.w13, w.w2, r, W) for r in range(W)] for _ in range(2)]
+            for T in Ts:
+                a = inputs.make_activations(T, H, E, cfg["routing"], seed=0, device=dev)
+                outs = [torch.empty(T, H, dtype=torch.bfloat16, device=dev) for _ in range(W)]
+                wss = [moe.alloc_workspace(T, H, I // W, E, k, moe.MOE_DT_FP8_E4M3, dev)
+                       for _ in range(W)]
+                words = [moe.h_amax_view(ws_) for ws_ in wss]
+                ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+                per = []
+                for it in range(reps + 3):
+                    sh = shards[it % 2]
+                    # hold the GPU for ~1 ms so that the host has enqueued the
+                    # phase's calls before its first kernel may start: the
+                    # events then see device time, not the host's enqueue rate
+                    torch.cuda._sleep(2_000_000)
+                    ev[0].record()
+                    for r in range(W):
+                        moe.moe_fused_forward_gate_up(a.x, a.logits, sh[r][0], sh[r][1],
+                                                      w.w13_scale, w.w2_scale, k, True,
+                                                      outs[r], wss[r])
+                    ev[1].record()
+                    m = torch.stack(words).amax()  # the all-reduce (MAX), not timed
+                    for wd in words:
+                        wd.copy_(m.reshape(1))
+                    torch.cuda._sleep(2_000_000)
+                    ev[2].record()
+                    for r in range(W):
+                        moe.moe_fused_forward_down(a.x, a.logits, sh[r][0], sh[r][1],
+                                                   w.w13_scale, w.w2_scale, k, True,
+                                                   outs[r], wss[r])
+                    ev[3].record()
+                    torch.cuda.synchronize()
+                    if it >= 3:
+                        per.append((ev[0].elapsed_time(ev[1]) + ev[2].elapsed_time(ev[3])) * 1e3 / W)
+                for ws_ in wss:
+                    if moe.moe_check_status(ws_) != 0:
+                        raise RuntimeError("device status")
+                per.sort()
+                row = {"workload": wl, "T": T, "W": W, "I_per_rank": I // W,
+                       "us_per_rank": round(per[len(per) // 2], 2)}
+                if W == 1:
+                    # the same layer as one call (no split, no collectives)
+                    ws1 = moe.alloc_workspace(T, H, I, E, k, moe.MOE_DT_FP8_E4M3, dev)
+                    out1 = torch.empty(T, H, dtype=torch.bfloat16, device=dev)
+                    ws_w = [w, inputs.Weights(w.w13.clone(), w.w2.clone(), w.w13_scale,
+                                              w.w2_scale, w.dtype, H, I, E)]
+
+                    def one(i):
+                        ww = ws_w[i % 2]
+                        moe.moe_fused_forward(a.x, a.logits, ww.w13, ww.w2, ww.w13_scale,
+                                              ww.w2_scale, k, True, out=out1, workspace=ws1)
+                    us1 = sorted(time_calls(one, 20))
+                    row["one_call_us"] = round(us1[len(us1) // 2], 2)
+                    del ws_w
+                rows.append(row)
+            del shards
+            torch.cuda.empty_cache()
+        del w
+        torch.cuda.empty_cache()
+    for r_ in rows:
+        base = next(x["us_per_rank"] for x in rows
+                    if x["workload"] == r_["workload"] and x["T"] == r_["T"] and x["W"] == 1)
+        r_["vs_one_rank"] = round(base / r_["us_per_rank"], 3)
+        r_["of_ideal"] = round(base / r_["W"] / r_["us_per_rank"], 3)
+    print(json.dumps({"metric": "per-rank layer device time, tensor-parallel shards over I "
+                                "(ranks run one after another on one GPU)",
+                      "unit": "us", "timing": "CUDA events around the W gate/up calls and "
+                      "around the W down calls, each phase enqueued behind a ~1 ms GPU sleep "
+                      "(the MAX of the h scale word between them and the output all-reduce "
+                      "are not timed), median over %d layers; one_call_us: the unsharded "
+                      "layer as one call, blocks of back-to-back calls" % reps,
+                      "rows": rows}), flush=True)
+
+
 def run_cta_trace(args, rank, local_rank):
     """Per-CTA %globaltimer stamps of the two expert GEMMs of one call per T,
     relative to the kernel's first CTA entry (us): min/median/max of the
@@ -1090,6 +1204,9 @@ def main():
         return
     if args.shape_sweep:
         run_shape_sweep(args, rank, local_rank)
+        return
+    if args.tp_sweep:
+        run_tp_sweep(args, rank, local_rank)
         return
     if args.impl == "reference":
         run_reference(args, rank, world)
