@@ -179,6 +179,33 @@ def test_fused_path_boundaries(gpu_lib, T, H, I, E, k, dtype):
     run_case(gpu_lib, w, a, k, True, rows=None)
 
 
+# Shapes drawn once with random.Random(20261203): E from 1 to 96, k <= min(E, 8),
+# H and I multiples of 128 up to 1024 / 1280, T from 1 to 2500, FP8 or bf16,
+# uniform or Zipf routing, with and without renormalisation (the oracle's work
+# kept under 4 G multiply-adds per case).
+RANDOM_SHAPES = [
+    (16, 384, 640, 3, 1, False, "fp8", "uniform"), (100, 640, 1152, 8, 3, False, "bf16", "uniform"),
+    (100, 1024, 128, 1, 1, True, "fp8", "zipf"), (17, 640, 640, 8, 5, True, "fp8", "zipf"),
+    (2500, 384, 256, 2, 2, False, "fp8", "uniform"), (100, 640, 1280, 3, 2, True, "bf16", "uniform"),
+    (2, 1024, 896, 96, 1, True, "fp8", "uniform"), (7, 1024, 384, 96, 7, True, "fp8", "zipf"),
+    (3, 512, 256, 32, 5, True, "fp8", "uniform"), (7, 640, 512, 13, 4, True, "bf16", "uniform"),
+    (17, 768, 512, 1, 1, False, "fp8", "zipf"), (17, 384, 768, 32, 6, True, "fp8", "uniform"),
+    (2, 128, 384, 96, 8, False, "fp8", "uniform"), (16, 128, 1152, 1, 1, False, "fp8", "zipf"),
+    (1500, 384, 1152, 8, 1, True, "fp8", "uniform"), (2, 384, 128, 96, 1, False, "fp8", "zipf"),
+    (17, 384, 1152, 2, 2, True, "fp8", "zipf"), (100, 128, 640, 13, 8, False, "bf16", "uniform"),
+    (100, 1024, 512, 2, 2, False, "fp8", "uniform"), (1, 896, 256, 32, 8, False, "fp8", "uniform"),
+    (1, 768, 1024, 2, 2, False, "fp8", "zipf"), (17, 768, 896, 96, 2, True, "bf16", "zipf"),
+    (7, 896, 256, 96, 2, True, "fp8", "uniform"), (3, 384, 1280, 2, 2, True, "bf16", "uniform"),
+]
+
+
+@pytest.mark.parametrize("T,H,I,E,k,renorm,dtype,routing", RANDOM_SHAPES)
+def test_fused_random_shapes(gpu_lib, T, H, I, E, k, renorm, dtype, routing):
+    w = inputs.make_weights(H, I, E, dtype, seed=T * 7 + I)
+    a = inputs.make_activations(T, H, E, routing, seed=T * 7 + I)
+    run_case(gpu_lib, w, a, k, renorm, rows=None)
+
+
 def test_fused_zipf_skew(gpu_lib):
     T, H, I, E, k = 300, 256, 256, 64, 8
     w = inputs.make_weights(H, I, E, "fp8", seed=5)
