@@ -17,7 +17,7 @@ pytestmark = pytest.mark.gpu
     (129, 5, 16, 64), (4096, 32, 128, 8192), (8192, 8, 32, 8192),
     (20000, 3, 256, 2048),   # two launches, one head vector per warp iteration
     (12000, 40, 16, 64),     # two launches, a partial group of heads
-    (2000, 1024, 8, 64),     # two launches with the fold kernel between them
+    (2000, 1024, 8, 64),     # two launches, 32 head vectors of 8 per warp iteration
 ])
 def test_inv_rope_quant_matches_oracle(gpu_lib, T, NH, D, max_pos):
     r = inputs.make_rope_inputs(T, NH, D, max_pos, seed=T)
@@ -27,6 +27,17 @@ def test_inv_rope_quant_matches_oracle(gpu_lib, T, NH, D, max_pos):
     assert gpu_lib.moe_check_status(scratch) == 0
     assert np.array_equal(scales.cpu().numpy(), ref["scales"])
     assert np.array_equal(codes.cpu().numpy(), ref["codes"])
+
+
+# More shapes drawn once with random.Random(47): head sizes 8..256, 1..512 heads,
+# T up to 9000, tables of 1..8192 positions (max_pos = 1: every position is 0).
+@pytest.mark.parametrize("T,NH,D,max_pos", [
+    (300, 2, 32, 8192), (17, 33, 64, 8192), (1217, 100, 64, 1), (1, 1, 64, 1),
+    (1217, 33, 8, 1000), (1217, 7, 16, 8192), (2, 512, 32, 1), (3000, 33, 128, 64),
+    (1217, 33, 128, 8192), (9000, 7, 16, 1),
+])
+def test_inv_rope_quant_random_shapes(gpu_lib, T, NH, D, max_pos):
+    test_inv_rope_quant_matches_oracle(gpu_lib, T, NH, D, max_pos)
 
 
 def test_zero_head_and_repeat_calls(gpu_lib):

@@ -41,6 +41,18 @@ def test_route_topk_parity(gpu_lib, T, E, k, kind, renorm):
     np.testing.assert_allclose(w.cpu().numpy(), ref_w, rtol=W_RTOL, atol=W_ATOL)
 
 
+# More router cases drawn once with random.Random(31): E 1..1024, k up to 32,
+# T up to 5000, every logit kind (ties, Zipf bias, |logits| ~ 1e4).
+@pytest.mark.parametrize("T,E,k,kind", [
+    (5, 1, 1, "large"), (1, 7, 6, "ties"), (31, 2, 1, "ties"), (1, 1024, 3, "ties"),
+    (5000, 31, 18, "large"), (5, 31, 19, "normal"), (1000, 1, 1, "ties"), (4096, 31, 11, "zipf"),
+    (64, 257, 16, "ties"), (1, 100, 4, "ties"), (64, 33, 9, "ties"), (5, 100, 2, "large"),
+])
+@pytest.mark.parametrize("renorm", [True, False])
+def test_route_topk_random_cases(gpu_lib, T, E, k, kind, renorm):
+    test_route_topk_parity(gpu_lib, T, E, k, kind, renorm)
+
+
 def test_route_zero_tokens(gpu_lib):
     lg = torch.zeros(0, 8, device="cuda")
     ids, w = gpu_lib.moe_route_topk(lg, 2, True)
@@ -68,6 +80,18 @@ def test_align_parity(gpu_lib, T, k, E, bm, kind):
     assert np.array_equal(res["tile_expert"][:n // bm].cpu().numpy(), ref["tile_expert"])
     # entries past the padded end are not written
     assert torch.all(res["sorted_ids"][n:] == -1)
+
+
+# More alignment cases drawn once with random.Random(31): E 1..1024, k up to 8,
+# T up to 7000 (up to 49,000 pairs), block_m from 1 to 256.
+@pytest.mark.parametrize("T,k,E,bm,kind", [
+    (7000, 4, 64, 33, "zipf"), (100, 4, 256, 128, "normal"), (100, 1, 1024, 16, "ties"),
+    (600, 7, 256, 128, "zipf"), (4100, 4, 256, 1, "ties"), (1, 5, 8, 2, "normal"),
+    (4100, 1, 1, 1, "zipf"), (100, 5, 513, 128, "normal"), (9, 2, 3, 256, "ties"),
+    (7000, 7, 1024, 1, "zipf"), (1, 2, 3, 256, "zipf"), (9, 1, 3, 16, "normal"),
+])
+def test_align_random_cases(gpu_lib, T, k, E, bm, kind):
+    test_align_parity(gpu_lib, T, k, E, bm, kind)
 
 
 def test_align_out_of_range_ids_are_skipped(gpu_lib):
