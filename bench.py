@@ -679,41 +679,52 @@ def run_ours(args, rank, local_rank, world):
     if not args.no_e2e:
         host = {T: (acts[T].x.cpu().pin_memory(), acts[T].logits.cpu().pin_memory(),
                     torch.empty(T, H, dtype=torch.bfloat16).pin_memory()) for T in Ts}
-        dx = {T: torch.empty_like(acts[T].x) for T in Ts}
-        dl = {T: torch.empty_like(acts[T].logits) for T in Ts}
         h2d = sum(T * H * 2 + T * E * 4 for T in Ts)
         d2h = sum(T * H * 2 for T in Ts)
 
-        # Copies run on a side stream, as a serving loop would issue them: the
-        # step's inputs go up first (each call waits for its own), each result
-        # comes back as soon as its call is done, and a call's input buffers
-        # are refilled only after that call of the previous step has run.
+        # Copies run on two side streams, as a serving loop would issue them:
+        # two sets of device buffers alternate step to step, the next step's
+        # inputs go up while this step runs, and the step's results come back
+        # once its calls are done.  The compute stream waits twice per step (its
+        # inputs are up; the results last held in this set have left) and
+        # records one event, so that nothing between two calls of a step keeps
+        # one call's first kernel from overlapping the previous call's last.
         compute = torch.cuda.current_stream(dev)
-        copier = torch.cuda.Stream(device=dev)
-        in_ready = {T: torch.cuda.Event() for T in Ts}
-        call_done = {T: torch.cuda.Event() for T in Ts}
-        for T in Ts:
-            call_done[T].record(compute)
+        up = torch.cuda.Stream(device=dev)
+        down = torch.cuda.Stream(device=dev)
+        dx = [{T: torch.empty_like(acts[T].x) for T in Ts} for _ in range(2)]
+        dl = [{T: torch.empty_like(acts[T].logits) for T in Ts} for _ in range(2)]
+        do = [{T: torch.empty(T, H, dtype=torch.bfloat16, device=dev) for T in Ts}
+              for _ in range(2)]
+        inputs_up = [torch.cuda.Event() for _ in range(2)]
+        step_done = [torch.cuda.Event() for _ in range(2)]
+        results_down = [torch.cuda.Event() for _ in range(2)]
+        for b in range(2):
+            step_done[b].record(compute)
+            results_down[b].record(compute)
 
         def e2e_step(s):
-            with torch.cuda.stream(copier):
+            b = s % 2
+            with torch.cuda.stream(up):
+                up.wait_event(step_done[b])  # the step that last used this set has run
                 for T in Ts:
-                    copier.wait_event(call_done[T])
                     hx, hl, _ = host[T]
-                    dx[T].copy_(hx, non_blocking=True)
-                    dl[T].copy_(hl, non_blocking=True)
-                    in_ready[T].record(copier)
+                    dx[b][T].copy_(hx, non_blocking=True)
+                    dl[b][T].copy_(hl, non_blocking=True)
+                inputs_up[b].record(up)
+            compute.wait_event(inputs_up[b])
+            compute.wait_event(results_down[b])
             for j, T in enumerate(Ts):
                 ww = copies[(s * calls_per_step + j) % len(copies)]
-                compute.wait_event(in_ready[T])
-                moe.moe_fused_forward(dx[T], dl[T], ww.w13, ww.w2, ww.w13_scale, ww.w2_scale, k,
-                                      True, out=outs[T], workspace=wss[T], debug_flags=flags)
-                call_done[T].record(compute)
-                with torch.cuda.stream(copier):
-                    copier.wait_event(call_done[T])
-                    host[T][2].copy_(outs[T], non_blocking=True)
-            # the step ends when its last result has reached the host buffer
-            compute.wait_stream(copier)
+                moe.moe_fused_forward(dx[b][T], dl[b][T], ww.w13, ww.w2, ww.w13_scale,
+                                      ww.w2_scale, k, True, out=do[b][T], workspace=wss[T],
+                                      debug_flags=flags)
+            step_done[b].record(compute)
+            with torch.cuda.stream(down):
+                down.wait_event(step_done[b])
+                for T in Ts:
+                    host[T][2].copy_(do[b][T], non_blocking=True)
+                results_down[b].record(down)
 
         for i in range(3):
             e2e_step(i)
@@ -723,8 +734,10 @@ def run_ours(args, rank, local_rank, world):
         s0 = torch.cuda.Event(enable_timing=True)
         s1 = torch.cuda.Event(enable_timing=True)
         s0.record()
+        up.wait_stream(compute)  # the first step's uploads start inside the timed region
         for s in range(K):
             e2e_step(s)
+        compute.wait_stream(down)  # the last results have reached the host
         s1.record()
         torch.cuda.synchronize()
         e_ms = max_over_ranks(s0.elapsed_time(s1), dist, dev)
