@@ -599,7 +599,7 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
     {
       const int nvec = kBF16 ? H / 8 : H / 16;  // 16-byte outputs per row
       uint4* xs = static_cast<uint4*>(p.xs);
-      const float sx = sh.s_x, rsx = __frcp_rn(sx);
+      const E4m3Div dx = e4m3_div(sh.s_x);
       const int chunk = q1 - q0;
       const int n_items = chunk * nvec;
       for (int i0 = 0; i0 < n_items; i0 += 4 * static_cast<int>(kEpiThreads)) {
@@ -631,8 +631,8 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
           if (kBF16) {
             xs[dst[u]] = v[u][0];
           } else {
-            const uint2 lo = quant8(v[u][0], sx, rsx);
-            const uint2 hi = quant8(v[u][1], sx, rsx);
+            const uint2 lo = quant8(v[u][0], dx);
+            const uint2 hi = quant8(v[u][1], dx);
             xs[dst[u]] = make_uint4(lo.x, lo.y, hi.x, hi.y);
           }
         }
@@ -789,7 +789,7 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
     if (ok && !kBF16) {
       s_h = scale_from_amax(__uint_as_float(ld_acquire(&ctrl->amax_h)));
       if (c == 0 && etid == 0) ctrl->s_h = s_h;
-      const float rs = __frcp_rn(s_h);
+      const E4m3Div dh = e4m3_div(s_h);
       const long long n16 = static_cast<long long>(sh.total_rows) * I / 16;
       const float4* src = static_cast<const float4*>(p.h);
       uint4* dst = reinterpret_cast<uint4*>(p.hq);
@@ -808,8 +808,8 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
         for (int u = 0; u < 4; ++u) {
           const long long i = i0 + u * stride;
           if (i < n16)
-            dst[i] = make_uint4(quant4(v[u][0], s_h, rs), quant4(v[u][1], s_h, rs),
-                                quant4(v[u][2], s_h, rs), quant4(v[u][3], s_h, rs));
+            dst[i] = make_uint4(quant4(v[u][0], dh), quant4(v[u][1], dh),
+                                quant4(v[u][2], dh), quant4(v[u][3], dh));
         }
       }
       fence_proxy_async_global();  // the codes are read by other CTAs' TMA

@@ -399,39 +399,57 @@ __device__ __forceinline__ float scale_from_amax(float amax) {
   return amax > 0.f ? __fdiv_rn(amax, 448.f) : 1.f;
 }
 
-// v / s correctly rounded to fp32, as far as its E4M3 code is concerned.
-// With rs = 1/s correctly rounded, q = v * rs (one rounding) lies within 2.5
-// ulp of the rounded quotient.  E4M3 keeps 3 of the 23 mantissa bits, so when
-// the 20 bits below them are more than 8 ulp away from the half-way pattern
-// (and q is zero or in E4M3's normal range, |q| >= 2^-6) the quotient and q
-// round to the same code and the multiply stands in for the division;
-// otherwise (a few percent of typical activations) the IEEE division runs.
-__device__ __forceinline__ float div_for_e4m3(float v, float s, float rs) {
-  const float q = __fmul_rn(v, rs);
-  const uint32_t b = __float_as_uint(q) & 0x7fffffffu;
-  const int d = static_cast<int>(b & 0xfffffu) - 0x80000;
-  if (b == 0u || ((b >> 23) >= 121u && (d > 8 || d < -8))) return q;
-  return __fdiv_rn(v, s);
+// Divisor of the E4M3 codes E4M3(RN(v / s)): s and two reciprocals bracketing
+// 1/s, rlo = RN(RN(1/s) (1 - 2^-20)) and rhi = RN(RN(1/s) (1 + 2^-20)).
+// Each rounding moves a value by a factor within 1 +- 2^-24, so for v != 0
+//   |RN(v rlo)| <= |v/s| (1 - 2^-20)(1 + 2^-24)^3 < |v/s| (1 - 2^-24) <= |RN(v/s)|
+// and likewise |RN(v/s)| < |RN(v rhi)| (quotients below 2^-126, where the
+// relative bounds lapse, have code zero at both ends and in between).  The
+// conversion to E4M3 (round to nearest even, saturating) is monotonic, so when
+// the two products give the same code, the IEEE quotient between them has it
+// too; otherwise (within 2^-20 of a rounding boundary: about one value in
+// 2^16) the division runs.  A scale whose reciprocal overflows brackets
+// nothing (rlo = 0, rhi = inf) and always takes the division.
+struct E4m3Div {
+  float s, rlo, rhi;
+};
+
+__device__ __forceinline__ E4m3Div e4m3_div(float s) {
+  const float rs = __frcp_rn(s);
+  E4m3Div d;
+  d.s = s;
+  if (isinf(rs)) {
+    d.rlo = 0.f;
+    d.rhi = __int_as_float(0x7f800000);
+  } else {
+    d.rlo = __fmul_rn(rs, 1.f - 0x1p-20f);
+    d.rhi = __fmul_rn(rs, 1.f + 0x1p-20f);
+  }
+  return d;
 }
 
-__device__ __forceinline__ uint16_t quant2(float a, float b, float s, float rs) {
-  return cvt_e4m3x2(div_for_e4m3(a, s, rs), div_for_e4m3(b, s, rs));
+// E4M3 codes of RN(a / s) and RN(b / s), a in the low byte.
+__device__ __forceinline__ uint16_t quant2(float a, float b, const E4m3Div& d) {
+  const uint16_t lo = cvt_e4m3x2(__fmul_rn(a, d.rlo), __fmul_rn(b, d.rlo));
+  const uint16_t hi = cvt_e4m3x2(__fmul_rn(a, d.rhi), __fmul_rn(b, d.rhi));
+  if (lo == hi) return lo;
+  return cvt_e4m3x2(__fdiv_rn(a, d.s), __fdiv_rn(b, d.s));
 }
 
-// 8 bf16 (one uint4) / s -> 8 E4M3 codes (two uint32); rs = __frcp_rn(s).
-__device__ __forceinline__ uint2 quant8(uint4 v, float s, float rs) {
+// 8 bf16 (one uint4) / s -> 8 E4M3 codes (two uint32).
+__device__ __forceinline__ uint2 quant8(uint4 v, const E4m3Div& d) {
   uint2 r;
-  r.x = static_cast<uint32_t>(quant2(bf16_lo(v.x), bf16_hi(v.x), s, rs)) |
-        (static_cast<uint32_t>(quant2(bf16_lo(v.y), bf16_hi(v.y), s, rs)) << 16);
-  r.y = static_cast<uint32_t>(quant2(bf16_lo(v.z), bf16_hi(v.z), s, rs)) |
-        (static_cast<uint32_t>(quant2(bf16_lo(v.w), bf16_hi(v.w), s, rs)) << 16);
+  r.x = static_cast<uint32_t>(quant2(bf16_lo(v.x), bf16_hi(v.x), d)) |
+        (static_cast<uint32_t>(quant2(bf16_lo(v.y), bf16_hi(v.y), d)) << 16);
+  r.y = static_cast<uint32_t>(quant2(bf16_lo(v.z), bf16_hi(v.z), d)) |
+        (static_cast<uint32_t>(quant2(bf16_lo(v.w), bf16_hi(v.w), d)) << 16);
   return r;
 }
 
-// 4 fp32 / s -> 4 E4M3 codes (one uint32); rs = __frcp_rn(s).
-__device__ __forceinline__ uint32_t quant4(float4 v, float s, float rs) {
-  return static_cast<uint32_t>(quant2(v.x, v.y, s, rs)) |
-         (static_cast<uint32_t>(quant2(v.z, v.w, s, rs)) << 16);
+// 4 fp32 / s -> 4 E4M3 codes (one uint32).
+__device__ __forceinline__ uint32_t quant4(float4 v, const E4m3Div& d) {
+  return static_cast<uint32_t>(quant2(v.x, v.y, d)) |
+         (static_cast<uint32_t>(quant2(v.z, v.w, d)) << 16);
 }
 
 __device__ __forceinline__ void red_add_f32(float* p, float v) {

@@ -75,7 +75,8 @@ __global__ void __launch_bounds__(kRopeThreads)
                      const float* __restrict__ cos_t, const float* __restrict__ sin_t, int T,
                      int NH, int D, int max_pos, unsigned* __restrict__ gmax,
                      float* __restrict__ scales, uint8_t* __restrict__ codes, Ctrl* ctrl) {
-  extern __shared__ unsigned s_head[];  // [NH]: max|y| bits, or the scales
+  // [NH]: max|y| bits; or the scales, then [2][NH] their bracketing reciprocals
+  extern __shared__ unsigned s_head[];
   __shared__ int s_bad;
   pdl_wait();
   pdl_trigger();
@@ -84,6 +85,9 @@ __global__ void __launch_bounds__(kRopeThreads)
       const float a = __uint_as_float(__ldcg(gmax + h));
       const float sc = a > 0.f ? __fdiv_rn(a, 448.f) : 1.f;
       s_head[h] = __float_as_uint(sc);
+      const E4m3Div d = e4m3_div(sc);
+      s_head[NH + h] = __float_as_uint(d.rlo);
+      s_head[2 * NH + h] = __float_as_uint(d.rhi);
       if (blockIdx.x == 0) scales[h] = sc;
     } else {
       s_head[h] = 0u;
@@ -135,13 +139,13 @@ __global__ void __launch_bounds__(kRopeThreads)
         rotate8(v[u], c, s, y);
         if (kQuant) {
           if (h < NH) {
-            const float sc = __uint_as_float(s_head[h]);
-            const float rsc = __frcp_rn(sc);  // codes of y / sc (see div_for_e4m3)
+            const E4m3Div d{__uint_as_float(s_head[h]), __uint_as_float(s_head[NH + h]),
+                            __uint_as_float(s_head[2 * NH + h])};
             uint2 q;
-            q.x = static_cast<uint32_t>(quant2(y[0], y[1], sc, rsc)) |
-                  (static_cast<uint32_t>(quant2(y[2], y[3], sc, rsc)) << 16);
-            q.y = static_cast<uint32_t>(quant2(y[4], y[5], sc, rsc)) |
-                  (static_cast<uint32_t>(quant2(y[6], y[7], sc, rsc)) << 16);
+            q.x = static_cast<uint32_t>(quant2(y[0], y[1], d)) |
+                  (static_cast<uint32_t>(quant2(y[2], y[3], d)) << 16);
+            q.y = static_cast<uint32_t>(quant2(y[4], y[5], d)) |
+                  (static_cast<uint32_t>(quant2(y[6], y[7], d)) << 16);
             *reinterpret_cast<uint2*>(codes + (row0 + h) * D + c8 * 8) = q;
           }
         } else {
@@ -173,7 +177,8 @@ constexpr int kCoopBatch = 2;      // warp iterations of head vectors per item
 // the cos/sin entries of those positions), with 2 kB 16-byte loads of x per
 // lane in flight.  kQuant = false: the CTA's per-head maxima of |y| into
 // s_head (max |y| bits), a position outside the tables into *bad_out.
-// kQuant = true: codes with the scales in s_head (fp32 bits).
+// kQuant = true: codes with the scales in s_head (fp32 bits), followed by
+// their bracketing reciprocals (two arrays of NH, see E4m3Div).
 template <bool kQuant, int kB>
 __device__ __forceinline__ void rope_items_pass(const __nv_bfloat16* __restrict__ x,
                                           const int32_t* __restrict__ pos,
@@ -235,13 +240,13 @@ __device__ __forceinline__ void rope_items_pass(const __nv_bfloat16* __restrict_
         rotate8(v[it][u], cs[it], sn[it], y);
         if (kQuant) {
           if (h < NH) {
-            const float sc = __uint_as_float(s_head[h]);
-            const float rsc = __frcp_rn(sc);  // codes of y / sc (see div_for_e4m3)
+            const E4m3Div d{__uint_as_float(s_head[h]), __uint_as_float(s_head[NH + h]),
+                            __uint_as_float(s_head[2 * NH + h])};
             uint2 q;
-            q.x = static_cast<uint32_t>(quant2(y[0], y[1], sc, rsc)) |
-                  (static_cast<uint32_t>(quant2(y[2], y[3], sc, rsc)) << 16);
-            q.y = static_cast<uint32_t>(quant2(y[4], y[5], sc, rsc)) |
-                  (static_cast<uint32_t>(quant2(y[6], y[7], sc, rsc)) << 16);
+            q.x = static_cast<uint32_t>(quant2(y[0], y[1], d)) |
+                  (static_cast<uint32_t>(quant2(y[2], y[3], d)) << 16);
+            q.y = static_cast<uint32_t>(quant2(y[4], y[5], d)) |
+                  (static_cast<uint32_t>(quant2(y[6], y[7], d)) << 16);
             *reinterpret_cast<uint2*>(codes + (row0 + h) * D + c8 * 8) = q;
           }
         } else {
@@ -300,7 +305,8 @@ __global__ void __launch_bounds__(kCoopThreads, 1)
                      const float* __restrict__ cos_t, const float* __restrict__ sin_t, int T,
                      int NH, int D, int max_pos, float* __restrict__ partials,
                      float* __restrict__ scales, uint8_t* __restrict__ codes, Ctrl* ctrl) {
-  extern __shared__ unsigned s_head[];  // [NH]: max|y| bits, then the scales
+  // [NH]: max|y| bits, then the scales, followed by [2][NH] reciprocals
+  extern __shared__ unsigned s_head[];
   __shared__ int s_bad;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
   const int G = static_cast<int>(gridDim.x);
@@ -318,6 +324,12 @@ __global__ void __launch_bounds__(kCoopThreads, 1)
   // every CTA folds the per-CTA maxima into the scales
   rope_fold_heads(partials, G, NH, s_head, blockIdx.x == 0 ? scales : nullptr,
                   blockIdx.x == 0 ? ctrl : nullptr);
+  __syncthreads();
+  for (int h = threadIdx.x; h < NH; h += blockDim.x) {
+    const E4m3Div d = e4m3_div(__uint_as_float(s_head[h]));
+    s_head[NH + h] = __float_as_uint(d.rlo);
+    s_head[2 * NH + h] = __float_as_uint(d.rhi);
+  }
   __syncthreads();
   rope_items_pass<true, kCoopBatch>(x, pos, cos_t, sin_t, T, NH, D, max_pos, s_head, codes,
                                     nullptr);
@@ -340,6 +352,22 @@ cudaError_t launch_inv_rope_quant(const __nv_bfloat16* x, const int32_t* pos, co
                                   uint8_t* codes, float* scales, Ctrl* ctrl, float* partials,
                                   int num_sms, cudaStream_t st) {
   const size_t smem = static_cast<size_t>(NH) * sizeof(float);
+  const size_t smem_q = 3 * smem;  // scales and their two reciprocals
+  static thread_local int configured_device = -1;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (configured_device != dev) {
+    const int max_q = 3 * 4096 * static_cast<int>(sizeof(float));
+    cudaError_t e = checked(cudaFuncSetAttribute(rope_pass_kernel<true>,
+                                                 cudaFuncAttributeMaxDynamicSharedMemorySize, max_q),
+                            "smem attribute");
+    if (e == cudaSuccess)
+      e = checked(cudaFuncSetAttribute(rope_coop_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       max_q),
+                  "smem attribute");
+    if (e != cudaSuccess) return e;
+    configured_device = dev;
+  }
   // small inputs: at most two rounds of two items per warp on one CTA per SM
   const int gh = (32 / (D / 8)) * kCoopBatch;
   const long long items = static_cast<long long>(T) * ((NH + gh - 1) / gh);
@@ -350,7 +378,7 @@ cudaError_t launch_inv_rope_quant(const __nv_bfloat16* x, const int32_t* pos, co
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = dim3(g);
     cfg.blockDim = dim3(kCoopThreads);
-    cfg.dynamicSmemBytes = smem;
+    cfg.dynamicSmemBytes = smem_q;
     cfg.stream = st;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeCooperative;  // the CTAs synchronise once
@@ -371,7 +399,7 @@ cudaError_t launch_inv_rope_quant(const __nv_bfloat16* x, const int32_t* pos, co
                  sin_t, T, NH, D, max_pos, gmax, static_cast<float*>(nullptr),
                  static_cast<uint8_t*>(nullptr), static_cast<Ctrl*>(nullptr));
   if (e != cudaSuccess) return e;
-  return launch_pdl(rope_pass_kernel<true>, dim3(grid), dim3(kRopeThreads), smem, st, x, pos,
+  return launch_pdl(rope_pass_kernel<true>, dim3(grid), dim3(kRopeThreads), smem_q, st, x, pos,
                     cos_t, sin_t, T, NH, D, max_pos, gmax, scales, codes, ctrl);
 }
 

@@ -591,7 +591,7 @@ __global__ void __launch_bounds__(256)
   const int nwarps = gridDim.x * (blockDim.x >> 5);
   const int w0 = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   const float s = ctrl->s_x;
-  const float rs = __frcp_rn(s);
+  const E4m3Div ds = e4m3_div(s);
   const int n16 = H / 16;
   const uint4 zero = make_uint4(0, 0, 0, 0);
   const unsigned rows = static_cast<unsigned>(ctrl->num_padded);
@@ -601,8 +601,8 @@ __global__ void __launch_bounds__(256)
     const int my_slot = lane < k ? tslots[lane] : 0;
     const uint4* src = reinterpret_cast<const uint4*>(x + static_cast<size_t>(t) * H);
     for (int c = lane; c < n16; c += 32) {
-      const uint2 lo = quant8(__ldg(src + 2 * c), s, rs);
-      const uint2 hi = quant8(__ldg(src + 2 * c + 1), s, rs);
+      const uint2 lo = quant8(__ldg(src + 2 * c), ds);
+      const uint2 hi = quant8(__ldg(src + 2 * c + 1), ds);
       const uint4 v = make_uint4(lo.x, lo.y, hi.x, hi.y);
       for (int j = 0; j < k; ++j) {
         const int slot = k <= 32 ? __shfl_sync(0xffffffffu, my_slot, j) : tslots[j];
@@ -643,7 +643,7 @@ __global__ void __launch_bounds__(256)
   const uint4 zero = make_uint4(0, 0, 0, 0);
   if (fp8) {
     const float sx = ctrl->s_x;
-    const float rsx = __frcp_rn(sx);
+    const E4m3Div dx = e4m3_div(sx);
     const int per_row = H / 16;
     const long long n = rows * per_row;
     uint4* dst = static_cast<uint4*>(xs);
@@ -654,8 +654,8 @@ __global__ void __launch_bounds__(256)
       uint4 v = zero;
       if (q < P) {
         const uint4* src = reinterpret_cast<const uint4*>(x + static_cast<size_t>(q / k) * H);
-        const uint2 lo = quant8(__ldg(src + 2 * c), sx, rsx);
-        const uint2 hi = quant8(__ldg(src + 2 * c + 1), sx, rsx);
+        const uint2 lo = quant8(__ldg(src + 2 * c), dx);
+        const uint2 hi = quant8(__ldg(src + 2 * c + 1), dx);
         v = make_uint4(lo.x, lo.y, hi.x, hi.y);
       }
       dst[i] = v;
@@ -683,7 +683,7 @@ __global__ void __launch_bounds__(256)
   pdl_wait();
   pdl_trigger();
   const float s = scale_from_amax(__uint_as_float(ctrl->amax_h));
-  const float rs = __frcp_rn(s);
+  const E4m3Div ds = e4m3_div(s);
   if (blockIdx.x == 0 && threadIdx.x == 0) ctrl->s_h = s;
   const long long n16 = static_cast<long long>(ctrl->num_padded) * I / 16;
   const float4* src = reinterpret_cast<const float4*>(h);
@@ -704,16 +704,16 @@ __global__ void __launch_bounds__(256)
       for (int c = 0; c < 4; ++c) b[c] = src[4 * i1 + c];
     }
     uint4 r;
-    r.x = quant4(a[0], s, rs);
-    r.y = quant4(a[1], s, rs);
-    r.z = quant4(a[2], s, rs);
-    r.w = quant4(a[3], s, rs);
+    r.x = quant4(a[0], ds);
+    r.y = quant4(a[1], ds);
+    r.z = quant4(a[2], ds);
+    r.w = quant4(a[3], ds);
     dst[i0] = r;
     if (i1 >= 0) {
-      r.x = quant4(b[0], s, rs);
-      r.y = quant4(b[1], s, rs);
-      r.z = quant4(b[2], s, rs);
-      r.w = quant4(b[3], s, rs);
+      r.x = quant4(b[0], ds);
+      r.y = quant4(b[1], ds);
+      r.z = quant4(b[2], ds);
+      r.w = quant4(b[3], ds);
       dst[i1] = r;
     }
   }
@@ -830,14 +830,14 @@ __global__ void __launch_bounds__(256)
   }
   __syncthreads();
   const float s = s_scale;
-  const float rs = __frcp_rn(s);
+  const E4m3Div ds = e4m3_div(s);
   if (blockIdx.x == 0 && threadIdx.x == 0) *scale = s;
   const uint4* src = reinterpret_cast<const uint4*>(x);
   uint4* dst = reinterpret_cast<uint4*>(xq);
   for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < n16;
        i += static_cast<long long>(gridDim.x) * blockDim.x) {
-    const uint2 a = quant8(__ldg(src + 2 * i), s, rs);
-    const uint2 b = quant8(__ldg(src + 2 * i + 1), s, rs);
+    const uint2 a = quant8(__ldg(src + 2 * i), ds);
+    const uint2 b = quant8(__ldg(src + 2 * i + 1), ds);
     dst[i] = make_uint4(a.x, a.y, b.x, b.y);
   }
 }

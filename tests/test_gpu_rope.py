@@ -115,3 +115,52 @@ def test_graph_replay_equals_eager(gpu_lib, T):
     ref = oracle.inv_rope_quant(b.x, b.positions, a.cos, a.sin)
     assert np.array_equal(scales.cpu().numpy(), ref["scales"])
     assert np.array_equal(codes.cpu().numpy(), ref["codes"])
+
+
+def _boundary_values(amax):
+    """fp32 values y whose quotients y / s (s = amax / 448, IEEE fp32) sit on
+    and around every E4M3 rounding boundary (the midpoints between consecutive
+    codes, subnormal ones included) and every E4M3 value, 6 ulps either side,
+    both signs; amax itself first, so that it is the head's maximum."""
+    c = np.arange(127)
+    e, m = c >> 3, c & 7
+    vals = np.where(e == 0, m * 2.0 ** -9, (1 + m / 8) * 2.0 ** (e - 7))
+    mids = (vals[:-1] + vals[1:]) / 2
+    s = np.float32(amax) / np.float32(448)
+    ys = []
+    for t in np.concatenate([mids, vals[1:]]):
+        y0 = np.array([np.float64(t) * np.float64(s)], np.float32)
+        for k in range(-6, 7):
+            y = (y0.view(np.int32) + k).view(np.float32)[0]
+            if 0 < y < amax:
+                ys += [y, -y]
+    return np.array([np.float32(amax)] + ys, np.float32)
+
+
+@pytest.mark.parametrize("T", [None, 12000])
+def test_inv_rope_quant_codes_at_e4m3_boundaries(gpu_lib, T):
+    # x pairs (1, 0) in head 0 and (0, 1) in head 1 turn the rotation into
+    # y = (c, -s) and (s, c): the caller's tables place y anywhere in fp32.
+    # T = None: one cooperative launch; 12000 tokens: the two-launch path.
+    amax = np.float32(3.7)
+    ys = _boundary_values(amax)
+    n = -(-ys.size // 8)
+    rng = np.random.default_rng(3)
+    pad = rng.uniform(-amax, amax, n * 8 - ys.size).astype(np.float32)
+    ys = np.concatenate([ys, pad]).reshape(n, 4, 2)
+    T = n if T is None else T
+    reps = -(-T // n)
+    cos = np.tile(ys[:, :, 0], (reps, 1))[:T]
+    sin = -np.tile(ys[:, :, 1], (reps, 1))[:T]
+    x = torch.zeros(T, 2, 8, dtype=torch.bfloat16)
+    x[:, 0, 0::2] = 1
+    x[:, 1, 1::2] = 1
+    pos = torch.arange(T, dtype=torch.int32)
+    cos_t, sin_t = torch.from_numpy(np.ascontiguousarray(cos)), torch.from_numpy(np.ascontiguousarray(sin))
+    ref = oracle.inv_rope_quant(x, pos, cos_t, sin_t)
+    assert ref["scales"][0] == np.float32(amax) / np.float32(448)
+    codes, scales, scratch = gpu_lib.moe_inv_rope_quant_per_head(
+        x.cuda(), pos.cuda(), cos_t.cuda(), sin_t.cuda())
+    assert gpu_lib.moe_check_status(scratch) == 0
+    assert np.array_equal(scales.cpu().numpy(), ref["scales"])
+    assert np.array_equal(codes.cpu().numpy(), ref["codes"])
