@@ -32,8 +32,9 @@ def test_reference_arm_json_line():
 
 
 def test_both_arms_print_the_same_config_dict():
-    """The driver compares the two arms' `config` objects: ours is built by
-    the same function as the reference arm's."""
+    """Both arms of bench.py describe the same workload with the same `config`
+    object, built by one function, so a comparison of the two lines can match
+    them."""
     sys.path.insert(0, ROOT)
     import bench
     from mixture_experts_layer_align_gb300 import inputs
