@@ -120,9 +120,10 @@ def test_quantize_e4m3_bit_exact(gpu_lib, T, H, scale):
 @pytest.mark.parametrize("amax_bits", [0x43E0, 0x43E2, 0x3F81, 0x4011, 0x3A83, 0x4C35])
 def test_quantize_e4m3_every_bf16_value(gpu_lib, amax_bits):
     """Every finite bf16 value of magnitude <= amax, both signs, under the scale
-    amax / 448: the kernels' multiply-by-reciprocal shortcut must give the code
-    of the correctly rounded quotient for each of them, including the values
-    whose quotient falls near an E4M3 rounding midpoint."""
+    amax / 448: the kernels' codes from two bracketing products (division only
+    where those disagree) must be the code of the correctly rounded quotient
+    for each of them, including the values whose quotient falls near an E4M3
+    rounding midpoint."""
     amax = np.array([amax_bits], np.uint16).view(np.uint16)[0]
     pos = np.arange(0, 0x7F80, dtype=np.uint16)          # +0 .. largest finite
     pos = pos[pos <= amax]
