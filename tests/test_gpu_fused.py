@@ -318,6 +318,23 @@ def test_fused_prefill_8192(gpu_lib, name):
     run_case(gpu_lib, w, a, c["top_k"], True, rows=None)
 
 
+# Far past the measured workloads: 65,536 tokens x top-8 = 524,288 pairs (512
+# alignment chunks, thousands of row tiles, rows per pair), Zipf routing, outputs
+# on 256 rows that cover every expert's segment.  bf16 weights: the oracle forms
+# only the sampled rows; FP8 with small H and I: the oracle forms h for every
+# pair, since the scale of h spans them all.
+@pytest.mark.slow
+@pytest.mark.parametrize("T,H,I,E,k,dtype", [
+    (65536, 1024, 512, 64, 8, "bf16"),
+    (65536, 256, 256, 32, 8, "fp8"),
+])
+def test_fused_far_past_the_workloads(gpu_lib, T, H, I, E, k, dtype):
+    w = inputs.make_weights(H, I, E, dtype, seed=21, device="cuda")
+    a = inputs.make_activations(T, H, E, "zipf", seed=21)
+    rows = rows_over_every_expert(a.logits, k, E, 256, seed=2)
+    run_case(gpu_lib, w, a, k, True, rows=rows)
+
+
 # (64, 256, 2176, 8, 2): single-SM kernels; (1024, 256, 512, 2, 2): 1024 rows
 # per expert, so the gate/up GEMM runs 256-token tiles on SM pairs.
 @pytest.mark.parametrize("T,H,I,E,k", [(64, 256, 2176, 8, 2), (1024, 256, 512, 2, 2)])
