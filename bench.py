@@ -264,7 +264,7 @@ def percentile(v, q):
 CALL_BLOCK = 5
 
 
-def time_calls(call, n, block=CALL_BLOCK, warm=5):
+def time_calls(call, n, block=CALL_BLOCK, warm=10):
     """Device time per call, us, of each of n blocks of `block` back-to-back
     calls: CUDA events on the current stream between blocks, none between the
     calls of a block (an event between two calls keeps the next call's first
