@@ -643,6 +643,22 @@ def run_ours(args, rank, local_rank, world):
                                          "rows in + h out, per launch",
                     "tensor_frac": round(achieved_tfs / tc_peak, 4)}
 
+    one_kernel_Ts = [T for T in Ts if launches(T) == 1]
+    if one_kernel_Ts:
+        # the whole layer runs as one kernel there, so the events between the
+        # steps of a call do not bracket the GEMMs: report that kernel against
+        # the layer's algorithmic bytes over the call time instead
+        ok_us = sum(sum(per_T_call_us[T]) for T in one_kernel_Ts)
+        ok_bytes = sum(stats[T]["layer_bytes"] for T in one_kernel_Ts) * K
+        ok_gbs = ok_bytes / (ok_us * 1e-6) / 1e9
+        roofline = {"kernel": "moe_fused_small_kernel (whole layer, one cooperative kernel)",
+                    "bound": "hbm", "achieved": round(ok_gbs, 1), "peak": hbm_peak,
+                    "peak_kind": f"{peak_kind} hbm_gbs", "unit": "GB/s",
+                    "frac": round(ok_gbs / hbm_peak, 4), "traffic": None,
+                    "algorithmic_bytes": "touched experts' weight bytes + scales + logits + x "
+                                         "in + out, per call",
+                    "calls": f"T in {one_kernel_Ts}"}
+
     tokens_per_step = sum(Ts)
     value = job_tokens_per_s(world, tokens_per_step, K, elapsed_ms)
     # per-T device time of a call without events inside it (events between
