@@ -191,20 +191,26 @@ class ClockSampler:
             rows = [r.split(", ") for r in f.read().strip().splitlines() if r.strip()]
         os.unlink(self.tmp.name)
         import datetime
-        mine = []
         uuids = {r[1].strip() for r in rows if len(r) >= 10}
         use_uuid = self.uuid if self.uuid in uuids else None
+        stamped = []
         for r in rows:
             if len(r) < 10 or (use_uuid and r[1].strip() != use_uuid):
                 continue
             try:
-                ts = datetime.datetime.strptime(r[0].strip(), "%Y/%m/%d %H:%M:%S.%f")
+                stamped.append((datetime.datetime.strptime(r[0].strip(), "%Y/%m/%d %H:%M:%S.%f"),
+                                r[1:]))
             except ValueError:
                 continue
-            if getattr(self, "t0", None) and getattr(self, "t1", None) and not (
-                    self.t0 <= ts <= self.t1):
-                continue
-            mine.append(r[1:])
+        t0, t1 = getattr(self, "t0", None), getattr(self, "t1", None)
+        window = "timed region"
+        mine = [r for ts, r in stamped if t0 is None or t1 is None or t0 <= ts <= t1]
+        if not mine and t0 is not None and t1 is not None:
+            # a timed region shorter than the sampling period: the samples
+            # taken within 100 ms of it
+            pad = datetime.timedelta(milliseconds=100)
+            mine = [r for ts, r in stamped if t0 - pad <= ts <= t1 + pad]
+            window = "within 100 ms of the timed region"
         sm, smax, reasons = [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         for r in mine:
@@ -216,9 +222,12 @@ class ClockSampler:
             for n, v in zip(names, r[5:9]):
                 if v.strip().lower() == "active":
                     reasons.add(n)
-        return {"sm_mhz": statistics.median(sm) if sm else None,
-                "sm_max_mhz": max(smax) if smax else None, "reasons": sorted(reasons),
-                "samples": len(sm)}
+        out = {"sm_mhz": statistics.median(sm) if sm else None,
+               "sm_max_mhz": max(smax) if smax else None, "reasons": sorted(reasons),
+               "samples": len(sm)}
+        if window != "timed region":
+            out["window"] = window
+        return out
 
 
 def tokens_list(args, cfg):
